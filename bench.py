@@ -1,0 +1,487 @@
+"""Benchmark of the FP8 paged KV-cache hot path on GB300.
+
+A step is one pass of the whole path over one batch of seeded synthetic input:
+kvfp8_reshape_and_cache of the batch's K/V rows into the paged FP8 cache, then
+kvfp8_paged_decode_attention of one query per sequence over that cache.  The metric is
+achieved HBM bandwidth: algorithmic bytes (each input byte read once, each output byte
+written once) divided by device time, in GB/s.
+
+Default workload: llama3_8b (32 q / 8 kv heads, head_dim 128, block 16, 64 sequences x
+4096 tokens; the step writes all 262144 context rows and decodes 64 queries).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, weak
+scaling, no collective on the data path); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {
+    "reshape_and_cache": ["fp8_paged_kv_reshape_gb300/csrc/reshape_and_cache.cu",
+                          "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
+    "paged_decode_attention": ["fp8_paged_kv_reshape_gb300/csrc/paged_decode.cu",
+                               "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
+}
+
+
+# ----------------------------------------------------------------- byte accounting
+
+def reshape_bytes(w: workloads.Workload, slot_mapping: np.ndarray, src_elem: int = 2) -> int:
+    """Algorithmic bytes of one reshape_and_cache: per valid row K+V read at src_elem bytes and
+    written at 1 byte each, plus the 8-byte slot of every row (padding rows read only it)."""
+    row = w.n_kv * w.head_dim
+    valid = int(np.count_nonzero(slot_mapping >= 0))
+    return valid * row * (2 * src_elem + 2) + 8 * int(slot_mapping.size)
+
+
+def decode_bytes(w: workloads.Workload, seq_lens: np.ndarray) -> int:
+    """Algorithmic bytes of one decode call: every cached K and V byte of every sequence, its
+    block-table entries and length, the bf16 query in and the bf16 output out."""
+    L = seq_lens.astype(np.int64)
+    row = w.n_kv * w.head_dim
+    kv = int((2 * L * row).sum())
+    tables = int((4 * np.ceil(L / w.block_size)).sum()) + 4 * L.size
+    qo = 2 * 2 * L.size * w.n_q * w.head_dim
+    return kv + tables + qo
+
+
+# ----------------------------------------------------------------- helpers
+
+def source_sha(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    rec = d.get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha") != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return int(rec["bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms in the background."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.t0 = time.time()
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(device_index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        self.samples = []
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                         reasons=parts[4:9]))
+            except ValueError:
+                continue
+
+    def summary(self):
+        if not self.samples:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        active = set()
+        for s in self.samples:
+            for n, v in zip(names, s["reasons"][1:]):
+                if v.lower() in ("active", "1"):
+                    active.add(n)
+        sm = [s["sm"] for s in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s["sm_max"] for s in self.samples),
+                "reasons": sorted(active), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- problem set-up
+
+class Problem:
+    """Device-resident inputs, caches and outputs of one workload."""
+
+    def __init__(self, name: str, device):
+        self.w = w = workloads.WORKLOADS[name]
+        self.lay = lay = workloads.make_layout(w)
+        self.device = device
+        self.ksc = workloads.scale_tensor(w.k_scale, w.scale_dtype, device)
+        self.vsc = workloads.scale_tensor(w.v_scale, w.scale_dtype, device)
+        self.kc = workloads.new_cache(lay.num_blocks, w, device)
+        self.vc = self.kc.clone()
+        ctx_k, ctx_v = workloads.make_kv(w, lay.slot_mapping.size, device)
+        self.ctx_slots = torch.from_numpy(lay.slot_mapping).to(device)
+        if w.kind == "mixed":
+            # the cache holds the context before the timed region; a step writes one new
+            # token per sequence (position len-1) and decodes
+            import fp8_paged_kv_reshape_gb300 as kv
+            kv.reshape_and_cache(ctx_k, ctx_v, self.kc, self.vc, self.ctx_slots, self.ksc, self.vsc)
+            del ctx_k, ctx_v
+            self.k, self.v = workloads.make_new_token_kv(w, lay.num_seqs, device)
+            last = lay.seq_lens.astype(np.int64) - 1
+            slots = lay.block_tables[np.arange(lay.num_seqs), last // w.block_size].astype(np.int64) \
+                * w.block_size + last % w.block_size
+            self.slots_np = slots
+        else:
+            self.k, self.v = ctx_k, ctx_v
+            self.slots_np = lay.slot_mapping
+        self.slots = torch.from_numpy(self.slots_np).to(device)
+        self.decode = w.kind != "write"
+        if self.decode:
+            self.q = workloads.make_query(w, lay.num_seqs, device)
+            self.bt = torch.from_numpy(lay.block_tables).to(device)
+            self.sl = torch.from_numpy(lay.seq_lens).to(device)
+            self.out = torch.empty_like(self.q)
+            import fp8_paged_kv_reshape_gb300 as kv
+            self.ws = torch.empty(kv.paged_decode_workspace_size(lay.num_seqs, w.n_q, w.head_dim),
+                                  dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.rs_bytes = reshape_bytes(w, self.slots_np)
+        self.dec_bytes = decode_bytes(w, lay.seq_lens) if self.decode else 0
+
+    def reshape(self):
+        import fp8_paged_kv_reshape_gb300 as kv
+        kv.reshape_and_cache(self.k, self.v, self.kc, self.vc, self.slots, self.ksc, self.vsc,
+                             status=self.status)
+
+    def attend(self):
+        import fp8_paged_kv_reshape_gb300 as kv
+        kv.paged_decode_attention(self.q, self.kc, self.vc, self.bt, self.sl, self.ksc, self.vsc,
+                                  out=self.out, workspace=self.ws, status=self.status)
+
+    def launches_per_step(self) -> int:
+        return 1 + (3 if self.decode else 0)  # reshape; plan + split-KV decode + combine
+
+    def describe(self) -> dict:
+        w, lay = self.w, self.lay
+        d = {"workload": w.name, "n_q": w.n_q, "n_kv": w.n_kv, "head_dim": w.head_dim,
+             "block_size": w.block_size, "num_seqs": lay.num_seqs,
+             "context_tokens": int(lay.seq_lens.sum()),
+             "rows_written_per_step": int(self.slots_np.size),
+             "k_scale": w.k_scale, "v_scale": w.v_scale, "scale_dtype": w.scale_dtype,
+             "step": ("reshape_and_cache(%d rows) + paged_decode_attention(%d seqs)"
+                      % (self.slots_np.size, lay.num_seqs)) if self.decode else
+                     "reshape_and_cache(%d rows)" % self.slots_np.size}
+        per_step = self.rs_bytes + self.dec_bytes
+        d["l2"] = ("inputs larger than L2 (%.2f GB of algorithmic traffic per step), no flush"
+                   % (per_step / 1e9)) if per_step > L2_BYTES else \
+            "L2 flushed between steps (a %d MB buffer written)" % (2 * L2_BYTES >> 20)
+        return d
+
+
+# ----------------------------------------------------------------- timed runs
+
+def run_ours(args, rank, world, device):
+    import fp8_paged_kv_reshape_gb300 as kv  # noqa: F401  (fails loudly without the library)
+
+    p = Problem(args.workload, device)
+    per_step = p.rs_bytes + p.dec_bytes
+    flush = None if per_step > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
+                                                         device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(evs=None):
+        if flush is not None:
+            flush.fill_(1)
+        if evs:
+            evs[0].record(stream)
+        p.reshape()
+        if evs:
+            evs[1].record(stream)
+        if p.decode:
+            p.attend()
+        if evs:
+            evs[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    assert int(p.status.item()) == 0, "device status set during warm-up"
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    # keep the GPU busy for ~0.5 s before timing so the sampler sees it under load
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize(device)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_stop.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    total_ms = t_start.elapsed_time(t_stop)
+    rs_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps if p.decode else 0.0
+    assert int(p.status.item()) == 0, "device status set during the timed steps"
+
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    e2e = run_e2e(args, p, device) if not args.no_e2e else None
+    if world > 1 and e2e is not None:
+        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+        e2e["value"] = world * per_step / (e2e["ms_per_step"] * 1e-3) / 1e9
+
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peaks()
+    kernels = {"reshape_and_cache": {"bytes_per_launch": p.rs_bytes, "ms": rs_ms,
+                                     "gbs": p.rs_bytes / (rs_ms * 1e-3) / 1e9}}
+    if p.decode:
+        kernels["paged_decode_attention"] = {"bytes_per_launch": p.dec_bytes, "ms": dec_ms,
+                                             "gbs": p.dec_bytes / (dec_ms * 1e-3) / 1e9,
+                                             "launches": 3}
+    for k in kernels.values():
+        k["frac"] = k["gbs"] / peak
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
+            "traffic": recorded_traffic(dom, args.workload),
+            "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
+    value = world * per_step * args.steps / (total_ms * 1e-3) / 1e9
+    line = {
+        "metric": "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
+        "compute": "f32 divide + E4M3 encode; fp16 mma.sync with f32 accumulate",
+        "data": "synthetic (seeded; see workloads/)",
+        "config": p.describe(), "roofline": roof, "kernels": kernels,
+        "gpu_launches": p.launches_per_step() * args.steps,
+        "clocks": sampler.summary(), "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, target_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, p: Problem, device):
+    """Same metric through the public API with host inputs: every step copies its inputs
+    from pinned host memory and reads the output back, inside the timed region."""
+    import fp8_paged_kv_reshape_gb300 as kv
+
+    hk, hv = p.k.cpu().pin_memory(), p.v.cpu().pin_memory()
+    hs = p.slots.cpu().pin_memory()
+    ins = [(hk, p.k), (hv, p.v), (hs, p.slots)]
+    if p.decode:
+        ins += [(p.q.cpu().pin_memory(), p.q), (p.bt.cpu().pin_memory(), p.bt),
+                (p.sl.cpu().pin_memory(), p.sl)]
+        hout = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = hout.numel() * hout.element_size() if p.decode else 4
+
+    hstat = torch.empty(1, dtype=torch.int32).pin_memory()
+
+    def step():
+        for h, d in ins:
+            d.copy_(h, non_blocking=True)
+        p.reshape()
+        if p.decode:
+            p.attend()
+            hout.copy_(p.out, non_blocking=True)
+        else:
+            hstat.copy_(p.status, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        step()
+    torch.cuda.synchronize(device)
+    n = max(1, min(args.steps, 20))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    ms = a.elapsed_time(b) / n
+    per_step = p.rs_bytes + p.dec_bytes
+    return {"value": per_step / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "steps": n, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------- CPU oracle legs
+
+def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_all, q):
+    """Run the CPU oracle on the given sequences of the workload: reshape their rows into
+    a cache, then decode every head of them.  Returns (seconds, algorithmic bytes)."""
+    import oracle
+
+    ks = workloads.stored_scale(w.k_scale, w.scale_dtype)
+    vs = workloads.stored_scale(w.v_scale, w.scale_dtype)
+    rows = np.nonzero(np.isin(lay.row_seq, seqs))[0] if lay.row_seq.size else np.zeros(0, int)
+    kh = k_all[torch.from_numpy(rows)].contiguous()
+    vh = v_all[torch.from_numpy(rows)].contiguous()
+    slots = lay.slot_mapping[rows]
+    kc = np.full((lay.num_blocks, w.block_size, w.n_kv, w.head_dim), workloads.SENTINEL, np.uint8)
+    vc = kc.copy()
+    decode = w.kind != "write"
+    sub_lens = lay.seq_lens[seqs]
+    t0 = time.perf_counter()
+    oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
+    if decode:
+        oracle.paged_decode_attention(q[torch.from_numpy(np.asarray(seqs))], kc, vc,
+                                      lay.block_tables[seqs], sub_lens, ks, vs)
+    dt = time.perf_counter() - t0
+    nbytes = reshape_bytes(w, slots) + (decode_bytes(w, sub_lens) if decode else 0)
+    return dt, nbytes
+
+
+def _cpu_inputs(name):
+    w = workloads.WORKLOADS[name]
+    lay = workloads.make_layout(w)
+    k, v = workloads.make_kv(w, lay.slot_mapping.size, "cpu")
+    q = workloads.make_query(w, lay.num_seqs, "cpu")
+    return w, lay, k, v, q
+
+
+def cpu_baseline(name: str, target_s: float = 12.0) -> dict:
+    """The oracle as it stands, single-threaded on the host, on a bounded sample of the same
+    workload (whole sequences: their rows written, then every head decoded)."""
+    w, lay, k, v, q = _cpu_inputs(name)
+    order = np.random.Generator(np.random.PCG64(w.seed + 5)).permutation(lay.num_seqs)
+    t, nb, used = 0.0, 0, []
+    for s in order:
+        dt, b = _oracle_sample(w, lay, [int(s)], k, v, q)
+        t += dt
+        nb += b
+        used.append(int(s))
+        if t >= target_s:
+            break
+    return {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d sequences of %s (%d tokens): oracle reshape of their rows + "
+                      "decode of all %d heads, %.1f s single-threaded"
+                      % (len(used), lay.num_seqs, name, int(lay.seq_lens[used].sum()), w.n_q, t)}
+
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores on this arm's workload and metric: each step
+    is a bounded sample (one sequence, its rows written and all heads decoded)."""
+    w, lay, k, v, q = _cpu_inputs(args.workload)
+    order = np.random.Generator(np.random.PCG64(w.seed + 6)).permutation(lay.num_seqs)
+    for i in range(args.warmup):
+        _oracle_sample(w, lay, [int(order[i % lay.num_seqs])], k, v, q)
+    t, nb = 0.0, 0
+    for i in range(args.steps):
+        dt, b = _oracle_sample(w, lay, [int(order[(args.warmup + i) % lay.num_seqs])], k, v, q)
+        t += dt
+        nb += b
+    value = nb / t / 1e9
+    sample = ("each step: 1 of %d sequences of %s, oracle reshape of its rows + decode of all "
+              "%d heads, single-threaded" % (lay.num_seqs, args.workload, w.n_q))
+    return {
+        "impl": "reference",
+        "metric": "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak",
+        "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded; see workloads/)",
+        "config": {"workload": args.workload, "n_q": w.n_q, "n_kv": w.n_kv,
+                   "head_dim": w.head_dim, "block_size": w.block_size},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3_8b", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    line = run_ours(args, rank, world, device)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,72 @@
+// Internal launch interface between the C ABI (kvfp8_api.cu) and the kernels.
+// Arguments arrive here already validated on the host.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvfp8 {
+
+struct ReshapeArgs {
+    const void *key;
+    const void *value;
+    int src_dtype;
+    int64_t key_stride;    // elements
+    int64_t value_stride;  // elements
+    int64_t num_tokens;
+    uint8_t *key_cache;
+    uint8_t *value_cache;
+    int64_t num_slots;     // num_blocks * block_size
+    int32_t row_elems;     // n_kv * head_dim, multiple of 8
+    const int64_t *slot_mapping;
+    const void *k_scale;
+    const void *v_scale;
+    int scale_dtype;
+    uint32_t *status;
+};
+
+cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
+
+// Split-KV decode attention: work is cut into 16-token chunks, the chunks of all
+// sequences are concatenated and every CTA of a fixed-size grid takes an equal
+// contiguous range of them.
+constexpr int kChunkTokens = 16;
+constexpr int kMaxDecodeCtas = 1024;
+
+struct DecodeArgs {
+    void *out;
+    const void *query;
+    const uint8_t *key_cache;
+    const uint8_t *value_cache;
+    const int32_t *block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t *seq_lens;
+    int32_t num_seqs;
+    int32_t n_q;
+    int32_t n_kv;
+    int32_t head_dim;
+    int32_t block_size;
+    int32_t num_blocks;
+    float sm_scale;  // > 0
+    const void *k_scale;
+    const void *v_scale;
+    int scale_dtype;
+    void *workspace;
+    uint32_t *status;
+};
+
+// Workspace layout, shared by the size query and the launcher.
+struct DecodeWorkspace {
+    size_t cstart_off, lse_off, o_off, total;
+};
+DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t head_dim);
+
+// Returns cudaErrorNotSupported for a shape without a kernel instance, or the first
+// CUDA error met while encoding tensor maps / launching.
+cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t stream);
+
+cudaError_t launch_dequant(void *dst, int dst_dtype, const uint8_t *src, int64_t n,
+                           const void *scale, int scale_dtype, cudaStream_t stream);
+
+}  // namespace kvfp8

@@ -1,0 +1,198 @@
+/*
+ * kvfp8 -- FP8 (OCP E4M3) paged KV cache for GB300 (sm_103a): C ABI.
+ *
+ * Three operations, all enqueued on a caller-supplied CUDA stream:
+ *   kvfp8_reshape_and_cache       bf16/f32 K,V rows -> divide by a per-layer scalar
+ *                                 scale -> E4M3 (RNE, saturating at +-448) -> scatter
+ *                                 into paged blocks at one byte per element
+ *   kvfp8_paged_decode_attention  one query per sequence reads the FP8 cache through
+ *                                 block tables, dequantizes in registers by the same
+ *                                 scales, and computes softmax(q.K^T * s) V with GQA
+ *   kvfp8_dequant                 bytes -> scale * value, for the rope-shift path
+ *                                 (dequantize, rotate, requantize)
+ *
+ * Sources, by page title and section:
+ *   [P1] llama.cpp commit 202c1a229 "llama : Add FP8 KV-cache support (#28392)"
+ *   [P2] llama.cpp compare osimons/ocp_fp8_kv (ggml-impl.h: the E4M3 codec)
+ *   [P3] vllm.cpp PR #1641 "feat(KV-FP8): W3 -- half-sized KV blocks the runner
+ *        actually serves, and a default scale that knows it was declared"
+ *
+ * Conventions common to every call
+ *   - Every pointer argument named "device" must be device memory of the current
+ *     device, 16-byte aligned (int64 slot mappings: 8-byte; int32 block tables and
+ *     sequence lengths: 4-byte).  The caller owns all memory, including workspaces;
+ *     the library allocates nothing and never synchronizes.
+ *   - Host-checkable errors (null pointers, shapes, dtypes, alignment, workspace
+ *     size) are returned before anything is enqueued; nothing is written then.
+ *   - Errors only the device can see (a scale that is zero or not finite, a slot or
+ *     block id out of range) skip the offending element/row/token and OR a bit into
+ *     the optional device word *status (KVFP8_DEV_*).  Nothing traps or spins
+ *     forever; the caller reads *status when it wants to.
+ *   - Launch failures are returned as KVFP8_ERR_CUDA.
+ *   - Cache layout (shared by K and V, which are separate arrays):
+ *       uint8 [num_blocks][block_size][n_kv][head_dim]
+ *     so token slot s = block * block_size + offset owns the n_kv*head_dim bytes at
+ *     s * n_kv * head_dim.  One byte per element: a block is exactly half the bytes
+ *     of the same block in bf16 ([P3] section "Three surfaces that no gate
+ *     reached", KVBytesPerBlock halved).
+ */
+#ifndef KVFP8_H
+#define KVFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVFP8_API __attribute__((visibility("default")))
+#else
+#define KVFP8_API
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *kvfp8_stream_t;
+
+typedef enum {
+    KVFP8_OK = 0,
+    KVFP8_ERR_NULL = 1,        /* a required pointer is null */
+    KVFP8_ERR_SHAPE = 2,       /* a size or shape is out of the supported range */
+    KVFP8_ERR_DTYPE = 3,       /* unsupported dtype code */
+    KVFP8_ERR_SCALE = 4,       /* a host-known scale is zero or not finite */
+    KVFP8_ERR_ALIGN = 5,       /* a pointer or stride breaks the 16-byte rule */
+    KVFP8_ERR_WORKSPACE = 6,   /* workspace_bytes below kvfp8_paged_decode_workspace_size */
+    KVFP8_ERR_CUDA = 7,        /* a CUDA launch or driver call failed */
+    KVFP8_ERR_UNSUPPORTED = 8  /* a valid shape this build has no kernel for */
+} kvfp8_status;
+
+typedef enum {
+    KVFP8_BF16 = 0,
+    KVFP8_F32 = 1
+} kvfp8_dtype;
+
+/* Bits ORed into the optional device status word. */
+#define KVFP8_DEV_BAD_SCALE (1u << 0) /* a device scale was zero or not finite: nothing written */
+#define KVFP8_DEV_BAD_SLOT  (1u << 1) /* a slot outside [-1, num_blocks*block_size): row skipped */
+#define KVFP8_DEV_BAD_BLOCK (1u << 2) /* a block id outside [0, num_blocks), or a seq_len above
+                                         max_blocks_per_seq*block_size (clamped) or negative */
+#define KVFP8_DEV_TIMEOUT   (1u << 3) /* a bounded wait inside a kernel gave up; output invalid */
+
+/*
+ * Quantize K and V rows and scatter them into the paged caches.
+ *
+ * Defined by: [P1] llama-graph.cpp build_attn_scale_kv_inputs (K/s_k and V/s_v via
+ * ggml_div before the cache copy) and llama-kv-cache.cpp cpy_k/cpy_v (rows stored at a
+ * per-token I64 destination index); [P2] ggml-impl.h ggml_fp32_to_f8_e4m3 (the encode);
+ * [P3] vt::ReshapeAndCacheFp8 (one shared source dtype for K and V).
+ *
+ * For every token i with slot = slot_mapping[i] != -1 and every (h, d):
+ *   key_cache  [slot][h][d] = E4M3( fp32(key  [i*key_stride   + h*head_dim + d]) / k_scale )
+ *   value_cache[slot][h][d] = E4M3( fp32(value[i*value_stride + h*head_dim + d]) / v_scale )
+ * where "/" is the IEEE float quotient (correctly rounded) and E4M3 rounds to nearest
+ * even, maps |y| >= 448 and +-inf to +-448 (0x7E/0xFE), keeps -0 as 0x80, and maps a NaN
+ * element to sign(element)|0x7F.  Bytes of slots not written keep their contents.
+ *
+ * key, value        device, src_dtype elements; token i's row starts at i*stride elements
+ * src_dtype         KVFP8_BF16 or KVFP8_F32, shared by key and value
+ * key_stride,
+ * value_stride      row strides in elements (>= n_kv*head_dim; stride*elem_size % 16 == 0)
+ * num_tokens        >= 0 (0 enqueues nothing)
+ * key_cache,
+ * value_cache       device uint8 caches, layout above
+ * num_blocks        >= 1;  block_size in [1, 1024];  n_kv >= 1;  head_dim >= 1 with
+ *                   n_kv*head_dim a multiple of 8
+ * slot_mapping      device int64 [num_tokens]; -1 = padding token (skipped)
+ * k_scale, v_scale  device scalars of scale_dtype (bf16 is widened exactly), or NULL for
+ *                   a scale of 1.  Must be finite and nonzero; negative is allowed.
+ * status            device uint32 or NULL
+ */
+KVFP8_API kvfp8_status kvfp8_reshape_and_cache(const void *key, const void *value, kvfp8_dtype src_dtype,
+                                     int64_t key_stride, int64_t value_stride, int64_t num_tokens,
+                                     uint8_t *key_cache, uint8_t *value_cache, int32_t num_blocks,
+                                     int32_t block_size, int32_t n_kv, int32_t head_dim,
+                                     const int64_t *slot_mapping, const void *k_scale,
+                                     const void *v_scale, kvfp8_dtype scale_dtype,
+                                     uint32_t *status, kvfp8_stream_t stream);
+
+/*
+ * Workspace bytes kvfp8_paged_decode_attention needs for this batch shape (split-KV
+ * partial results and the per-call chunk plan).  Pure host arithmetic.
+ */
+KVFP8_API size_t kvfp8_paged_decode_workspace_size(int32_t num_seqs, int32_t n_q, int32_t head_dim);
+
+/*
+ * Single-query (decode) paged attention over the FP8 cache.
+ *
+ * Defined by: [P1] tests/test-fp8.cpp check_fp8_attention (softmax(q.k/sqrt(d)) V over
+ * all past tokens, on K and V rounded through the cache format) and llama-graph.cpp
+ * build_attn_scale_kv_inputs / build_attn_scale_kv_output ((Q*s_k).(K/s_k) = Q.K and
+ * P*(V/s_v)*s_v = P*V: dequantizing by the same scales); [P2] ggml-impl.h
+ * ggml_f8_e4m3_to_fp32 (the decode).
+ *
+ * For every sequence b and query head h, with G = n_q / n_kv, kv = h / G,
+ * L = seq_lens[b] and token t < L stored in physical block block_tables[b][t / block_size]
+ * at row t % block_size:
+ *   s_t = sm_scale * k_scale * sum_d q[b][h][d] * E4M3dec(K[t][kv][d])
+ *   out[b][h][d] = v_scale * sum_t softmax(s)_t * E4M3dec(V[t][kv][d])   (bf16)
+ * L == 0 gives a zero row.  Accumulation is fp32; q and the decoded cache enter the
+ * tensor cores as fp16 (exact for the cache; q must lie within fp16 range).
+ *
+ * out               device bf16 [num_seqs][n_q][head_dim]
+ * query             device bf16 [num_seqs][n_q][head_dim]
+ * key_cache,
+ * value_cache       device uint8 caches, layout above
+ * block_tables      device int32 [num_seqs][max_blocks_per_seq]
+ * seq_lens          device int32 [num_seqs]
+ * num_seqs >= 0; n_q % n_kv == 0 with n_q / n_kv <= 16; head_dim in {64, 128, 256};
+ * block_size in {8, 16, 32, 64, 128, 256}; num_blocks*block_size < 2^31.  This build
+ * has kernels for n_kv <= 8 with n_kv*head_dim <= 2048, and n_q/n_kv <= 8 at
+ * head_dim 256; other valid shapes return KVFP8_ERR_UNSUPPORTED.
+ * sm_scale          <= 0 selects 1/sqrt(head_dim)
+ * k_scale, v_scale  device scalars of scale_dtype, or NULL for 1
+ * workspace         device, >= kvfp8_paged_decode_workspace_size(...) bytes, contents
+ *                   need no initialization; calls that overlap on the GPU must not share it
+ * status            device uint32 or NULL
+ */
+KVFP8_API kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const uint8_t *key_cache,
+                                          const uint8_t *value_cache, const int32_t *block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                          int32_t num_seqs, int32_t n_q, int32_t n_kv,
+                                          int32_t head_dim, int32_t block_size,
+                                          int32_t num_blocks, float sm_scale,
+                                          const void *k_scale, const void *v_scale,
+                                          kvfp8_dtype scale_dtype, void *workspace,
+                                          size_t workspace_bytes, uint32_t *status,
+                                          kvfp8_stream_t stream);
+
+/*
+ * Dequantize n E4M3 bytes: dst[i] = scale * E4M3dec(src[i]), product in fp32, then
+ * rounded to dst_dtype (bf16: round to nearest even).  NaN codes give NaN.
+ *
+ * Defined by: [P1] llama-kv-cache.cpp build_rope_shift (F8 joins the dequantize ->
+ * rope -> requantize path) and tests/test-fp8.cpp check_fp8_context_shift (stored bytes
+ * after a shift equal quantize(rope(decode(bytes)))).  Requantize with
+ * kvfp8_reshape_and_cache.  Rope is linear, so the shift path may run scale-free
+ * (scale = NULL) as long as dequant and requant agree.
+ *
+ * dst    device, dst_dtype [n];  src device uint8 [n];  n >= 0
+ * scale  device scalar of scale_dtype, or NULL for 1
+ */
+KVFP8_API kvfp8_status kvfp8_dequant(void *dst, kvfp8_dtype dst_dtype, const uint8_t *src, int64_t n,
+                           const void *scale, kvfp8_dtype scale_dtype, kvfp8_stream_t stream);
+
+/*
+ * Host-side scale check: KVFP8_OK if s is finite and nonzero, else KVFP8_ERR_SCALE.
+ * [P1] llama-context.cpp llama_init_from_model ("must be finite and nonzero").
+ */
+KVFP8_API kvfp8_status kvfp8_check_scale_host(float s);
+
+/* Static, human-readable name of a status code. */
+KVFP8_API const char *kvfp8_status_string(kvfp8_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVFP8_H */

@@ -1,0 +1,108 @@
+"""The C-ABI library loads and exports what include/kvfp8.h declares; host-side
+validation returns its documented codes before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import fp8_paged_kv_reshape_gb300 as kv
+from fp8_paged_kv_reshape_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kvfp8.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KVFP8_API\s+[\w\s\*]*?\b(kvfp8_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_functions():
+    assert _declared() == sorted(binding.ABI_FUNCTIONS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(kv.LIB_PATH)
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", kv.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (kvfp8_\w+)", out))
+    assert exported == set(_declared())  # nothing else leaks out of the ABI
+
+
+def test_status_strings_and_scale_check():
+    for code in range(9):
+        assert kv.status_string(code) not in ("", "unknown status")
+    assert kv.status_string(99) == "unknown status"
+    assert kv.check_scale_host(0.05) == binding.OK
+    assert kv.check_scale_host(-2.0) == binding.OK
+    for bad in (0.0, float("inf"), float("-inf"), float("nan")):
+        assert kv.check_scale_host(bad) == binding.ERR_SCALE
+
+
+def test_workspace_size_grows_with_the_batch():
+    a = kv.paged_decode_workspace_size(64, 32, 128)
+    b = kv.paged_decode_workspace_size(128, 32, 128)
+    assert 0 < a < b
+    assert kv.paged_decode_workspace_size(-1, 32, 128) == 0
+
+
+def _reshape(**over):
+    args = dict(key=ctypes.c_void_p(16), value=ctypes.c_void_p(16), src_dtype=binding.BF16,
+                key_stride=1024, value_stride=1024, num_tokens=4, key_cache=ctypes.c_void_p(16),
+                value_cache=ctypes.c_void_p(16), num_blocks=4, block_size=16, n_kv=8,
+                head_dim=128, slot_mapping=ctypes.c_void_p(16), k_scale=None, v_scale=None,
+                scale_dtype=binding.F32, status=None, stream=None)
+    args.update(over)
+    return kv.LIB.kvfp8_reshape_and_cache(*args.values())
+
+
+def test_reshape_host_validation():
+    assert _reshape(key=None) == binding.ERR_NULL
+    assert _reshape(slot_mapping=None) == binding.ERR_NULL
+    assert _reshape(src_dtype=7) == binding.ERR_DTYPE
+    assert _reshape(scale_dtype=5) == binding.ERR_DTYPE
+    assert _reshape(n_kv=1, head_dim=3) == binding.ERR_SHAPE        # row not a multiple of 8
+    assert _reshape(key_stride=100) == binding.ERR_SHAPE            # stride below the row
+    assert _reshape(num_blocks=0) == binding.ERR_SHAPE
+    assert _reshape(key=ctypes.c_void_p(24)) == binding.ERR_ALIGN
+    assert _reshape(key_stride=1028) == binding.ERR_ALIGN           # 2056 bytes
+    assert _reshape(slot_mapping=ctypes.c_void_p(20)) == binding.ERR_ALIGN
+    assert _reshape(num_tokens=0, key=None) == binding.OK           # nothing to do
+
+
+def _decode(**over):
+    args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16), key_cache=ctypes.c_void_p(16),
+                value_cache=ctypes.c_void_p(16), block_tables=ctypes.c_void_p(16),
+                max_blocks_per_seq=256, seq_lens=ctypes.c_void_p(16), num_seqs=4, n_q=32, n_kv=8,
+                head_dim=128, block_size=16, num_blocks=1024, sm_scale=0.0, k_scale=None,
+                v_scale=None, scale_dtype=binding.F32, workspace=ctypes.c_void_p(16),
+                workspace_bytes=1 << 30, status=None, stream=None)
+    args.update(over)
+    return kv.LIB.kvfp8_paged_decode_attention(*args.values())
+
+
+def test_decode_host_validation():
+    assert _decode(query=None) == binding.ERR_NULL
+    assert _decode(workspace=None) == binding.ERR_NULL
+    assert _decode(n_q=30) == binding.ERR_SHAPE                      # not a multiple of n_kv
+    assert _decode(n_q=8 * 17) == binding.ERR_SHAPE                  # group above 16
+    assert _decode(head_dim=96) == binding.ERR_SHAPE
+    assert _decode(block_size=12) == binding.ERR_SHAPE
+    assert _decode(n_kv=16, n_q=32) == binding.ERR_UNSUPPORTED
+    assert _decode(head_dim=256, n_q=8 * 16) == binding.ERR_UNSUPPORTED
+    assert _decode(sm_scale=float("nan")) == binding.ERR_SCALE
+    assert _decode(out=ctypes.c_void_p(8)) == binding.ERR_ALIGN
+    assert _decode(workspace_bytes=100) == binding.ERR_WORKSPACE
+    assert _decode(num_seqs=0, query=None) == binding.OK
+
+
+def test_dequant_host_validation():
+    lib = kv.LIB
+    assert lib.kvfp8_dequant(None, binding.F32, ctypes.c_void_p(16), 16, None, 0, None) == binding.ERR_NULL
+    assert lib.kvfp8_dequant(ctypes.c_void_p(16), 9, ctypes.c_void_p(16), 16, None, 0, None) == binding.ERR_DTYPE
+    assert lib.kvfp8_dequant(ctypes.c_void_p(16), binding.F32, ctypes.c_void_p(16), -1, None, 0, None) == binding.ERR_SHAPE
+    assert lib.kvfp8_dequant(ctypes.c_void_p(16), binding.F32, ctypes.c_void_p(17), 16, None, 0, None) == binding.ERR_ALIGN
+    assert lib.kvfp8_dequant(None, binding.F32, None, 0, None, 0, None) == binding.OK

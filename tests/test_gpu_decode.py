@@ -1,0 +1,212 @@
+"""kvfp8_paged_decode_attention on the GPU vs the double-precision CPU oracle.
+
+Tolerance (per element): |gpu - oracle| <= 2e-3 + 1e-2 * |oracle|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+kv = pytest.importorskip("fp8_paged_kv_reshape_gb300")
+
+
+def _case(n_q, n_kv, hd, bs, lengths, seed, ks=0.05, vs=0.04, kv_std=1.0, spare_blocks=3,
+          sdt=torch.float32, sm_scale=0.0, null_scales=False):
+    """Random inputs; the cache is written by the oracle (so decode is tested alone) and
+    copied to the GPU; returns GPU output and oracle output."""
+    g = torch.Generator().manual_seed(seed)
+    lengths = list(lengths)
+    need = [math.ceil(L / bs) for L in lengths]
+    nb = sum(need) + spare_blocks
+    perm = torch.randperm(nb, generator=g).numpy().astype(np.int32)
+    maxb = max(1, max(need) if need else 1)
+    bt = np.full((len(lengths), maxb), -1, np.int32)
+    at = 0
+    for i, n in enumerate(need):
+        bt[i, :n] = perm[at:at + n]
+        at += n
+    total = sum(lengths)
+    k = (torch.randn(total, n_kv, hd, generator=g) * kv_std).to(torch.bfloat16)
+    v = (torch.randn(total, n_kv, hd, generator=g) * kv_std).to(torch.bfloat16)
+    q = torch.randn(len(lengths), n_q, hd, generator=g).to(torch.bfloat16)
+    slots = np.concatenate([bt[i, np.arange(L) // bs].astype(np.int64) * bs + np.arange(L) % bs
+                            for i, L in enumerate(lengths)]) if total else np.zeros(0, np.int64)
+    ksf = workloads.stored_scale(ks, "f32" if sdt == torch.float32 else "bf16")
+    vsf = workloads.stored_scale(vs, "f32" if sdt == torch.float32 else "bf16")
+    if null_scales:
+        ksf = vsf = 1.0
+    kc = np.full((nb, bs, n_kv, hd), workloads.SENTINEL, np.uint8)
+    vc = kc.copy()
+    assert oracle.reshape_and_cache(k, v, kc, vc, slots, bs, ksf, vsf) == 0
+    ref, st = oracle.paged_decode_attention(q, kc, vc, bt, np.array(lengths, np.int32), ksf, vsf,
+                                            sm_scale)
+    assert st == 0
+    ksc = None if null_scales else torch.tensor([ks], dtype=sdt, device="cuda")
+    vsc = None if null_scales else torch.tensor([vs], dtype=sdt, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kv.paged_decode_attention(q.cuda(), torch.from_numpy(kc).cuda(),
+                                    torch.from_numpy(vc).cuda(), torch.from_numpy(bt).cuda(),
+                                    torch.tensor(lengths, dtype=torch.int32, device="cuda"), ksc,
+                                    vsc, sm_scale=sm_scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, ref
+
+
+CASES = [
+    # name, n_q, n_kv, head_dim, block_size, lengths
+    ("g4_ragged", 32, 8, 128, 16, [1, 15, 16, 17, 31, 33, 100, 257, 1000, 4096]),
+    ("g8", 64, 8, 128, 16, [5, 3000, 70, 2]),
+    ("g5_bs32", 40, 8, 128, 32, [16, 17, 1023, 2048, 33, 0, 64]),
+    ("g1_hd64_bs8", 4, 4, 64, 8, [1, 7, 8, 9, 200]),
+    ("g2_hd64", 4, 2, 64, 16, [17, 33, 64, 100]),
+    ("g16_nt2", 32, 2, 128, 16, [50, 500]),
+    ("g12_hd64_nt2", 24, 2, 64, 16, [77, 1234]),
+    ("g2_hd256_bs64", 4, 2, 256, 64, [65, 300, 1]),
+    ("mha_g1", 8, 8, 128, 16, [40, 129]),
+    ("bs128", 32, 8, 128, 128, [300, 1000, 129]),
+    ("bs256_g6", 24, 4, 128, 256, [700, 5]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_shapes_against_oracle(case):
+    name, n_q, n_kv, hd, bs, lengths = case
+    out, ref = _case(n_q, n_kv, hd, bs, lengths, seed=hash(name) % 1000)
+    gpu_util.assert_attention_close(out, ref, name)
+
+
+def test_one_long_sequence_spans_every_cta():
+    out, ref = _case(32, 8, 128, 16, [100_003], seed=11)
+    gpu_util.assert_attention_close(out, ref, "one_long")
+
+
+def test_many_short_sequences():
+    lengths = [1] * 2000 + [17] * 50 + [0] * 10 + [16] * 40
+    out, ref = _case(16, 4, 64, 16, lengths, seed=12)
+    gpu_util.assert_attention_close(out, ref, "many_short")
+
+
+def test_scale_variants():
+    lens = [300, 17, 1]
+    for kwargs in (dict(sdt=torch.bfloat16), dict(null_scales=True), dict(ks=-0.07, vs=0.5),
+                   dict(sm_scale=0.02), dict(ks=0.125, vs=0.25, kv_std=0.05)):
+        out, ref = _case(32, 8, 128, 16, lens, seed=13, **kwargs)
+        gpu_util.assert_attention_close(out, ref, str(kwargs))
+
+
+def test_scale_swap_would_be_caught():
+    # [P3] read-side mutation table: reading V with K's scale must leave the tolerance.
+    out, ref = _case(32, 8, 128, 16, [500, 60], seed=14, ks=0.05, vs=0.02)
+    gpu_util.assert_attention_close(out, ref)
+    g = out.float().cpu().numpy() * (0.05 / 0.02)
+    assert np.count_nonzero(np.abs(g - ref) > 2e-3 + 1e-2 * np.abs(ref)) > 0
+
+
+def test_all_empty_sequences_give_zeros():
+    out, ref = _case(32, 8, 128, 16, [0, 0, 0], seed=15)
+    assert torch.count_nonzero(out).item() == 0 and np.all(ref == 0)
+
+
+def test_deterministic():
+    w = workloads.WORKLOADS["tiny"]
+    lay = workloads.make_layout(w)
+    k, v = workloads.make_kv(w, lay.slot_mapping.size, "cuda")
+    q = workloads.make_query(w, lay.num_seqs, "cuda")
+    ksc, vsc = gpu_util.scale_pair(w)
+    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
+    vc = kc.clone()
+    kv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(lay.slot_mapping).cuda(), ksc, vsc)
+    bt = torch.from_numpy(lay.block_tables).cuda()
+    sl = torch.from_numpy(lay.seq_lens).cuda()
+    a = kv.paged_decode_attention(q, kc, vc, bt, sl, ksc, vsc)
+    b = kv.paged_decode_attention(q, kc, vc, bt, sl, ksc, vsc)
+    assert torch.equal(a, b)
+
+
+def test_bad_block_and_length_are_flagged():
+    q = torch.randn(2, 4, 64, device="cuda").to(torch.bfloat16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.uint8, device="cuda")
+    bt = torch.tensor([[0, 1], [2, 9]], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kv.paged_decode_attention(q, kc, kc, bt, torch.tensor([20, 20], dtype=torch.int32,
+                                                                device="cuda"), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kv.DEV_BAD_BLOCK
+    assert torch.isfinite(out.float()).all()
+    status.zero_()
+    kv.paged_decode_attention(q, kc, kc, bt, torch.tensor([5, 40], dtype=torch.int32,
+                                                          device="cuda"), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & kv.DEV_BAD_BLOCK
+
+
+def test_bad_device_scale_writes_nothing():
+    q = torch.randn(2, 4, 64, device="cuda").to(torch.bfloat16)
+    kc = torch.zeros(4, 16, 2, 64, dtype=torch.uint8, device="cuda")
+    bt = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32, device="cuda")
+    sl = torch.tensor([20, 30], dtype=torch.int32, device="cuda")
+    for bad in (0.0, float("nan"), float("inf")):
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.full_like(q, 7.0)
+        kv.paged_decode_attention(q, kc, kc, bt, sl, torch.tensor([bad], device="cuda"),
+                                  torch.tensor([1.0], device="cuda"), out=out, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == kv.DEV_BAD_SCALE
+        assert bool((out == 7.0).all())
+
+
+def _full_size(name, n_pairs):
+    w = workloads.WORKLOADS[name]
+    lay = workloads.make_layout(w)
+    k, v = workloads.make_kv(w, lay.slot_mapping.size, "cuda")
+    q = workloads.make_query(w, lay.num_seqs, "cuda")
+    ksc, vsc = gpu_util.scale_pair(w)
+    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
+    vc = kc.clone()
+    kv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(lay.slot_mapping).cuda(), ksc, vsc)
+    if w.kind == "mixed":  # the serving step: one new token per sequence at len-1, then decode
+        kn, vn = workloads.make_new_token_kv(w, lay.num_seqs, "cuda")
+        last = lay.seq_lens - 1
+        new_slots = lay.block_tables[np.arange(lay.num_seqs), last // w.block_size].astype(np.int64) \
+            * w.block_size + last % w.block_size
+        kv.reshape_and_cache(kn, vn, kc, vc, torch.from_numpy(new_slots).cuda(), ksc, vsc)
+        # the oracle sees the same rows: replace the context row at len-1 by the new token
+        rows = np.nonzero(lay.row_pos == (lay.seq_lens[lay.row_seq] - 1))[0]
+        k = k.clone()
+        v = v.clone()
+        k[torch.from_numpy(rows).cuda()] = kn[torch.from_numpy(lay.row_seq[rows]).cuda().long()]
+        v[torch.from_numpy(rows).cuda()] = vn[torch.from_numpy(lay.row_seq[rows]).cuda().long()]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kv.paged_decode_attention(q, kc, vc, torch.from_numpy(lay.block_tables).cuda(),
+                                    torch.from_numpy(lay.seq_lens).cuda(), ksc, vsc, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.Generator(np.random.PCG64(w.seed + 77))
+    seqs = rng.integers(0, lay.num_seqs, n_pairs)
+    seqs[0], seqs[-1] = int(np.argmax(lay.seq_lens)), int(np.argmin(lay.seq_lens))
+    pairs = [(int(b), int(h)) for b, h in zip(seqs, rng.integers(0, w.n_q, n_pairs))]
+    ks, vs = gpu_util.stored_scales(w)
+    ref = gpu_util.oracle_pairs(pairs, k, v, q, lay, w, ks, vs)
+    got = torch.stack([out[b, h] for b, h in pairs])
+    gpu_util.assert_attention_close(got, ref, name)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_full_size_llama3_8b_sampled():
+    _full_size("llama3_8b", 48)
+
+
+def test_full_size_long_context_sampled():
+    _full_size("long_context", 12)
+
+
+def test_full_size_mixed_serving_sampled():
+    _full_size("mixed_serving", 48)

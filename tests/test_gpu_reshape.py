@@ -1,0 +1,209 @@
+"""kvfp8_reshape_and_cache on the GPU vs the CPU oracle: cache bytes bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_util, pins
+
+pytestmark = pytest.mark.gpu
+
+kv = pytest.importorskip("fp8_paged_kv_reshape_gb300")
+
+SCALES = [0.05, 0.04, 0.03, 0.3, 3.7, 0.125, 0.25, 0.03125, 0.5, 1.0, -0.05, 3.0, 1e-3, 7.3e5,
+          2.0 ** -7, 2.0 ** -13, 2.0 ** -11, 2.0 ** -9, 1.0e-30, 3.0e30]
+
+
+def _run(key, value, slots, nb, bs, ks, vs, sdt=torch.float32, status=None):
+    n_kv, hd = key.shape[1], key.shape[2]
+    kc = torch.full((nb, bs, n_kv, hd), workloads.SENTINEL, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    ksc = None if ks is None else torch.tensor([ks], dtype=sdt, device="cuda")
+    vsc = None if vs is None else torch.tensor([vs], dtype=sdt, device="cuda")
+    kv.reshape_and_cache(key, value, kc, vc, slots, ksc, vsc, status=status)
+    torch.cuda.synchronize()
+    return kc.cpu().numpy(), vc.cpu().numpy()
+
+
+def _oracle(key_host, value_host, slots_np, nb, bs, n_kv, hd, ks, vs, src=oracle.BF16):
+    kc = np.full((nb, bs, n_kv, hd), workloads.SENTINEL, np.uint8)
+    vc = kc.copy()
+    st = oracle.reshape_and_cache(key_host, value_host, kc, vc, slots_np, bs,
+                                  1.0 if ks is None else ks, 1.0 if vs is None else vs,
+                                  src_dtype=src)
+    assert st == 0
+    return kc, vc
+
+
+def test_every_bf16_value_at_many_scales():
+    bits = np.arange(1 << 16, dtype=np.uint16)
+    k = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(8192, 1, 8)
+    v = torch.from_numpy(bits[::-1].view(np.int16).copy()).view(torch.bfloat16).reshape(8192, 1, 8)
+    slots = torch.arange(8192, dtype=torch.int64)
+    kd, vd, sd = k.cuda(), v.cuda(), slots.cuda()
+    for s in SCALES:
+        s32 = float(np.float32(s))
+        kc, vc = _run(kd, vd, sd, 8192, 1, s32, -s32)
+        ko, vo = _oracle(gpu_util.to_u16(k), gpu_util.to_u16(v), slots.numpy(), 8192, 1, 1, 8, s32,
+                         -s32)
+        bad = np.nonzero(kc.ravel() != ko.ravel())[0]
+        assert bad.size == 0, (s, [(hex(int(bits[i])), hex(kc.ravel()[i]), hex(ko.ravel()[i]))
+                                   for i in bad[:8]])
+        np.testing.assert_array_equal(vc, vo)
+
+
+def test_float32_source_bit_patterns():
+    rng = np.random.Generator(np.random.PCG64(21))
+    x = rng.integers(0, 1 << 32, size=1 << 21, dtype=np.uint64).astype(np.uint32).view(np.float32)
+    y = (rng.standard_normal(1 << 21) * np.exp2(rng.uniform(-14, 12, 1 << 21))).astype(np.float32)
+    special = np.array([np.nan, -np.nan, np.inf, -np.inf, 0.0, -0.0, 448.0, 464.0, -464.0, 1e-45,
+                        -1e-45, 2.0 ** -10, 3 * 2.0 ** -10, 432.0, 3.4e38, -3.4e38], np.float32)
+    neg_nan = np.array([0xFFC00000, 0xFF800001, 0x7F800001], np.uint32).view(np.float32)
+    data = np.concatenate([x, y, special, neg_nan])
+    data = np.concatenate([data, np.zeros((-data.size) % 8, np.float32)])
+    n = data.size // 8
+    key = torch.from_numpy(data.reshape(n, 1, 8).copy())
+    slots = torch.arange(n, dtype=torch.int64)
+    for s in (0.05, 0.03, 1.0, -0.125):
+        s32 = float(np.float32(s))
+        kc, vc = _run(key.cuda(), key.cuda(), slots.cuda(), n, 1, s32, s32)
+        ko, _ = _oracle(key.numpy(), key.numpy(), slots.numpy(), n, 1, 1, 8, s32, s32, src=oracle.F32)
+        bad = np.nonzero(kc.ravel() != ko.ravel())[0]
+        assert bad.size == 0, (s, [(hex(int(data.view(np.uint32)[i])), hex(kc.ravel()[i]),
+                                    hex(ko.ravel()[i])) for i in bad[:8]])
+        np.testing.assert_array_equal(vc, kc)
+
+
+def test_special_values_follow_the_page_encoder():
+    # NaN keeps its own sign, +-inf and |x/s| >= 448 saturate, -0 stays 0x80.
+    # bf16 bits: +NaN, -NaN, +inf, -inf, -0, +0, 22.375, 23.25, -30, 2^-100
+    bits = np.array([0x7FC0, 0xFFC0, 0x7F80, 0xFF80, 0x8000, 0x0000, 0x41B3, 0x41BA, 0xC1F0,
+                     0x0D80, 0, 0, 0, 0, 0, 0], np.uint16)
+    x = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16)
+    key = x.reshape(2, 1, 8).cuda()
+    kc, _ = _run(key, key, torch.arange(2, dtype=torch.int64, device="cuda"), 2, 1, 0.05, 0.05)
+    got = [int(v) for v in kc.ravel()[:10]]
+    assert got == [0x7F, 0xFF, 0x7E, 0xFE, 0x80, 0x00, 0x7E, 0x7E, 0xFE, 0x00]
+    ko, _ = _oracle(bits.reshape(2, 1, 8), bits.reshape(2, 1, 8), np.arange(2), 2, 1, 1, 8, 0.05, 0.05)
+    assert got == [int(v) for v in ko.ravel()[:10]]
+
+
+def _workload_inputs(name, **over):
+    w = workloads.WORKLOADS[name]
+    lay = workloads.make_layout(w, **over)
+    k, v = workloads.make_kv(w, lay.slot_mapping.size, device="cuda")
+    return w, lay, k, v
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill_write"])
+def test_workload_full_cache_bit_exact(name):
+    w, lay, k, v = _workload_inputs(name)
+    ks, vs = gpu_util.stored_scales(w)
+    ksc, vsc = gpu_util.scale_pair(w)
+    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
+    vc = kc.clone()
+    kv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(lay.slot_mapping).cuda(), ksc, vsc)
+    torch.cuda.synchronize()
+    ko = workloads.new_cache(lay.num_blocks, w).numpy()
+    vo = ko.copy()
+    assert oracle.reshape_and_cache(gpu_util.to_u16(k), gpu_util.to_u16(v), ko, vo,
+                                    lay.slot_mapping, w.block_size, ks, vs) == 0
+    assert np.array_equal(kc.cpu().numpy(), ko)
+    assert np.array_equal(vc.cpu().numpy(), vo)
+    if name == "prefill_write":
+        assert (lay.slot_mapping == -1).sum() > 0  # padding rows were present and skipped
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "long_context", "mixed_serving"])
+def test_workload_full_size_sampled_rows(name):
+    # Full-size prefill of the whole context; the oracle recomputes a seeded sample of rows.
+    w, lay, k, v = _workload_inputs(name)
+    ks, vs = gpu_util.stored_scales(w)
+    ksc, vsc = gpu_util.scale_pair(w)
+    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
+    vc = kc.clone()
+    slots = torch.from_numpy(lay.slot_mapping).cuda()
+    kv.reshape_and_cache(k, v, kc, vc, slots, ksc, vsc)
+    torch.cuda.synchronize()
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    rows = np.sort(rng.choice(lay.slot_mapping.size, size=4096, replace=False))
+    rows = np.unique(np.concatenate([rows, [0, lay.slot_mapping.size - 1]]))
+    ridx = torch.from_numpy(rows).cuda()
+    n = rows.size
+    ko = np.full((n, 1, w.n_kv, w.head_dim), 0, np.uint8)
+    vo = ko.copy()
+    assert oracle.reshape_and_cache(gpu_util.to_u16(k.index_select(0, ridx)),
+                                    gpu_util.to_u16(v.index_select(0, ridx)), ko, vo,
+                                    np.arange(n, dtype=np.int64), 1, ks, vs) == 0
+    flat_k = kc.view(-1, w.n_kv, w.head_dim)
+    flat_v = vc.view(-1, w.n_kv, w.head_dim)
+    sl = slots.index_select(0, ridx)
+    np.testing.assert_array_equal(flat_k.index_select(0, sl).cpu().numpy(), ko[:, 0])
+    np.testing.assert_array_equal(flat_v.index_select(0, sl).cpu().numpy(), vo[:, 0])
+    if name == "llama3_8b":  # the 0.1% outliers x20 reach the saturation code
+        assert (np.abs(ko.astype(np.int16) & 0x7F) == 0x7E).any()
+
+
+def test_strided_rows_from_a_fused_projection():
+    torch.manual_seed(3)
+    n, n_kv, hd, n_q = 300, 8, 128, 32
+    qkv = torch.randn(n, (n_q + 2 * n_kv) * hd, device="cuda").to(torch.bfloat16)
+    key = qkv[:, n_q * hd:(n_q + n_kv) * hd].view(n, n_kv, hd)
+    val = qkv[:, (n_q + n_kv) * hd:].view(n, n_kv, hd)
+    assert key.stride(0) == (n_q + 2 * n_kv) * hd
+    slots = torch.randperm(64 * 16, device="cuda")[:n].to(torch.int64)
+    kc, vc = _run(key, val, slots, 64, 16, 0.05, 0.04)
+    ko, vo = _oracle(gpu_util.to_u16(key.contiguous()), gpu_util.to_u16(val.contiguous()),
+                     slots.cpu().numpy(), 64, 16, n_kv, hd, 0.05, 0.04)
+    np.testing.assert_array_equal(kc, ko)
+    np.testing.assert_array_equal(vc, vo)
+
+
+def test_null_and_bf16_scales():
+    torch.manual_seed(4)
+    key = (torch.randn(64, 2, 64, device="cuda") * 30).to(torch.bfloat16)
+    slots = torch.arange(64, dtype=torch.int64, device="cuda")
+    kc, vc = _run(key, key, slots, 4, 16, None, None)
+    ko, vo = _oracle(gpu_util.to_u16(key), gpu_util.to_u16(key), slots.cpu().numpy(), 4, 16, 2, 64,
+                     1.0, 1.0)
+    np.testing.assert_array_equal(kc, ko)
+    b = workloads.stored_scale(0.05, "bf16")
+    kc, _ = _run(key, key, slots, 4, 16, 0.05, 0.05, sdt=torch.bfloat16)
+    ko, _ = _oracle(gpu_util.to_u16(key), gpu_util.to_u16(key), slots.cpu().numpy(), 4, 16, 2, 64, b, b)
+    np.testing.assert_array_equal(kc, ko)
+
+
+def test_device_errors_set_status_and_skip():
+    key = torch.ones(4, 1, 8, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.tensor([0, 99, -1, -7], dtype=torch.int64, device="cuda")
+    kc, _ = _run(key, key, slots, 2, 2, 0.5, 0.5, status=status)
+    assert int(status.item()) == kv.DEV_BAD_SLOT
+    flat = kc.reshape(4, 8)
+    assert np.all(flat[0] == oracle.e4m3_encode(2.0)) and np.all(flat[1:] == workloads.SENTINEL)
+    for bad in (0.0, float("inf"), float("nan")):
+        status.zero_()
+        kc, vc = _run(key, key, torch.arange(4, dtype=torch.int64, device="cuda"), 2, 2, bad, 0.5,
+                      status=status)
+        assert int(status.item()) == kv.DEV_BAD_SCALE
+        assert np.all(kc == workloads.SENTINEL) and np.all(vc == workloads.SENTINEL)
+
+
+def test_padding_rows_and_sentinel_survive():
+    torch.manual_seed(5)
+    key = torch.randn(40, 2, 64, device="cuda").to(torch.bfloat16)
+    slots = torch.full((40,), -1, dtype=torch.int64)
+    slots[::3] = torch.randperm(64)[: len(slots[::3])]
+    kc, vc = _run(key, key, slots.cuda(), 4, 16, 0.05, 0.04)
+    ko, vo = _oracle(gpu_util.to_u16(key), gpu_util.to_u16(key), slots.numpy(), 4, 16, 2, 64, 0.05, 0.04)
+    np.testing.assert_array_equal(kc, ko)
+    np.testing.assert_array_equal(vc, vo)
+    assert (kc == workloads.SENTINEL).all(axis=(2, 3)).sum() == 64 - len(slots[::3])
+
+
+def test_block_is_half_the_bf16_bytes():
+    w = workloads.WORKLOADS["llama3_8b"]
+    kc = workloads.new_cache(1, w, "cuda")
+    bf = torch.empty((1, w.block_size, w.n_kv, w.head_dim), dtype=torch.bfloat16, device="cuda")
+    assert 2 * kc.numel() * kc.element_size() == bf.numel() * bf.element_size()
