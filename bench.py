@@ -154,9 +154,9 @@ class ClockSampler:
 class Problem:
     """Device-resident inputs, caches and outputs of one workload."""
 
-    def __init__(self, name: str, device):
+    def __init__(self, name: str, device, num_seqs: int | None = None):
         self.w = w = workloads.WORKLOADS[name]
-        self.lay = lay = workloads.make_layout(w)
+        self.lay = lay = workloads.make_layout(w, num_seqs=num_seqs)
         self.device = device
         self.ksc = workloads.scale_tensor(w.k_scale, w.scale_dtype, device)
         self.vsc = workloads.scale_tensor(w.v_scale, w.scale_dtype, device)
@@ -227,7 +227,7 @@ class Problem:
 def run_ours(args, rank, world, device):
     import fp8_paged_kv_reshape_gb300 as kv  # noqa: F401  (fails loudly without the library)
 
-    p = Problem(args.workload, device)
+    p = Problem(args.workload, device, args.num_seqs)
     per_step = p.rs_bytes + p.dec_bytes
     flush = None if per_step > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
                                                          device=device)
@@ -460,6 +460,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="fewer sequences than the workload names (small profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -12,8 +12,11 @@
 //    are fewer chunks than CTAs) takes an equal contiguous, non-empty range, whatever
 //    the length mix.  A sequence that lies inside one CTA is
 //    finished there; otherwise each CTA writes a partial (normalized o, log2-sum-exp) and
-//    a combine kernel merges them.  Partial (seq, cta) pairs are stored at index seq+cta,
-//    which is unique because both grow monotonically along the chunk order.
+//    the last CTA to finish its part (an atomic arrival count per sequence) merges them.
+//    Partial (seq, cta) pairs are stored at index seq+cta, which is unique because both
+//    grow monotonically along the chunk order.  A one-CTA plan kernel computes the
+//    chunk prefix over the sequences first; the decode grid is launched as its
+//    programmatic dependent, so its prologue overlaps the plan.
 //  * One CTA = one producer warp + one consumer warp per kv head.  A 16-token chunk of a
 //    block holds all kv heads of those tokens (16 contiguous rows of n_kv*head_dim bytes),
 //    so the producer issues TMA tensor loads of [16 rows x 128 B] boxes (one per head and
@@ -74,6 +77,7 @@ struct KernelArgs {
     const void *v_scale;
     int32_t scale_dtype;
     const int32_t *cstart;
+    int32_t *counters;  // per-sequence arrivals of CTAs that finished a split part
     float *part_lse;
     float *part_o;
     uint32_t *status;
@@ -183,11 +187,20 @@ __device__ __forceinline__ uint32_t swz(int row, int cc) {
 
 // ---------------------------------------------------------------- kernels
 
-// Exclusive prefix of per-sequence chunk counts: cstart[s] = first chunk of sequence s,
-// cstart[num_seqs] = total.  One CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int32_t num_seqs,
-                                                    int32_t max_len, int32_t *cstart,
-                                                    uint32_t *status) {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Per-call plan, one CTA of 1024 threads:
+//  * cstart[s] = first chunk of sequence s (exclusive prefix of its 16-token chunk
+//    counts), cstart[num_seqs] = total;
+//  * the arrival counters of the split-KV merge are zeroed;
+//  * the output rows of empty sequences are zeroed (no CTA visits them).
+__global__ void __launch_bounds__(1024)
+plan_kernel(const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, int32_t *cstart,
+            int32_t *counters, __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
+    pdl_trigger();  // the decode grid may start its prologue; it waits for this grid's writes
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -203,6 +216,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t *seq_lens, int
                 L = L < 0 ? 0 : max_len;
             }
             n = (L + kChunkTokens - 1) / kChunkTokens;
+            counters[i] = 0;
+        }
+        unsigned empty = __ballot_sync(0xFFFFFFFFu, i < num_seqs && n == 0);
+        while (empty) {  // this warp zeroes the output rows of its empty sequences
+            const int b = __ffs(empty) - 1;
+            empty &= empty - 1;
+            uint4 *row = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(base + warp * 32 + b) *
+                                                             out_row_elems);
+            for (int k = lane; k < out_row_elems / 8; k += 32) row[k] = make_uint4(0u, 0u, 0u, 0u);
         }
         int x = n;
 #pragma unroll
@@ -236,8 +258,46 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t P) {
     return static_cast<int>(((x + 1) * P - 1) / T);
 }
 
+// Merge the partials (seq, c), c in [cf, cl], of one sequence into its bf16 output:
+// out = v_scale * sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).  Partials of other CTAs
+// are read around L1 (they were written by other SMs in this grid).
+template <int HD>
+__device__ void merge_partials(const KernelArgs &a, int seq, int cf, int cl, float sv, int tid,
+                               int nthreads) {
+    const int pairs = a.n_q * HD / 2;
+    __nv_bfloat16 *out = a.out + static_cast<int64_t>(seq) * a.n_q * HD;
+    for (int i = tid; i < pairs; i += nthreads) {
+        const int head = i / (HD / 2);
+        const int d = (i % (HD / 2)) * 2;
+        float M = -INFINITY;
+        for (int c = cf; c <= cl; ++c)
+            M = fmaxf(M, __ldcg(a.part_lse + (static_cast<int64_t>(seq) + c) * a.n_q + head));
+        float den = 0.f, acc0 = 0.f, acc1 = 0.f;
+        if (M != -INFINITY) {
+            for (int c = cf; c <= cl; ++c) {
+                const int64_t p = static_cast<int64_t>(seq) + c;
+                const float lse = __ldcg(a.part_lse + p * a.n_q + head);
+                if (lse == -INFINITY) continue;
+                const float w = ex2(lse - M);
+                const float2 v =
+                    __ldcg(reinterpret_cast<const float2 *>(a.part_o + (p * a.n_q + head) * HD + d));
+                den += w;
+                acc0 += w * v.x;
+                acc1 += w * v.y;
+            }
+        }
+        const float inv = den > 0.f ? sv / den : 0.f;
+        reinterpret_cast<uint32_t *>(out)[i] = bf16x2_from_f32(acc0 * inv, acc1 * inv);
+    }
+}
+
+// Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
+// (head_dim * query tiles <= 128); one otherwise.
 template <int HD, int NT>
-__global__ void __launch_bounds__(kThreadsMax, 1)
+constexpr int min_ctas_per_sm() { return HD * NT <= 128 ? 2 : 1; }
+
+template <int HD, int NT>
+__global__ void __launch_bounds__(kThreadsMax, min_ctas_per_sm<HD, NT>())
 decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
               const KernelArgs a) {
     constexpr int SEG = HD >= 128 ? 128 : 64;  // bytes per TMA box row (swizzle span)
@@ -254,24 +314,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     const int R = a.n_kv * HD;
     const uint32_t chunk_bytes = static_cast<uint32_t>(kChunkTokens * R);
     const uint32_t stage_bytes = 2u * chunk_bytes;
-    const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;  // full[S], empty[S]
-    ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(base_ptr + S * stage_bytes + 16 * S);
+    // mbarriers: full[S], empty[S], then seg (consumer warps done with a split segment)
+    // and info (the merge decision is published)
+    const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;
+    const uint32_t seg_bar = bars + 16 * S, info_bar = seg_bar + 8;
+    ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(base_ptr + S * stage_bytes + 16 * S + 16);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(meta + S);
-
-    const float sk = load_scale(a.k_scale, a.scale_dtype);
-    const float sv = load_scale(a.v_scale, a.scale_dtype);
-    if (!scale_ok(sk) || !scale_ok(sv)) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
-        return;
-    }
-
-    // Effective grid: at most one CTA per chunk, so that every active CTA's range is
-    // non-empty and the CTAs between a sequence's first and last one all hold a part of it.
-    const int64_t T = a.cstart[a.num_seqs];
-    const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);
-    if (static_cast<int64_t>(blockIdx.x) >= P) return;
-    const int64_t chunk_lo = static_cast<int64_t>(blockIdx.x) * T / P;
-    const int64_t chunk_hi = static_cast<int64_t>(blockIdx.x + 1) * T / P;
+    volatile int32_t *merge_info = abort_flag + 1;  // last flag, cf, cl
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -279,14 +328,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             mbar_init(bars + 8 * i, 1);
             mbar_init(bars + 8 * (S + i), a.n_kv);
         }
+        mbar_init(seg_bar, a.n_kv);
+        mbar_init(info_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == a.n_kv && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    pdl_wait();  // the plan grid's cstart/counters/zeroed rows are visible from here on
+
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        return;
+    }
+    // Effective grid: at most one CTA per chunk, so that every active CTA's range is
+    // non-empty and the CTAs between a sequence's first and last one all hold a part of it.
+    const int64_t T = a.cstart[a.num_seqs];
+    const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);
+    if (static_cast<int64_t>(blockIdx.x) >= P) return;
+    const int64_t chunk_lo = static_cast<int64_t>(blockIdx.x) * T / P;
+    const int64_t chunk_hi = static_cast<int64_t>(blockIdx.x + 1) * T / P;
     __syncthreads();
 
     if (warp == a.n_kv) {
         // ------------------------------------------------------------ producer warp
-        int64_t it = 0;
+        int64_t issued = 0;
+        int stage = 0;
+        uint32_t phase = 0;
         bool aborted = false;
         if (chunk_lo < chunk_hi) {
             // sequence holding chunk_lo: last s with cstart[s] <= chunk_lo
@@ -300,7 +372,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             int L = min(max(a.seq_lens[s], 0), a.max_len);
             int wbase = -1 << 30;  // first block-table entry held in the lane window
             int32_t win = 0;
-            for (int64_t x = chunk_lo; x < chunk_hi; ++x, ++it) {
+            for (int64_t x = chunk_lo; x < chunk_hi; ++x) {
                 while (x >= ce) {
                     ++s;
                     cs = ce;
@@ -335,10 +407,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                 if (x == chunk_lo || x == cs) flags |= kFirst;
                 if (x == chunk_hi - 1 || x == ce - 1) flags |= kLast;
                 if (cs >= chunk_lo && ce <= chunk_hi) flags |= kDirect;
-                const int stage = static_cast<int>(it % S);
-                const uint32_t parity = static_cast<uint32_t>((it / S) & 1) ^ 1u;
                 if (lane == 0) {
-                    if (!mbar_wait(bars + 8 * (S + stage), parity, abort_flag)) {
+                    if (!mbar_wait(bars + 8 * (S + stage), phase ^ 1u, abort_flag)) {
                         aborted = true;
                     } else {
                         if (!ok) {
@@ -367,13 +437,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                 }
                 aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
                 if (aborted) break;
+                ++issued;
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
         if (!aborted) {
-            const int stage = static_cast<int>(it % S);
-            const uint32_t parity = static_cast<uint32_t>((it / S) & 1) ^ 1u;
             if (lane == 0) {
-                if (!mbar_wait(bars + 8 * (S + stage), parity, abort_flag)) {
+                if (!mbar_wait(bars + 8 * (S + stage), phase ^ 1u, abort_flag)) {
                     aborted = true;
                 } else {
                     meta[stage] = ChunkMeta{0, 0, 0, kDone};
@@ -386,8 +459,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             flag(a.status, KVFP8_DEV_TIMEOUT);
             *abort_flag = 1;
             // let copies already issued land before the CTA's shared memory goes away
-            const int64_t first = it > S ? it - S : 0;
-            for (int64_t k = first; k < it; ++k) {
+            const int64_t first = issued > S ? issued - S : 0;
+            for (int64_t k = first; k < issued; ++k) {
                 const volatile int32_t never = 0;
                 mbar_wait(bars + 8 * static_cast<int>(k % S), static_cast<uint32_t>((k / S) & 1),
                           &never);
@@ -397,6 +470,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         // ------------------------------------------------------------ consumer warp
         const int kvh = warp;
         const int gid = lane >> 2, tig = lane & 3;
+        const int cthreads = a.n_kv * 32;
+        uint32_t seg_phase = 0;
         const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
 
         float o[KP][2][NT][4];
@@ -419,10 +494,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         const int vtok = (lane & 7) + ((lane >> 4) << 3);
         const int vchunk_hi = (lane >> 3) & 1;    // +1 chunk for lanes 8..15 and 24..31
 
-        for (int64_t it = 0;; ++it) {
-            const int stage = static_cast<int>(it % S);
-            const uint32_t parity = static_cast<uint32_t>((it / S) & 1);
-            if (!mbar_wait(bars + 8 * stage, parity, abort_flag)) {
+        int stage = 0;
+        uint32_t phase = 0;
+        for (;;) {
+            // every lane waits (acquire on the TMA bytes); the outcome is made warp-uniform
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bars + 8 * stage, phase, abort_flag))) {
                 if (lane == 0) {
                     flag(a.status, KVFP8_DEV_TIMEOUT);
                     *abort_flag = 1;
@@ -561,6 +637,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bars + 8 * (S + stage));
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
 
             if (mt.flags & kLast) {
                 const bool direct = (mt.flags & kDirect) != 0;
@@ -605,53 +685,46 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                         }
                     }
                 }
+                if (!direct) {
+                    // The last CTA to finish its part of this sequence merges every part.
+                    // Consumer warps meet on two mbarriers (bounded waits, never a hardware
+                    // barrier a timed-out warp could leave hanging).
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(seg_bar);
+                    if (warp == 0 && lane == 0) {
+                        // past this wait every consumer warp is done reading merge_info
+                        int last = 0, cf = 0, cl = 0;
+                        if (mbar_wait(seg_bar, seg_phase, abort_flag)) {
+                            cf = cta_of(a.cstart[mt.seq], T, P);
+                            cl = cta_of(a.cstart[mt.seq + 1] - 1, T, P);
+                            last = atomicAdd(a.counters + mt.seq, 1) == cl - cf;
+                        }
+                        merge_info[0] = last;
+                        merge_info[1] = cf;
+                        merge_info[2] = cl;
+                        mbar_arrive(info_bar);
+                    }
+                    const bool ok =
+                        __all_sync(0xFFFFFFFFu, mbar_wait(info_bar, seg_phase, abort_flag));
+                    seg_phase ^= 1u;
+                    if (!ok) {
+                        if (lane == 0) {
+                            flag(a.status, KVFP8_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                        break;
+                    }
+                    if (merge_info[0]) {
+                        __threadfence();
+                        merge_partials<HD>(a, mt.seq, merge_info[1], merge_info[2], sv,
+                                           threadIdx.x, cthreads);
+                    }
+                }
             }
         }
     }
     __syncthreads();
-}
-
-// Merge the partials of sequences that crossed CTA ranges; zero empty sequences.
-template <int HD>
-__global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
-    const float sk = load_scale(a.k_scale, a.scale_dtype);
-    const float sv = load_scale(a.v_scale, a.scale_dtype);
-    if (!scale_ok(sk) || !scale_ok(sv)) return;
-    const int s = blockIdx.x;
-    const int64_t cs = a.cstart[s], ce = a.cstart[s + 1];
-    __nv_bfloat16 *out = a.out + static_cast<int64_t>(s) * a.n_q * HD;
-    const int pairs = a.n_q * HD / 2;
-    if (ce == cs) {
-        for (int i = threadIdx.x; i < pairs; i += blockDim.x)
-            reinterpret_cast<uint32_t *>(out)[i] = 0u;
-        return;
-    }
-    const int64_t T = a.cstart[a.num_seqs];
-    const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);  // the effective grid
-    const int cf = cta_of(cs, T, P), cl = cta_of(ce - 1, T, P);
-    if (cf == cl) return;  // finished inside one CTA
-    for (int i = threadIdx.x; i < pairs; i += blockDim.x) {
-        const int head = i / (HD / 2);
-        const int d = (i % (HD / 2)) * 2;
-        float M = -INFINITY;
-        for (int c = cf; c <= cl; ++c)
-            M = fmaxf(M, a.part_lse[(static_cast<int64_t>(s) + c) * a.n_q + head]);
-        float den = 0.f, acc0 = 0.f, acc1 = 0.f;
-        if (M != -INFINITY) {
-            for (int c = cf; c <= cl; ++c) {
-                const int64_t p = static_cast<int64_t>(s) + c;
-                const float lse = a.part_lse[p * a.n_q + head];
-                if (lse == -INFINITY) continue;
-                const float w = ex2(lse - M);
-                const float2 v = *reinterpret_cast<const float2 *>(a.part_o + (p * a.n_q + head) * HD + d);
-                den += w;
-                acc0 += w * v.x;
-                acc1 += w * v.y;
-            }
-        }
-        const float inv = den > 0.f ? sv / den : 0.f;
-        reinterpret_cast<uint32_t *>(out)[i] = bf16x2_from_f32(acc0 * inv, acc1 * inv);
-    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -710,13 +783,19 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     constexpr int SEG = HD >= 128 ? 128 : 64;
     const int row_bytes = d.n_kv * HD;
     const int stage_bytes = 2 * kChunkTokens * row_bytes;
-    const int ctas_per_sm = std::max(1, env_int("KVFP8_DECODE_CTAS_PER_SM", 1));
+    const int ctas_per_sm = std::max(
+        1, std::min(min_ctas_per_sm<HD, NT>(), env_int("KVFP8_DECODE_CTAS_PER_SM", 2)));
     const int max_stages = std::max(2, std::min(8, env_int("KVFP8_DECODE_MAX_STAGES", 8)));
-    // per stage: the K and V chunk, two mbarriers and one ChunkMeta; plus the abort flag
-    // and up to 1 KiB to align the ring to the 128-byte swizzle span
-    auto smem_for = [&](int st) { return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 1024; };
+    // per stage: the K and V chunk, two mbarriers and one ChunkMeta; then two more
+    // mbarriers, the abort flag and the merge decision; up to 1 KiB to align the ring to
+    // the 128-byte swizzle span; 1 KiB of the SM's shared memory goes to each CTA's
+    // system use
+    auto smem_for = [&](int st) {
+        return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 16 + 1024;
+    };
+    const size_t sm_budget = static_cast<size_t>(smem_optin) + 1024;
     int stages = max_stages;
-    while (stages > 2 && smem_for(stages) * ctas_per_sm > static_cast<size_t>(smem_optin)) --stages;
+    while (stages > 2 && (smem_for(stages) + 1024) * ctas_per_sm > sm_budget) --stages;
     const size_t smem = smem_for(stages);
     if (smem > static_cast<size_t>(smem_optin)) return cudaErrorNotSupported;
 
@@ -759,6 +838,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.v_scale = d.v_scale;
     k.scale_dtype = d.scale_dtype;
     k.cstart = reinterpret_cast<const int32_t *>(w + ws.cstart_off);
+    k.counters = reinterpret_cast<int32_t *>(w + ws.counter_off);
     k.part_lse = reinterpret_cast<float *>(w + ws.lse_off);
     k.part_o = reinterpret_cast<float *>(w + ws.o_off);
     k.status = d.status;
@@ -767,12 +847,23 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.box_rows = box_rows;
 
     plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.num_seqs, k.max_len,
-                                        reinterpret_cast<int32_t *>(w + ws.cstart_off), d.status);
+                                        reinterpret_cast<int32_t *>(w + ws.cstart_off), k.counters,
+                                        k.out, d.n_q * HD, d.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    kern<<<num_ctas, threads, smem, stream>>>(tmk, tmv, k);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    combine_kernel<HD><<<d.num_seqs, 256, 0, stream>>>(k);
-    return cudaGetLastError();
+
+    // Programmatic dependent launch: the decode grid starts its prologue while the plan
+    // grid runs and waits (griddepcontrol.wait) before touching any data.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, k);
 }
 
 }  // namespace
@@ -782,7 +873,8 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
     const size_t parts = static_cast<size_t>(num_seqs) + kMaxDecodeCtas;
     DecodeWorkspace w;
     w.cstart_off = 0;
-    w.lse_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
+    w.counter_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
+    w.lse_off = w.counter_off + up(sizeof(int32_t) * static_cast<size_t>(num_seqs));
     w.o_off = w.lse_off + up(sizeof(float) * parts * n_q);
     w.total = w.o_off + up(sizeof(float) * parts * n_q * head_dim);
     return w;

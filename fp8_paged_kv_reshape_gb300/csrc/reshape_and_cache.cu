@@ -6,15 +6,26 @@
 // (IEEE float quotient), rounded to E4M3 (nearest even, saturating at +-448), and the
 // row's n_kv*head_dim bytes land at slot * n_kv*head_dim in the cache.
 //
-// Design: HBM-streaming.  One warp owns one (token, K|V) row; a lane moves 8 elements
-// per 16-byte load (bf16) and issues all of its loads for the row before converting,
-// so a 1 KiB-row warp keeps 2 KiB of reads in flight.  Loads are streaming (evict
-// first: every input byte is read once); each lane writes 8 contiguous output bytes so
-// a warp's stores cover whole 256-byte spans of the destination row.  Per element the
-// work is one unpack, one correctly rounded divide (__fdiv_rn) and half a packed
-// convert; a NaN check on the packed bytes sends the rare NaN/inf words to a slow path
-// that sets the sign the way the CPU reference does.
+// Design: HBM-streaming with few instructions per element.
+//  * Persistent warps.  A warp owns every (gridDim*8)-th row of the (token, K|V) row
+//    sequence, so it always handles K rows or always V rows (one scale per warp), and
+//    keeps two rows in registers: while it converts and stores one, the 16-byte
+//    streaming loads of the next are in flight; slot indices are fetched two rows ahead.
+//  * Division.  The quotient must be the IEEE float quotient x/s (correctly rounded).
+//    With y = RN(1/|s|) computed once per thread, q0 = RN(x*y) is within two ulps;
+//    one residual step q1 = q0 + (x - q0*|s|)*y (fused multiply-adds) makes it faithful
+//    and a second step gives RN(x/|s|) by Markstein's theorem (y within half an ulp of
+//    1/|s|, q1 faithful, exact FMA residual; see Markstein, "Computation of elementary
+//    functions on the IBM RISC System/6000 processor", IBM J. R&D 34(1), 1990).  The
+//    theorem's range conditions hold whenever 2^-60 <= |s| <= 2^60 and the quotient
+//    decides the byte; other scales take __fdiv_rn.  Signs are set from the operands
+//    (zeros included), and the few words whose packed codes come out as NaN (a NaN
+//    element, an infinite element, or a quotient so large that the steps overflow) get
+//    their bytes re-derived from the operands.
+//  * Rows of more than 2048 elements take a plain per-row loop.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "kvfp8_device.cuh"
 #include "kvfp8_internal.h"
@@ -22,39 +33,67 @@
 namespace kvfp8 {
 namespace {
 
-constexpr int kWarps = 8;    // rows per CTA
-constexpr int kUnroll = 4;   // 8-element groups per lane kept in flight
+constexpr int kWarps = 8;  // per CTA
 
-// Re-derive one byte of a word whose packed code came out as a NaN code: a NaN element
-// keeps its own sign (sign(x)|0x7F); an infinite quotient saturates (sign(q)|0x7E).
-__device__ __forceinline__ uint32_t fix_byte(uint32_t w, uint32_t nanmask, int i, float x, float q) {
+// The reciprocal-and-corrections divide of the header note, for |s| in [2^-60, 2^60].
+struct FastDiv {
+    float sa;    // |s|
+    float y;     // RN(1 / |s|)
+    uint32_t neg;  // 0x80808080 when s < 0 (the byte signs are flipped after packing)
+    __device__ __forceinline__ explicit FastDiv(float s) {
+        sa = fabsf(s);
+        y = __fdiv_rn(1.0f, sa);  // correctly rounded reciprocal
+        neg = signbit(s) ? 0x80808080u : 0u;
+    }
+    // RN(x / |s|) with the sign of x
+    __device__ __forceinline__ float quot(float x) const {
+        const float q0 = x * y;
+        const float r0 = fmaf(-q0, sa, x);
+        const float q1 = fmaf(r0, y, q0);
+        const float r1 = fmaf(-q1, sa, x);
+        const float q2 = fmaf(r1, y, q1);
+        // the exact quotient's sign is the sign of x: restore it (a zero may have lost it)
+        return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) |
+                               (__float_as_uint(x) & 0x80000000u));
+    }
+};
+
+__device__ __forceinline__ uint32_t fix_byte(uint32_t w, uint32_t nanmask, int i, float x,
+                                             bool s_neg) {
     if (((nanmask >> (8 * i)) & 0xFFu) == 0u) return w;
+    // a NaN element keeps its own sign; anything else that produced a NaN code is a
+    // quotient out of range, which saturates with the quotient's sign
     const uint32_t code = isnan(x) ? ((signbit(x) ? 0x80u : 0u) | 0x7Fu)
-                                   : ((signbit(q) ? 0x80u : 0u) | 0x7Eu);
+                                   : (((signbit(x) != s_neg) ? 0x80u : 0u) | 0x7Eu);
     return (w & ~(0xFFu << (8 * i))) | (code << (8 * i));
 }
 
 __device__ __noinline__ uint32_t patch_word(uint32_t w, uint32_t nanmask, float x0, float x1,
-                                            float x2, float x3, float q0, float q1, float q2,
-                                            float q3) {
-    w = fix_byte(w, nanmask, 0, x0, q0);
-    w = fix_byte(w, nanmask, 1, x1, q1);
-    w = fix_byte(w, nanmask, 2, x2, q2);
-    return fix_byte(w, nanmask, 3, x3, q3);
+                                            float x2, float x3, bool s_neg) {
+    w = fix_byte(w, nanmask, 0, x0, s_neg);
+    w = fix_byte(w, nanmask, 1, x1, s_neg);
+    w = fix_byte(w, nanmask, 2, x2, s_neg);
+    return fix_byte(w, nanmask, 3, x3, s_neg);
 }
 
-// Eight floats -> eight E4M3 bytes (x[0] in the lowest byte), divided by s.
-__device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s) {
+// Eight floats -> eight E4M3 bytes (x[0] in the lowest byte): E4M3(x / s).
+template <bool kFast>
+__device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const FastDiv &fd) {
     float q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
+    for (int i = 0; i < 8; ++i) q[i] = kFast ? fd.quot(x[i]) : __fdiv_rn(x[i], s);
     uint32_t w0 = e4m3x2_from_f32(q[0], q[1]) | (e4m3x2_from_f32(q[2], q[3]) << 16);
     uint32_t w1 = e4m3x2_from_f32(q[4], q[5]) | (e4m3x2_from_f32(q[6], q[7]) << 16);
+    if (kFast) {  // the fast quotient carries sign(x); apply sign(s)
+        w0 ^= fd.neg;
+        w1 ^= fd.neg;
+    }
     const uint32_t m0 = nan_byte_mask(w0);
     const uint32_t m1 = nan_byte_mask(w1);
     if (__builtin_expect((m0 | m1) != 0u, 0)) {
-        if (m0) w0 = patch_word(w0, m0, x[0], x[1], x[2], x[3], q[0], q[1], q[2], q[3]);
-        if (m1) w1 = patch_word(w1, m1, x[4], x[5], x[6], x[7], q[4], q[5], q[6], q[7]);
+        const bool s_neg = signbit(s);
+        if (m0) w0 = patch_word(w0, m0, x[0], x[1], x[2], x[3], s_neg);
+        if (m1) w1 = patch_word(w1, m1, x[4], x[5], x[6], x[7], s_neg);
     }
     return make_uint2(w0, w1);
 }
@@ -89,9 +128,89 @@ struct Group<true> {  // fp32: 32 bytes
     static constexpr int kBytes = 32;
 };
 
-template <bool kF32>
-__global__ void __launch_bounds__(kWarps * 32)
-reshape_and_cache_kernel(const ReshapeArgs a) {
+struct RowCtx {
+    const uint8_t *src;  // K or V base
+    uint8_t *cache;
+    int64_t stride_bytes;
+    float s;
+};
+
+__device__ __forceinline__ int64_t slot_of(const ReshapeArgs &a, int64_t row, int64_t rows) {
+    return row < rows ? __ldg(a.slot_mapping + (row >> 1)) : -1;
+}
+
+// A row is written iff its slot is in range; -1 is padding; anything else is flagged
+// (once per token, by its K row) and skipped.
+__device__ __forceinline__ bool row_ok(const ReshapeArgs &a, int64_t row, int64_t slot, int lane) {
+    if (slot >= 0 && slot < a.num_slots) return true;
+    if (slot != -1 && lane == 0 && (row & 1) == 0) flag(a.status, KVFP8_DEV_BAD_SLOT);
+    return false;
+}
+
+template <bool kF32, int U>
+__device__ __forceinline__ void load_row(Group<kF32> (&buf)[U], const RowCtx &c, int64_t row,
+                                         int groups, int lane) {
+    const uint8_t *p = c.src + (row >> 1) * c.stride_bytes;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int g = lane + 32 * u;
+        if (g < groups) buf[u].load(p + static_cast<int64_t>(g) * Group<kF32>::kBytes);
+    }
+}
+
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void store_row(const Group<kF32> (&buf)[U], const RowCtx &c,
+                                          const FastDiv &fd, int64_t slot, int row_elems,
+                                          int groups, int lane) {
+    uint8_t *dst = c.cache + slot * row_elems;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int g = lane + 32 * u;
+        if (g < groups) {
+            float x[8];
+            buf[u].unpack(x);
+            *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
+                quantize8<kFast>(x, c.s, fd);
+        }
+    }
+}
+
+__device__ __forceinline__ bool fast_range(float s) {
+    const float sa = fabsf(s);
+    return sa >= 0x1p-60f && sa <= 0x1p60f;
+}
+
+// The rows of one warp (every stride-th row from r), two in flight.
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void pipelined_rows(const ReshapeArgs &a, const RowCtx &c, int64_t r,
+                                               int64_t stride, int64_t rows, int lane) {
+    const FastDiv fd(c.s);
+    const int groups = a.row_elems >> 3;
+    Group<kF32> A[U], B[U];
+    int64_t s1 = slot_of(a, r, rows);
+    int64_t s2 = slot_of(a, r + stride, rows);
+    bool ok1 = r < rows && row_ok(a, r, s1, lane);
+    if (ok1) load_row<kF32, U>(A, c, r, groups, lane);
+    while (r < rows) {
+        int64_t rn = r + stride;
+        bool ok2 = rn < rows && row_ok(a, rn, s2, lane);
+        if (ok2) load_row<kF32, U>(B, c, rn, groups, lane);
+        int64_t s3 = slot_of(a, rn + stride, rows);
+        if (ok1) store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
+        r = rn; s1 = s2; s2 = s3; ok1 = ok2;
+        if (r >= rows) break;
+        rn = r + stride;
+        ok2 = rn < rows && row_ok(a, rn, s2, lane);
+        if (ok2) load_row<kF32, U>(A, c, rn, groups, lane);
+        s3 = slot_of(a, rn + stride, rows);
+        if (ok1) store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
+        r = rn; s1 = s2; s2 = s3; ok1 = ok2;
+    }
+}
+
+// Rows of up to 256*U elements.
+template <bool kF32, int U>
+__global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const ReshapeArgs a) {
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
     if (!scale_ok(sk) || !scale_ok(sv)) {
@@ -99,56 +218,97 @@ reshape_and_cache_kernel(const ReshapeArgs a) {
         return;
     }
     const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    if (row >= 2 * a.num_tokens) return;
-    const int64_t tok = row >> 1;
-    const bool is_v = (row & 1) != 0;
+    const int64_t rows = 2 * a.num_tokens;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;  // even
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const bool is_v = (r & 1) != 0;  // fixed for the warp: the stride is even
+    RowCtx c;
+    c.src = static_cast<const uint8_t *>(is_v ? a.value : a.key);
+    c.cache = is_v ? a.value_cache : a.key_cache;
+    c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
+    c.s = is_v ? sv : sk;
+    if (fast_range(c.s))  // uniform per warp
+        pipelined_rows<kF32, U, true>(a, c, r, stride, rows, lane);
+    else
+        pipelined_rows<kF32, U, false>(a, c, r, stride, rows, lane);
+}
 
-    const int64_t slot = __ldg(a.slot_mapping + tok);
-    if (slot == -1) return;  // padding token
-    if (slot < 0 || slot >= a.num_slots) {
-        if (lane == 0 && !is_v) flag(a.status, KVFP8_DEV_BAD_SLOT);
+// Any row length: one warp per row, groups streamed in rounds of 4 per lane.
+template <bool kF32>
+__global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const ReshapeArgs a) {
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
         return;
     }
-    const float s = is_v ? sv : sk;
-    const int64_t stride = is_v ? a.value_stride : a.key_stride;
-    const uint8_t *src = static_cast<const uint8_t *>(is_v ? a.value : a.key) +
-                         tok * stride * (kF32 ? 4 : 2);
-    uint8_t *dst = (is_v ? a.value_cache : a.key_cache) + slot * a.row_elems;
-    const int groups = a.row_elems >> 3;
-
-    for (int g0 = lane; g0 < groups; g0 += 32 * kUnroll) {
-        Group<kF32> in[kUnroll];
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = 2 * a.num_tokens;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); r < rows;
+         r += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t slot = __ldg(a.slot_mapping + (r >> 1));
+        if (!row_ok(a, r, slot, lane)) continue;
+        const bool is_v = (r & 1) != 0;
+        const float s = is_v ? sv : sk;
+        const FastDiv fd(s);
+        const bool fast = fast_range(s);
+        const uint8_t *src = static_cast<const uint8_t *>(is_v ? a.value : a.key) +
+                             (r >> 1) * (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
+        uint8_t *dst = (is_v ? a.value_cache : a.key_cache) + slot * a.row_elems;
+        const int groups = a.row_elems >> 3;
+        for (int g0 = lane; g0 < groups; g0 += 32 * 4) {
+            Group<kF32> in[4];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int g = g0 + 32 * u;
-            if (g < groups) in[u].load(src + static_cast<int64_t>(g) * Group<kF32>::kBytes);
-        }
+            for (int u = 0; u < 4; ++u)
+                if (g0 + 32 * u < groups)
+                    in[u].load(src + static_cast<int64_t>(g0 + 32 * u) * Group<kF32>::kBytes);
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const int g = g0 + 32 * u;
-            if (g < groups) {
-                float x[8];
-                in[u].unpack(x);
-                *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) = quantize8(x, s);
+            for (int u = 0; u < 4; ++u) {
+                const int g = g0 + 32 * u;
+                if (g < groups) {
+                    float x[8];
+                    in[u].unpack(x);
+                    *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
+                        fast ? quantize8<true>(x, s, fd) : quantize8<false>(x, s, fd);
+                }
             }
         }
     }
+}
+
+template <typename K>
+cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t stream) {
+    int dev = 0, sms = 0, occ = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kWarps * 32, 0)) !=
+        cudaSuccess)
+        return err;
+    const int64_t rows = 2 * a.num_tokens;
+    const int64_t want = (rows + kWarps - 1) / kWarps;
+    const int64_t full = static_cast<int64_t>(sms) * std::max(occ, 1);
+    const unsigned blocks = static_cast<unsigned>(std::min(want, full));
+    kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool kF32>
+cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
+    const int per_lane = (a.row_elems / 8 + 31) / 32;  // 8-element groups per lane
+    if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<kF32, 1>, a, stream);
+    if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<kF32, 2>, a, stream);
+    if (per_lane <= 4) return launch_persistent(reshape_pipelined_kernel<kF32, 4>, a, stream);
+    if (per_lane <= 8) return launch_persistent(reshape_pipelined_kernel<kF32, 8>, a, stream);
+    return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream) {
     if (a.num_tokens == 0) return cudaSuccess;
-    const int64_t rows = 2 * a.num_tokens;
-    const int64_t blocks = (rows + kWarps - 1) / kWarps;
-    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    const dim3 grid(static_cast<unsigned>(blocks)), block(kWarps * 32);
-    if (a.src_dtype == KVFP8_F32)
-        reshape_and_cache_kernel<true><<<grid, block, 0, stream>>>(a);
-    else
-        reshape_and_cache_kernel<false><<<grid, block, 0, stream>>>(a);
-    return cudaGetLastError();
+    return a.src_dtype == KVFP8_F32 ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
 }
 
 }  // namespace kvfp8

@@ -12,7 +12,10 @@ pytestmark = pytest.mark.gpu
 kv = pytest.importorskip("fp8_paged_kv_reshape_gb300")
 
 SCALES = [0.05, 0.04, 0.03, 0.3, 3.7, 0.125, 0.25, 0.03125, 0.5, 1.0, -0.05, 3.0, 1e-3, 7.3e5,
-          2.0 ** -7, 2.0 ** -13, 2.0 ** -11, 2.0 ** -9, 1.0e-30, 3.0e30]
+          2.0 ** -7, 2.0 ** -13, 2.0 ** -11, 2.0 ** -9, 1.0e-30, 3.0e30,
+          # edges of the reciprocal-and-corrections divide's range [2^-60, 2^60]
+          2.0 ** -60, 2.0 ** 60, 1.5 * 2.0 ** -61, 1.5 * 2.0 ** 60, 1.25 * 2.0 ** -60,
+          0.75 * 2.0 ** 61]
 
 
 def _run(key, value, slots, nb, bs, ks, vs, sdt=torch.float32, status=None):
@@ -65,7 +68,7 @@ def test_float32_source_bit_patterns():
     n = data.size // 8
     key = torch.from_numpy(data.reshape(n, 1, 8).copy())
     slots = torch.arange(n, dtype=torch.int64)
-    for s in (0.05, 0.03, 1.0, -0.125):
+    for s in (0.05, 0.03, 1.0, -0.125, 2.0 ** -60, -2.0 ** 60, 1e-25, 3.7e22):
         s32 = float(np.float32(s))
         kc, vc = _run(key.cuda(), key.cuda(), slots.cuda(), n, 1, s32, s32)
         ko, _ = _oracle(key.numpy(), key.numpy(), slots.numpy(), n, 1, 1, 8, s32, s32, src=oracle.F32)
