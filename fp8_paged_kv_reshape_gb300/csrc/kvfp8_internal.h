@@ -58,7 +58,7 @@ struct DecodeArgs {
 
 // Workspace layout, shared by the size query and the launcher.
 struct DecodeWorkspace {
-    size_t cstart_off, counter_off, lse_off, o_off, total;
+    size_t cstart_off, lse_off, o_off, total;
 };
 DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t head_dim);
 

@@ -12,11 +12,11 @@
 //    are fewer chunks than CTAs) takes an equal contiguous, non-empty range, whatever
 //    the length mix.  A sequence that lies inside one CTA is
 //    finished there; otherwise each CTA writes a partial (normalized o, log2-sum-exp) and
-//    the last CTA to finish its part (an atomic arrival count per sequence) merges them.
-//    Partial (seq, cta) pairs are stored at index seq+cta, which is unique because both
-//    grow monotonically along the chunk order.  A one-CTA plan kernel computes the
-//    chunk prefix over the sequences first; the decode grid is launched as its
-//    programmatic dependent, so its prologue overlaps the plan.
+//    a combine kernel merges them, one thread per four output dims.  Partial (seq, cta)
+//    pairs are stored at index seq+cta, which is unique because both grow monotonically
+//    along the chunk order.  A one-CTA plan kernel computes the chunk prefix over the
+//    sequences first.  Plan -> decode -> combine are chained as programmatic dependent
+//    launches, so each grid's launch and prologue overlap its predecessor.
 //  * One CTA = one producer warp + one consumer warp per kv head.  A 16-token chunk of a
 //    block holds all kv heads of those tokens (16 contiguous rows of n_kv*head_dim bytes),
 //    so the producer issues TMA tensor loads of [16 rows x 128 B] boxes (one per head and
@@ -77,7 +77,6 @@ struct KernelArgs {
     const void *v_scale;
     int32_t scale_dtype;
     const int32_t *cstart;
-    int32_t *counters;  // per-sequence arrivals of CTAs that finished a split part
     float *part_lse;
     float *part_o;
     uint32_t *status;
@@ -195,11 +194,10 @@ __device__ __forceinline__ void pdl_trigger() {
 // Per-call plan, one CTA of 1024 threads:
 //  * cstart[s] = first chunk of sequence s (exclusive prefix of its 16-token chunk
 //    counts), cstart[num_seqs] = total;
-//  * the arrival counters of the split-KV merge are zeroed;
 //  * the output rows of empty sequences are zeroed (no CTA visits them).
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, int32_t *cstart,
-            int32_t *counters, __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
+            __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
     pdl_trigger();  // the decode grid may start its prologue; it waits for this grid's writes
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
@@ -216,7 +214,6 @@ plan_kernel(const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, int32_t 
                 L = L < 0 ? 0 : max_len;
             }
             n = (L + kChunkTokens - 1) / kChunkTokens;
-            counters[i] = 0;
         }
         unsigned empty = __ballot_sync(0xFFFFFFFFu, i < num_seqs && n == 0);
         while (empty) {  // this warp zeroes the output rows of its empty sequences
@@ -258,37 +255,55 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t P) {
     return static_cast<int>(((x + 1) * P - 1) / T);
 }
 
-// Merge the partials (seq, c), c in [cf, cl], of one sequence into its bf16 output:
-// out = v_scale * sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).  Partials of other CTAs
-// are read around L1 (they were written by other SMs in this grid).
+// Merge the partials (seq, c), c in [cf, cl], of every sequence that crossed CTA ranges:
+// out = v_scale * sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).  One thread per four output
+// dims of one head; the partial loop is unrolled so its loads are in flight together.
+// Launched as a programmatic dependent of the decode grid.
 template <int HD>
-__device__ void merge_partials(const KernelArgs &a, int seq, int cf, int cl, float sv, int tid,
-                               int nthreads) {
-    const int pairs = a.n_q * HD / 2;
-    __nv_bfloat16 *out = a.out + static_cast<int64_t>(seq) * a.n_q * HD;
-    for (int i = tid; i < pairs; i += nthreads) {
-        const int head = i / (HD / 2);
-        const int d = (i % (HD / 2)) * 2;
-        float M = -INFINITY;
-        for (int c = cf; c <= cl; ++c)
-            M = fmaxf(M, __ldcg(a.part_lse + (static_cast<int64_t>(seq) + c) * a.n_q + head));
-        float den = 0.f, acc0 = 0.f, acc1 = 0.f;
-        if (M != -INFINITY) {
-            for (int c = cf; c <= cl; ++c) {
-                const int64_t p = static_cast<int64_t>(seq) + c;
-                const float lse = __ldcg(a.part_lse + p * a.n_q + head);
-                if (lse == -INFINITY) continue;
-                const float w = ex2(lse - M);
-                const float2 v =
-                    __ldcg(reinterpret_cast<const float2 *>(a.part_o + (p * a.n_q + head) * HD + d));
-                den += w;
-                acc0 += w * v.x;
-                acc1 += w * v.y;
-            }
+__global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
+    constexpr int TPH = HD / 4;     // threads per head
+    constexpr int HPB = 256 / TPH;  // heads per CTA
+    pdl_wait();                     // the decode grid's partials are visible from here on
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) return;
+    const int seq = blockIdx.x;
+    const int head = blockIdx.y * HPB + threadIdx.x / TPH;
+    if (head >= a.n_q) return;
+    const int64_t cs = a.cstart[seq], ce = a.cstart[seq + 1];
+    if (ce == cs) return;  // empty: zeroed by the plan kernel
+    const int64_t T = a.cstart[a.num_seqs];
+    const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);  // the effective grid
+    const int cf = cta_of(cs, T, P), cl = cta_of(ce - 1, T, P);
+    if (cf == cl) return;  // finished inside one CTA
+    const int k = cl - cf + 1;
+    const int d = (threadIdx.x % TPH) * 4;
+    const int64_t p0 = static_cast<int64_t>(seq) + cf;
+    const float *lse = a.part_lse + p0 * a.n_q + head;
+    const float *o = a.part_o + (p0 * a.n_q + head) * HD + d;
+    const int64_t lse_stride = a.n_q, o_stride = static_cast<int64_t>(a.n_q) * HD;
+    float M = -INFINITY;
+#pragma unroll 8
+    for (int c = 0; c < k; ++c) M = fmaxf(M, lse[c * lse_stride]);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll 8
+        for (int c = 0; c < k; ++c) {
+            const float w = ex2(lse[c * lse_stride] - M);  // 0 for an empty part (-inf)
+            const float4 v = *reinterpret_cast<const float4 *>(o + c * o_stride);
+            den += w;
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
-        const float inv = den > 0.f ? sv / den : 0.f;
-        reinterpret_cast<uint32_t *>(out)[i] = bf16x2_from_f32(acc0 * inv, acc1 * inv);
     }
+    const float inv = den > 0.f ? sv / den : 0.f;
+    uint2 r;
+    r.x = bf16x2_from_f32(acc.x * inv, acc.y * inv);
+    r.y = bf16x2_from_f32(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(a.out + (static_cast<int64_t>(seq) * a.n_q + head) * HD + d) = r;
 }
 
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
@@ -314,13 +329,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     const int R = a.n_kv * HD;
     const uint32_t chunk_bytes = static_cast<uint32_t>(kChunkTokens * R);
     const uint32_t stage_bytes = 2u * chunk_bytes;
-    // mbarriers: full[S], empty[S], then seg (consumer warps done with a split segment)
-    // and info (the merge decision is published)
-    const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;
-    const uint32_t seg_bar = bars + 16 * S, info_bar = seg_bar + 8;
-    ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(base_ptr + S * stage_bytes + 16 * S + 16);
+    const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;  // full[S], empty[S]
+    ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(base_ptr + S * stage_bytes + 16 * S);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(meta + S);
-    volatile int32_t *merge_info = abort_flag + 1;  // last flag, cf, cl
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -328,8 +339,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             mbar_init(bars + 8 * i, 1);
             mbar_init(bars + 8 * (S + i), a.n_kv);
         }
-        mbar_init(seg_bar, a.n_kv);
-        mbar_init(info_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -337,7 +346,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
-    pdl_wait();  // the plan grid's cstart/counters/zeroed rows are visible from here on
+    pdl_wait();     // the plan grid's cstart and zeroed rows are visible from here on
+    pdl_trigger();  // let the combine grid get launched; it waits for this grid to finish
 
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
@@ -470,8 +480,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         // ------------------------------------------------------------ consumer warp
         const int kvh = warp;
         const int gid = lane >> 2, tig = lane & 3;
-        const int cthreads = a.n_kv * 32;
-        uint32_t seg_phase = 0;
         const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
 
         float o[KP][2][NT][4];
@@ -685,42 +693,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                         }
                     }
                 }
-                if (!direct) {
-                    // The last CTA to finish its part of this sequence merges every part.
-                    // Consumer warps meet on two mbarriers (bounded waits, never a hardware
-                    // barrier a timed-out warp could leave hanging).
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(seg_bar);
-                    if (warp == 0 && lane == 0) {
-                        // past this wait every consumer warp is done reading merge_info
-                        int last = 0, cf = 0, cl = 0;
-                        if (mbar_wait(seg_bar, seg_phase, abort_flag)) {
-                            cf = cta_of(a.cstart[mt.seq], T, P);
-                            cl = cta_of(a.cstart[mt.seq + 1] - 1, T, P);
-                            last = atomicAdd(a.counters + mt.seq, 1) == cl - cf;
-                        }
-                        merge_info[0] = last;
-                        merge_info[1] = cf;
-                        merge_info[2] = cl;
-                        mbar_arrive(info_bar);
-                    }
-                    const bool ok =
-                        __all_sync(0xFFFFFFFFu, mbar_wait(info_bar, seg_phase, abort_flag));
-                    seg_phase ^= 1u;
-                    if (!ok) {
-                        if (lane == 0) {
-                            flag(a.status, KVFP8_DEV_TIMEOUT);
-                            *abort_flag = 1;
-                        }
-                        break;
-                    }
-                    if (merge_info[0]) {
-                        __threadfence();
-                        merge_partials<HD>(a, mt.seq, merge_info[1], merge_info[2], sv,
-                                           threadIdx.x, cthreads);
-                    }
-                }
             }
         }
     }
@@ -786,13 +758,10 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     const int ctas_per_sm = std::max(
         1, std::min(min_ctas_per_sm<HD, NT>(), env_int("KVFP8_DECODE_CTAS_PER_SM", 2)));
     const int max_stages = std::max(2, std::min(8, env_int("KVFP8_DECODE_MAX_STAGES", 8)));
-    // per stage: the K and V chunk, two mbarriers and one ChunkMeta; then two more
-    // mbarriers, the abort flag and the merge decision; up to 1 KiB to align the ring to
-    // the 128-byte swizzle span; 1 KiB of the SM's shared memory goes to each CTA's
-    // system use
-    auto smem_for = [&](int st) {
-        return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 16 + 1024;
-    };
+    // per stage: the K and V chunk, two mbarriers and one ChunkMeta; then the abort flag
+    // and up to 1 KiB to align the ring to the 128-byte swizzle span; 1 KiB of the SM's
+    // shared memory goes to each CTA's system use
+    auto smem_for = [&](int st) { return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 1024; };
     const size_t sm_budget = static_cast<size_t>(smem_optin) + 1024;
     int stages = max_stages;
     while (stages > 2 && (smem_for(stages) + 1024) * ctas_per_sm > sm_budget) --stages;
@@ -838,7 +807,6 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.v_scale = d.v_scale;
     k.scale_dtype = d.scale_dtype;
     k.cstart = reinterpret_cast<const int32_t *>(w + ws.cstart_off);
-    k.counters = reinterpret_cast<int32_t *>(w + ws.counter_off);
     k.part_lse = reinterpret_cast<float *>(w + ws.lse_off);
     k.part_o = reinterpret_cast<float *>(w + ws.o_off);
     k.status = d.status;
@@ -847,8 +815,8 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.box_rows = box_rows;
 
     plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.num_seqs, k.max_len,
-                                        reinterpret_cast<int32_t *>(w + ws.cstart_off), k.counters,
-                                        k.out, d.n_q * HD, d.status);
+                                        reinterpret_cast<int32_t *>(w + ws.cstart_off), k.out,
+                                        d.n_q * HD, d.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     // Programmatic dependent launch: the decode grid starts its prologue while the plan
@@ -863,7 +831,14 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmk, tmv, k);
+    if ((err = cudaLaunchKernelEx(&cfg, kern, tmk, tmv, k)) != cudaSuccess) return err;
+
+    constexpr int kHeadsPerCta = 256 / (HD / 4);
+    cudaLaunchConfig_t ccfg = cfg;
+    ccfg.gridDim = dim3(d.num_seqs, (d.n_q + kHeadsPerCta - 1) / kHeadsPerCta);
+    ccfg.blockDim = dim3(256);
+    ccfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&ccfg, combine_kernel<HD>, k);
 }
 
 }  // namespace
@@ -873,8 +848,7 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
     const size_t parts = static_cast<size_t>(num_seqs) + kMaxDecodeCtas;
     DecodeWorkspace w;
     w.cstart_off = 0;
-    w.counter_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
-    w.lse_off = w.counter_off + up(sizeof(int32_t) * static_cast<size_t>(num_seqs));
+    w.lse_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
     w.o_off = w.lse_off + up(sizeof(float) * parts * n_q);
     w.total = w.o_off + up(sizeof(float) * parts * n_q * head_dim);
     return w;
