@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     check_scale_host,
     dequant,
     paged_decode_attention,
+    paged_decode_attention_noalloc,
     paged_decode_workspace_size,
     reshape_and_cache,
     status_string,

@@ -15,7 +15,8 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libkvfp8.so")
 HEADER = os.path.join(ROOT, "include", "kvfp8.h")
 
-SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "dequant.cu"]
+SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "dequant.cu",
+           "decode_noalloc.cu"]
 DEPS = ["kvfp8_device.cuh", "kvfp8_internal.h"]
 
 NVCC_FLAGS = [

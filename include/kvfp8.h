@@ -167,6 +167,35 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query
                                           kvfp8_stream_t stream);
 
 /*
+ * Size in bytes of the fixed device scratch array that
+ * kvfp8_paged_decode_attention_noalloc uses in place of a caller workspace (32 MiB).
+ */
+#define KVFP8_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * kvfp8_paged_decode_attention for callers that cannot allocate device memory: same
+ * arguments, outputs and errors, minus the workspace.  The source pages have no
+ * counterpart of this call; it exists for callers that cannot call cudaMalloc (a
+ * plug-in whose host runtime owns every device allocation, a serving loop that must not
+ * allocate once it runs, a caller with no allocator of its own).
+ *
+ * The split-KV scratch is a fixed device array of KVFP8_NOALLOC_SCRATCH_BYTES inside this
+ * library, held by every GPU that loads the library until the process exits.  A batch
+ * whose kvfp8_paged_decode_workspace_size exceeds it returns KVFP8_ERR_WORKSPACE before
+ * anything is enqueued.  The call allocates nothing.  The first call on each device looks
+ * up the array's device address (with that device current); make that first call
+ * before any stream capture.  All calls share the array, which keeps the last call's
+ * contents (nothing in it needs to start at zero); calls that overlap on the GPU race on
+ * it, so order them on one stream or serialize them.
+ */
+KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
+    void *out, const void *query, const uint8_t *key_cache, const uint8_t *value_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+    int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float sm_scale, const void *k_scale, const void *v_scale,
+    kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream);
+
+/*
  * Dequantize n E4M3 bytes: dst[i] = scale * E4M3dec(src[i]), product in fp32, then
  * rounded to dst_dtype (bf16: round to nearest even).  NaN codes give NaN.
  *
