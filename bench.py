@@ -67,6 +67,20 @@ def decode_bytes(w: workloads.Workload, seq_lens: np.ndarray) -> int:
 
 # ----------------------------------------------------------------- helpers
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The maximum of x over all ranks (the job's time is its slowest rank's)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the bytes every rank processed over the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 def source_sha(files) -> str:
     h = hashlib.sha256()
     for f in files:
@@ -276,17 +290,11 @@ def run_ours(args, rank, world, device):
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps if p.decode else 0.0
     assert int(p.status.item()) == 0, "device status set during the timed steps"
 
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-
+    total_ms = max_over_ranks(total_ms, world, device)
     e2e = run_e2e(args, p, device) if not args.no_e2e else None
-    if world > 1 and e2e is not None:
-        t = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(t.item())
-        e2e["value"] = world * per_step / (e2e["ms_per_step"] * 1e-3) / 1e9
+    if e2e is not None:
+        e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, device)
+        e2e["value"] = whole_job_gbs(per_step, 1, world, e2e["ms_per_step"])
 
     if rank != 0:
         return None
@@ -304,7 +312,7 @@ def run_ours(args, rank, world, device):
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
             "traffic": recorded_traffic(dom, args.workload),
             "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
-    value = world * per_step * args.steps / (total_ms * 1e-3) / 1e9
+    value = whole_job_gbs(per_step, args.steps, world, total_ms)
     line = {
         "metric": "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

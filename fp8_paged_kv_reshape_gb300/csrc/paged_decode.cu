@@ -257,47 +257,52 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t P) {
 
 // Merge the partials (seq, c), c in [cf, cl], of every sequence that crossed CTA ranges:
 // out = v_scale * sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M).  One thread per four output
-// dims of one head; the partial loop is unrolled so its loads are in flight together.
+// dims of one head.  A single pass with a running maximum: the loads of all partials are
+// independent of one another (the loop is unrolled), so they are in flight together.
 // Launched as a programmatic dependent of the decode grid.
 template <int HD>
 __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
     constexpr int TPH = HD / 4;     // threads per head
     constexpr int HPB = 256 / TPH;  // heads per CTA
-    pdl_wait();                     // the decode grid's partials are visible from here on
-    const float sk = load_scale(a.k_scale, a.scale_dtype);
-    const float sv = load_scale(a.v_scale, a.scale_dtype);
-    if (!scale_ok(sk) || !scale_ok(sv)) return;
     const int seq = blockIdx.x;
     const int head = blockIdx.y * HPB + threadIdx.x / TPH;
-    if (head >= a.n_q) return;
-    const int64_t cs = a.cstart[seq], ce = a.cstart[seq + 1];
+    const int d = (threadIdx.x % TPH) * 4;
+    pdl_wait();  // the decode grid's partials are visible from here on
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    const int64_t cs = a.cstart[seq], ce = a.cstart[seq + 1], T = a.cstart[a.num_seqs];
+    if (!scale_ok(sk) || !scale_ok(sv) || head >= a.n_q) return;
     if (ce == cs) return;  // empty: zeroed by the plan kernel
-    const int64_t T = a.cstart[a.num_seqs];
     const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);  // the effective grid
     const int cf = cta_of(cs, T, P), cl = cta_of(ce - 1, T, P);
     if (cf == cl) return;  // finished inside one CTA
     const int k = cl - cf + 1;
-    const int d = (threadIdx.x % TPH) * 4;
     const int64_t p0 = static_cast<int64_t>(seq) + cf;
     const float *lse = a.part_lse + p0 * a.n_q + head;
     const float *o = a.part_o + (p0 * a.n_q + head) * HD + d;
     const int64_t lse_stride = a.n_q, o_stride = static_cast<int64_t>(a.n_q) * HD;
-    float M = -INFINITY;
-#pragma unroll 8
-    for (int c = 0; c < k; ++c) M = fmaxf(M, lse[c * lse_stride]);
-    float den = 0.f;
+    float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
 #pragma unroll 8
-        for (int c = 0; c < k; ++c) {
-            const float w = ex2(lse[c * lse_stride] - M);  // 0 for an empty part (-inf)
-            const float4 v = *reinterpret_cast<const float4 *>(o + c * o_stride);
-            den += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+    for (int c = 0; c < k; ++c) {
+        const float l = lse[c * lse_stride];
+        const float4 v = *reinterpret_cast<const float4 *>(o + c * o_stride);
+        if (l == -INFINITY) continue;  // a part with no valid token
+        if (l > M) {                   // rescale what has been summed so far
+            const float r = ex2(M - l);  // 0 while M is still -inf
+            den *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            M = l;
         }
+        const float w = ex2(l - M);
+        den += w;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
     }
     const float inv = den > 0.f ? sv / den : 0.f;
     uint2 r;

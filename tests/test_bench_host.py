@@ -1,0 +1,89 @@
+"""Host-side logic of bench.py on CPU: the multi-rank aggregation under a world_size-2
+gloo group, and the reference arm (the CPU oracle) on the tiny workload."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, times, out_q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    import bench
+
+    mx = bench.max_over_ranks(times[rank], world, torch.device("cpu"))
+    torch.distributed.barrier()
+    out_q.put((rank, mx, bench.whole_job_gbs(1_000_000, 10, world, mx)))
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_value_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    times = [3.0, 5.0]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, times, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, mx, val in res:
+        assert mx == 5.0  # the slowest rank's time
+        assert val == pytest.approx(2 * 1_000_000 * 10 / 5e-3 / 1e9)
+
+
+def _bench(*args, env=None):
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args],
+                          capture_output=True, text=True, env=e, timeout=600)
+
+
+def test_reference_arm_prints_one_line_with_the_contract_keys():
+    r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3")
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "tiny"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+               env={"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_byte_accounting():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["llama3_8b"]
+    slots = np.array([0, -1, 5, 7], np.int64)
+    assert bench.reshape_bytes(w, slots) == 3 * 1024 * 6 + 8 * 4
+    lens = np.array([16, 17, 0], np.int32)
+    per = bench.decode_bytes(w, lens)
+    assert per == 2 * 33 * 1024 + 4 * (1 + 2 + 0) + 4 * 3 + 2 * 2 * 3 * 32 * 128
