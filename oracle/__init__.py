@@ -54,6 +54,12 @@ def _load():
         lib.kvo_reshape_and_cache.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P, i32, i32,
                                               i32, i32, P, f32, f32]
         lib.kvo_reshape_and_cache.restype = u32
+        lib.kvo_rope.argtypes = [P, i32, i32, ctypes.c_int, P]
+        lib.kvo_rope.restype = None
+        lib.kvo_rope_reshape_and_cache.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P, i32,
+                                                   i32, i32, i32, P, P, P, i64, i32, ctypes.c_int,
+                                                   f32, f32]
+        lib.kvo_rope_reshape_and_cache.restype = u32
         lib.kvo_dequant.argtypes = [P, ctypes.c_int, P, i64, ctypes.c_int, f32]
         lib.kvo_dequant.restype = None
         lib.kvo_paged_decode_attention.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
@@ -151,6 +157,42 @@ def reshape_and_cache(key, value, key_cache: np.ndarray, value_cache: np.ndarray
     return int(_load().kvo_reshape_and_cache(
         _ptr(k), _ptr(v), src_dtype, ks, vs, num_tokens, _ptr(key_cache), _ptr(value_cache),
         num_blocks, block_size, n_kv, hd, _ptr(slots), float(np.float32(k_scale)),
+        float(np.float32(v_scale))))
+
+
+def rope(x: np.ndarray, cos_sin_row: np.ndarray, rot: int, neox: bool) -> np.ndarray:
+    """Rotate one head vector (float32) by one table row; returns a new array."""
+    v = np.ascontiguousarray(x, dtype=np.float32).copy()
+    cs = np.ascontiguousarray(cos_sin_row, dtype=np.float32)
+    assert cs.size >= rot and v.size >= rot
+    _load().kvo_rope(_ptr(v), v.size, rot, 1 if neox else 0, _ptr(cs))
+    return v
+
+
+def rope_reshape_and_cache(key, value, key_cache: np.ndarray, value_cache: np.ndarray,
+                           slot_mapping: np.ndarray, positions: np.ndarray, cos_sin: np.ndarray,
+                           rot: int, neox: bool, block_size: int, k_scale: float, v_scale: float,
+                           src_dtype: int = BF16) -> int:
+    """Rope on K, then quantize-and-scatter K and V in place; returns the status bits.
+    cos_sin: float32 [max_pos, rot] (cos then sin halves)."""
+    if src_dtype == BF16:
+        k = _as_u16(key)
+        v = _as_u16(value)
+    else:
+        k = np.ascontiguousarray(key, dtype=np.float32)
+        v = np.ascontiguousarray(value, dtype=np.float32)
+    num_blocks, bs, n_kv, hd = key_cache.shape
+    assert bs == block_size and value_cache.shape == key_cache.shape
+    cs = np.ascontiguousarray(cos_sin, dtype=np.float32)
+    assert cs.ndim == 2 and cs.shape[1] == rot
+    num_tokens = k.shape[0]
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    assert slots.shape[0] == num_tokens and pos.shape[0] == num_tokens
+    return int(_load().kvo_rope_reshape_and_cache(
+        _ptr(k), _ptr(v), src_dtype, n_kv * hd, n_kv * hd, num_tokens, _ptr(key_cache),
+        _ptr(value_cache), num_blocks, block_size, n_kv, hd, _ptr(slots), _ptr(pos), _ptr(cs),
+        cs.shape[0], rot, 1 if neox else 0, float(np.float32(k_scale)),
         float(np.float32(v_scale))))
 
 

@@ -229,6 +229,75 @@ uint32_t kvo_reshape_and_cache(const void *key, const void *value, int src_dtype
     return status;
 }
 
+/* Rotary position embedding of one head's vector, in float.
+ * [P1] llama-graph.cpp build_attn: "expand k later to enable rope fusion which directly
+ * writes into k-v cache" -- the fused form rotates K and stores it in one pass.
+ * READING (the pages leave rope to the model): the caller supplies the table
+ * cos_sin[pos][0..rot/2) = cos, cos_sin[pos][rot/2..rot) = sin (fp32), and each pair
+ * (a, b) of the first rot dims becomes
+ *     a' = a*cos - b*sin,   b' = a*sin + b*cos
+ * with every product and sum rounded to float in that order (no fused multiply-add).
+ * neox != 0 pairs dim i with dim i + rot/2 (GPT-NeoX layout); neox == 0 pairs 2i with
+ * 2i+1 (GPT-J layout).  Pair i uses cos/sin entry i.  Dims >= rot pass through. */
+void kvo_rope(float *x, int32_t head_dim, int32_t rot, int neox, const float *cs_row)
+{
+    const int32_t half = rot / 2;
+    for (int32_t i = 0; i < half; ++i) {
+        const int32_t ia = neox ? i : 2 * i;
+        const int32_t ib = neox ? i + half : 2 * i + 1;
+        const float c = cs_row[i], sn = cs_row[half + i];
+        const float a = x[ia], b = x[ib];
+        const float ac = a * c, bs = b * sn, as = a * sn, bc = b * c;
+        x[ia] = ac - bs;
+        x[ib] = as + bc;
+    }
+    (void)head_dim;
+}
+
+/* reshape_and_cache with rope applied to K first (positions[i] selects the table row);
+ * V is stored as in kvo_reshape_and_cache.  Status bits as there; a position outside
+ * [0, max_pos) flags KVO_BAD_SLOT and skips the row. */
+uint32_t kvo_rope_reshape_and_cache(const void *key, const void *value, int src_dtype,
+                                    int64_t key_stride, int64_t value_stride,
+                                    int64_t num_tokens, uint8_t *key_cache,
+                                    uint8_t *value_cache, int32_t num_blocks,
+                                    int32_t block_size, int32_t n_kv, int32_t head_dim,
+                                    const int64_t *slot_mapping, const int64_t *positions,
+                                    const float *cos_sin, int64_t max_pos, int32_t rot,
+                                    int neox, float k_scale, float v_scale)
+{
+    uint32_t status = 0;
+    if (!kvo_scale_ok(k_scale) || !kvo_scale_ok(v_scale))
+        return KVO_BAD_SCALE;
+    const int64_t row = (int64_t)n_kv * head_dim;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    float *buf = (float *)malloc(sizeof(float) * (size_t)head_dim);
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot == -1)
+            continue;
+        if (slot < 0 || slot >= num_slots || positions[i] < 0 || positions[i] >= max_pos) {
+            status |= KVO_BAD_SLOT;
+            continue;
+        }
+        const float *cs_row = cos_sin + positions[i] * rot;
+        uint8_t *kdst = key_cache + slot * row;
+        uint8_t *vdst = value_cache + slot * row;
+        for (int32_t h = 0; h < n_kv; ++h) {
+            for (int32_t d = 0; d < head_dim; ++d)
+                buf[d] = kvo_load_src(key, src_dtype, i * key_stride + (int64_t)h * head_dim + d);
+            kvo_rope(buf, head_dim, rot, neox, cs_row);
+            for (int32_t d = 0; d < head_dim; ++d) {
+                const int64_t e = (int64_t)h * head_dim + d;
+                kdst[e] = kvo_store_code(buf[d], k_scale);
+                vdst[e] = kvo_store_code(kvo_load_src(value, src_dtype, i * value_stride + e), v_scale);
+            }
+        }
+    }
+    free(buf);
+    return status;
+}
+
 /* Dequantize n bytes: dst = s * decode(code), the product taken in float.
  * [P1] llama-kv-cache.cpp build_rope_shift routes F8_E4M3 through the
  * dequantize -> rope -> requantize path; [P1] tests/test-fp8.cpp
