@@ -19,5 +19,6 @@ from .binding import (  # noqa: F401
     paged_decode_attention_noalloc,
     paged_decode_workspace_size,
     reshape_and_cache,
+    rope_reshape_and_cache,
     status_string,
 )

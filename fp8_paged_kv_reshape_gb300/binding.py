@@ -27,6 +27,7 @@ DEV_TIMEOUT = 1 << 3
 # The functions include/kvfp8.h declares; the library must export every one.
 ABI_FUNCTIONS = (
     "kvfp8_reshape_and_cache",
+    "kvfp8_rope_reshape_and_cache",
     "kvfp8_paged_decode_workspace_size",
     "kvfp8_paged_decode_attention",
     "kvfp8_paged_decode_attention_noalloc",
@@ -54,6 +55,10 @@ def _load() -> ctypes.CDLL:
     lib.kvfp8_reshape_and_cache.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P, i32, i32, i32,
                                             i32, P, P, P, ctypes.c_int, P, P]
     lib.kvfp8_reshape_and_cache.restype = ctypes.c_int
+    lib.kvfp8_rope_reshape_and_cache.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P, P, i32, i32,
+                                                 i32, i32, P, P, P, i64, i32, i32, P, P,
+                                                 ctypes.c_int, P, P]
+    lib.kvfp8_rope_reshape_and_cache.restype = ctypes.c_int
     lib.kvfp8_paged_decode_workspace_size.argtypes = [i32, i32, i32]
     lib.kvfp8_paged_decode_workspace_size.restype = sz
     lib.kvfp8_paged_decode_attention.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32,
@@ -148,6 +153,43 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.T
         _ptr(key_cache), _ptr(value_cache), key_cache.shape[0], key_cache.shape[1], n_kv, hd,
         _ptr(slot_mapping), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(status), _stream(stream))
     _check(rc, "kvfp8_reshape_and_cache")
+
+
+def rope_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                           value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                           positions: torch.Tensor, cos_sin_cache: torch.Tensor,
+                           is_neox: bool = True, k_scale: torch.Tensor | None = None,
+                           v_scale: torch.Tensor | None = None,
+                           status: torch.Tensor | None = None, stream=None) -> None:
+    """kvfp8_rope_reshape_and_cache: rope on K (table cos_sin_cache float32 [max_pos, rot]),
+    then the store of reshape_and_cache; positions int64 [num_tokens]."""
+    if key.dtype != value.dtype or key.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("key and value must share one dtype, bfloat16 or float32")
+    if key.dim() != 3 or value.shape != key.shape:
+        raise ValueError("key/value must be [num_tokens, n_kv, head_dim] with equal shapes")
+    n, n_kv, hd = key.shape
+    for t in (key, value):
+        if t.stride(2) != 1 or t.stride(1) != hd:
+            raise ValueError("key/value inner dims [n_kv, head_dim] must be dense")
+    if key_cache.dtype != torch.uint8 or key_cache.shape != value_cache.shape or \
+            key_cache.dim() != 4 or tuple(key_cache.shape[2:]) != (n_kv, hd) or \
+            not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous uint8 [num_blocks, block_size, n_kv, head_dim]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n or \
+            positions.dtype != torch.int64 or positions.numel() != n:
+        raise ValueError("slot_mapping and positions must be int64 [num_tokens]")
+    if cos_sin_cache.dtype != torch.float32 or cos_sin_cache.dim() != 2 or \
+            not cos_sin_cache.is_contiguous():
+        raise ValueError("cos_sin_cache must be a contiguous float32 [max_pos, rot_dim] tensor")
+    sdt = _scale_args(k_scale, v_scale)
+    rc = LIB.kvfp8_rope_reshape_and_cache(
+        _ptr(key), _ptr(value), F32 if key.dtype == torch.float32 else BF16,
+        key.stride(0) if n > 0 else n_kv * hd, value.stride(0) if n > 0 else n_kv * hd, n,
+        _ptr(key_cache), _ptr(value_cache), key_cache.shape[0], key_cache.shape[1], n_kv, hd,
+        _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache), cos_sin_cache.shape[0],
+        cos_sin_cache.shape[1], 1 if is_neox else 0, _ptr(k_scale), _ptr(v_scale), sdt,
+        _ptr(status), _stream(stream))
+    _check(rc, "kvfp8_rope_reshape_and_cache")
 
 
 def paged_decode_workspace_size(num_seqs: int, n_q: int, head_dim: int) -> int:

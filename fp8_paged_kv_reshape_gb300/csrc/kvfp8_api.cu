@@ -65,6 +65,62 @@ kvfp8_status kvfp8_reshape_and_cache(const void *key, const void *value, kvfp8_d
     a.v_scale = v_scale;
     a.scale_dtype = scale_dtype;
     a.status = status;
+    a.positions = nullptr;
+    a.cos_sin = nullptr;
+    a.max_pos = 0;
+    a.rot = 0;
+    a.neox = 0;
+    a.head_dim = head_dim;
+    return from_cuda(kvfp8::launch_reshape_and_cache(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvfp8_status kvfp8_rope_reshape_and_cache(
+    const void *key, const void *value, kvfp8_dtype src_dtype, int64_t key_stride,
+    int64_t value_stride, int64_t num_tokens, uint8_t *key_cache, uint8_t *value_cache,
+    int32_t num_blocks, int32_t block_size, int32_t n_kv, int32_t head_dim,
+    const int64_t *slot_mapping, const int64_t *positions, const float *cos_sin_cache,
+    int64_t max_position, int32_t rot_dim, int32_t is_neox, const void *k_scale,
+    const void *v_scale, kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream) {
+    if (!dtype_ok(src_dtype) || !dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || block_size > 1024 || n_kv < 1 ||
+        max_position < 1)
+        return KVFP8_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
+    if (rot_dim < 16 || rot_dim > head_dim || (rot_dim & (rot_dim - 1)) != 0) return KVFP8_ERR_SHAPE;
+    const int64_t row = static_cast<int64_t>(n_kv) * head_dim;
+    if (key_stride < row || value_stride < row) return KVFP8_ERR_SHAPE;
+    if (row > 2048) return KVFP8_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return KVFP8_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping || !positions ||
+        !cos_sin_cache)
+        return KVFP8_ERR_NULL;
+    const int64_t esz = src_dtype == KVFP8_F32 ? 4 : 2;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (key_stride * esz) % 16 != 0 || (value_stride * esz) % 16 != 0 ||
+        !aligned(slot_mapping, 8) || !aligned(positions, 8) || !aligned16(cos_sin_cache))
+        return KVFP8_ERR_ALIGN;
+    kvfp8::ReshapeArgs a;
+    a.key = key;
+    a.value = value;
+    a.src_dtype = src_dtype;
+    a.key_stride = key_stride;
+    a.value_stride = value_stride;
+    a.num_tokens = num_tokens;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.num_slots = static_cast<int64_t>(num_blocks) * block_size;
+    a.row_elems = static_cast<int32_t>(row);
+    a.slot_mapping = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.scale_dtype = scale_dtype;
+    a.status = status;
+    a.positions = positions;
+    a.cos_sin = cos_sin_cache;
+    a.max_pos = max_position;
+    a.rot = rot_dim;
+    a.neox = is_neox ? 1 : 0;
+    a.head_dim = head_dim;
     return from_cuda(kvfp8::launch_reshape_and_cache(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -24,6 +24,13 @@ struct ReshapeArgs {
     const void *v_scale;
     int scale_dtype;
     uint32_t *status;
+    // rope on K before the store (kvfp8_rope_reshape_and_cache); cos_sin == nullptr: none
+    const int64_t *positions;
+    const float *cos_sin;  // [max_pos][rot]: cos half, then sin half
+    int64_t max_pos;
+    int32_t rot;
+    int32_t neox;
+    int32_t head_dim;
 };
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);

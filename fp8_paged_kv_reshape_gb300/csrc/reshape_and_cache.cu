@@ -233,6 +233,139 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const Re
         pipelined_rows<kF32, U, false>(a, c, r, stride, rows, lane);
 }
 
+// ---------------------------------------------------------------- rope + cache write
+//
+// K rows are rotated (rope) before the divide/encode; V rows are stored as above.  The
+// rotation of a pair (a, b) by the table entry (c, s) is a' = a*c - b*s, b' = a*s + b*c,
+// each product and sum rounded to float in that order (no fused multiply-add), so the
+// bytes match a plain CPU evaluation.  In the NeoX layout dim i pairs with i + rot/2: a
+// lane's 8-dim group and its partner group sit rot/16 lanes apart inside the head's
+// lane block, and are exchanged with one shuffle per value.  In the GPT-J layout pairs
+// are adjacent dims inside the group.
+
+__device__ __forceinline__ bool pos_ok(const ReshapeArgs &a, int64_t pos) {
+    return pos >= 0 && pos < a.max_pos;
+}
+
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], const RowCtx &c,
+                                               const FastDiv &fd, const ReshapeArgs &a,
+                                               int64_t slot, int64_t pos, int groups, int lane) {
+    uint8_t *dst = c.cache + slot * a.row_elems;
+    const float *cs = a.cos_sin + pos * a.rot;
+    const int half = a.rot >> 1;
+    const int partner = half >> 3;  // lanes between a group and its NeoX partner
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int g = lane + 32 * u;
+        float x[8];
+        buf[u].unpack(x);  // lanes past the row hold stale values; they only feed shuffles
+        const int d0 = (g * 8) % a.head_dim;
+        if (a.neox) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(0xFFFFFFFFu, x[i], partner);
+            if (g < groups && d0 < a.rot) {
+                const bool first = d0 < half;
+                const int ci = first ? d0 : d0 - half;
+                const float4 c0 = *reinterpret_cast<const float4 *>(cs + ci);
+                const float4 c1 = *reinterpret_cast<const float4 *>(cs + ci + 4);
+                const float4 s0 = *reinterpret_cast<const float4 *>(cs + half + ci);
+                const float4 s1 = *reinterpret_cast<const float4 *>(cs + half + ci + 4);
+                const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[i] = first ? __fsub_rn(__fmul_rn(x[i], cv[i]), __fmul_rn(y[i], sv[i]))
+                                 : __fadd_rn(__fmul_rn(y[i], sv[i]), __fmul_rn(x[i], cv[i]));
+            }
+        } else if (g < groups && d0 < a.rot) {
+            const float4 cv = *reinterpret_cast<const float4 *>(cs + d0 / 2);
+            const float4 sv = *reinterpret_cast<const float4 *>(cs + half + d0 / 2);
+            const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
+            const float ss[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float p = x[2 * j], q = x[2 * j + 1];
+                x[2 * j] = __fsub_rn(__fmul_rn(p, cc[j]), __fmul_rn(q, ss[j]));
+                x[2 * j + 1] = __fadd_rn(__fmul_rn(p, ss[j]), __fmul_rn(q, cc[j]));
+            }
+        }
+        if (g < groups)
+            *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
+                quantize8<kFast>(x, c.s, fd);
+    }
+}
+
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void rope_pipelined_rows(const ReshapeArgs &a, const RowCtx &c,
+                                                    bool is_k, int64_t r, int64_t stride,
+                                                    int64_t rows, int lane) {
+    const FastDiv fd(c.s);
+    const int groups = a.row_elems >> 3;
+    auto pos_of = [&](int64_t row) -> int64_t {
+        return row < rows ? __ldg(a.positions + (row >> 1)) : 0;
+    };
+    auto ok_of = [&](int64_t row, int64_t slot, int64_t pos) -> bool {
+        if (row >= rows) return false;
+        const bool sok = slot >= 0 && slot < a.num_slots;
+        if (sok && pos_ok(a, pos)) return true;
+        if (slot != -1 && lane == 0 && (row & 1) == 0) flag(a.status, KVFP8_DEV_BAD_SLOT);
+        return false;
+    };
+    Group<kF32> A[U], B[U];
+    int64_t s1 = slot_of(a, r, rows), p1 = pos_of(r);
+    int64_t s2 = slot_of(a, r + stride, rows), p2 = pos_of(r + stride);
+    bool ok1 = ok_of(r, s1, p1);
+    if (ok1) load_row<kF32, U>(A, c, r, groups, lane);
+    while (r < rows) {
+        int64_t rn = r + stride;
+        bool ok2 = ok_of(rn, s2, p2);
+        if (ok2) load_row<kF32, U>(B, c, rn, groups, lane);
+        int64_t s3 = slot_of(a, rn + stride, rows), p3 = pos_of(rn + stride);
+        if (ok1) {
+            if (is_k) store_row_rope<kF32, U, kFast>(A, c, fd, a, s1, p1, groups, lane);
+            else store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
+        }
+        r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
+        if (r >= rows) break;
+        rn = r + stride;
+        ok2 = ok_of(rn, s2, p2);
+        if (ok2) load_row<kF32, U>(A, c, rn, groups, lane);
+        s3 = slot_of(a, rn + stride, rows);
+        p3 = pos_of(rn + stride);
+        if (ok1) {
+            if (is_k) store_row_rope<kF32, U, kFast>(B, c, fd, a, s1, p1, groups, lane);
+            else store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
+        }
+        r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
+    }
+}
+
+template <bool kF32, int U>
+__global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const ReshapeArgs a) {
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = 2 * a.num_tokens;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;  // even
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    const bool is_v = (r & 1) != 0;
+    RowCtx c;
+    c.src = static_cast<const uint8_t *>(is_v ? a.value : a.key);
+    c.cache = is_v ? a.value_cache : a.key_cache;
+    c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
+    c.s = is_v ? sv : sk;
+    if (fast_range(c.s))
+        rope_pipelined_rows<kF32, U, true>(a, c, !is_v, r, stride, rows, lane);
+    else
+        rope_pipelined_rows<kF32, U, false>(a, c, !is_v, r, stride, rows, lane);
+}
+
 // Any row length: one warp per row, groups streamed in rounds of 4 per lane.
 template <bool kF32>
 __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const ReshapeArgs a) {
@@ -304,10 +437,23 @@ cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
     return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream);
 }
 
+template <bool kF32>
+cudaError_t dispatch_rope(const ReshapeArgs &a, cudaStream_t stream) {
+    const int per_lane = (a.row_elems / 8 + 31) / 32;
+    if (per_lane <= 1) return launch_persistent(rope_reshape_kernel<kF32, 1>, a, stream);
+    if (per_lane <= 2) return launch_persistent(rope_reshape_kernel<kF32, 2>, a, stream);
+    if (per_lane <= 4) return launch_persistent(rope_reshape_kernel<kF32, 4>, a, stream);
+    if (per_lane <= 8) return launch_persistent(rope_reshape_kernel<kF32, 8>, a, stream);
+    return cudaErrorNotSupported;
+}
+
 }  // namespace
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream) {
     if (a.num_tokens == 0) return cudaSuccess;
+    if (a.cos_sin != nullptr)
+        return a.src_dtype == KVFP8_F32 ? dispatch_rope<true>(a, stream)
+                                        : dispatch_rope<false>(a, stream);
     return a.src_dtype == KVFP8_F32 ? dispatch<true>(a, stream) : dispatch<false>(a, stream);
 }
 

@@ -117,6 +117,36 @@ KVFP8_API kvfp8_status kvfp8_reshape_and_cache(const void *key, const void *valu
                                      uint32_t *status, kvfp8_stream_t stream);
 
 /*
+ * kvfp8_reshape_and_cache with rotary position embedding applied to K first, in the same
+ * pass (V is stored unrotated).
+ *
+ * Defined by: [P1] llama-graph.cpp build_attn ("rope fusion which directly writes into
+ * k-v cache"); the rotation itself is the model's, so its form is fixed here: for token i
+ * with p = positions[i], table row T = cos_sin_cache[p] (cos in T[0..rot/2), sin in
+ * T[rot/2..rot)), every pair (a, b) of the first rot_dim dims of each K head becomes
+ *   a' = a*cos - b*sin,   b' = a*sin + b*cos      (pair j uses cos/sin entry j)
+ * with each product and sum rounded to float in that order (no fused multiply-add).
+ * is_neox != 0: dim j pairs with j + rot_dim/2 (GPT-NeoX); 0: dim 2j with 2j+1 (GPT-J).
+ * Dims >= rot_dim pass through.  Then K and V are stored exactly as by
+ * kvfp8_reshape_and_cache.
+ *
+ * Arguments as kvfp8_reshape_and_cache, plus:
+ * positions       device int64 [num_tokens]; a position outside [0, max_position) skips the
+ *                 token and sets KVFP8_DEV_BAD_SLOT
+ * cos_sin_cache   device float32 [max_position][rot_dim], 16-byte aligned
+ * rot_dim         a power of two in [16, head_dim]
+ * head_dim must be 64, 128 or 256; rows of more than 2048 elements (n_kv*head_dim) return
+ * KVFP8_ERR_UNSUPPORTED.
+ */
+KVFP8_API kvfp8_status kvfp8_rope_reshape_and_cache(
+    const void *key, const void *value, kvfp8_dtype src_dtype, int64_t key_stride,
+    int64_t value_stride, int64_t num_tokens, uint8_t *key_cache, uint8_t *value_cache,
+    int32_t num_blocks, int32_t block_size, int32_t n_kv, int32_t head_dim,
+    const int64_t *slot_mapping, const int64_t *positions, const float *cos_sin_cache,
+    int64_t max_position, int32_t rot_dim, int32_t is_neox, const void *k_scale,
+    const void *v_scale, kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream);
+
+/*
  * Workspace bytes kvfp8_paged_decode_attention needs for this batch shape (split-KV
  * partial results and the per-call chunk plan).  Pure host arithmetic.
  */

@@ -73,6 +73,30 @@ def test_reshape_host_validation():
     assert _reshape(num_tokens=0, key=None) == binding.OK           # nothing to do
 
 
+def test_rope_reshape_host_validation():
+    def call(**over):
+        args = dict(key=ctypes.c_void_p(16), value=ctypes.c_void_p(16), src_dtype=binding.BF16,
+                    key_stride=1024, value_stride=1024, num_tokens=4,
+                    key_cache=ctypes.c_void_p(16), value_cache=ctypes.c_void_p(16), num_blocks=4,
+                    block_size=16, n_kv=8, head_dim=128, slot_mapping=ctypes.c_void_p(16),
+                    positions=ctypes.c_void_p(16), cos_sin=ctypes.c_void_p(16), max_pos=4096,
+                    rot=128, neox=1, k_scale=None, v_scale=None, scale_dtype=binding.F32,
+                    status=None, stream=None)
+        args.update(over)
+        return kv.LIB.kvfp8_rope_reshape_and_cache(*args.values())
+    assert call(positions=None) == binding.ERR_NULL
+    assert call(cos_sin=None) == binding.ERR_NULL
+    assert call(rot=96) == binding.ERR_SHAPE          # not a power of two
+    assert call(rot=256) == binding.ERR_SHAPE         # above head_dim
+    assert call(rot=8) == binding.ERR_SHAPE
+    assert call(head_dim=96, n_kv=8, key_stride=768, value_stride=768) == binding.ERR_SHAPE
+    assert call(max_pos=0) == binding.ERR_SHAPE
+    assert call(n_kv=32, key_stride=4096, value_stride=4096) == binding.ERR_UNSUPPORTED
+    assert call(cos_sin=ctypes.c_void_p(24)) == binding.ERR_ALIGN
+    assert call(positions=ctypes.c_void_p(20)) == binding.ERR_ALIGN
+    assert call(num_tokens=0, key=None) == binding.OK
+
+
 def _decode(**over):
     args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16), key_cache=ctypes.c_void_p(16),
                 value_cache=ctypes.c_void_p(16), block_tables=ctypes.c_void_p(16),

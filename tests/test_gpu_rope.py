@@ -1,0 +1,89 @@
+"""kvfp8_rope_reshape_and_cache on the GPU vs the CPU oracle: cache bytes bit for bit.
+The rotation uses a caller-supplied float32 cos/sin table (see include/kvfp8.h)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from tests import gpu_util
+
+pytestmark = pytest.mark.gpu
+
+kv = pytest.importorskip("fp8_paged_kv_reshape_gb300")
+
+
+def _table(max_pos, rot, base=10000.0):
+    inv = base ** (-np.arange(0, rot, 2, dtype=np.float64) / rot)
+    ang = np.arange(max_pos)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+CASES = [  # n_kv, head_dim, rot, neox, src dtype, tokens
+    (8, 128, 128, True, torch.bfloat16, 3000),
+    (8, 128, 64, True, torch.bfloat16, 1000),
+    (8, 128, 128, False, torch.bfloat16, 1000),
+    (2, 64, 64, True, torch.bfloat16, 777),
+    (2, 64, 32, False, torch.bfloat16, 100),
+    (4, 256, 256, True, torch.bfloat16, 500),
+    (8, 256, 128, False, torch.bfloat16, 300),
+    (1, 128, 16, True, torch.bfloat16, 64),
+    (8, 128, 128, True, torch.float32, 600),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"nkv{c[0]}_hd{c[1]}_rot{c[2]}_{'neox' if c[3] else 'gptj'}_{str(c[4])[6:]}" for c in CASES])
+def test_rope_cache_write_bit_exact(case):
+    n_kv, hd, rot, neox, dt, n = case
+    g = torch.Generator().manual_seed(n + hd + rot)
+    k = (torch.randn(n, n_kv, hd, generator=g) * 3).to(dt)
+    v = (torch.randn(n, n_kv, hd, generator=g) * 3).to(dt)
+    max_pos = 8192
+    pos = torch.randint(0, max_pos, (n,), generator=g, dtype=torch.int64)
+    nb, bs = (n + 15) // 16 + 3, 16
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(torch.int64)
+    slots[::17] = -1
+    table = _table(max_pos, rot)
+    kc = torch.full((nb, bs, n_kv, hd), 0x5A, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    sc = (torch.tensor([0.05], device="cuda"), torch.tensor([0.04], device="cuda"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv.rope_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, slots.cuda(), pos.cuda(),
+                              torch.from_numpy(table).cuda(), neox, *sc, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ko = np.full((nb, bs, n_kv, hd), 0x5A, np.uint8)
+    vo = ko.copy()
+    src = oracle.F32 if dt == torch.float32 else oracle.BF16
+    kin = k.numpy() if dt == torch.float32 else k
+    vin = v.numpy() if dt == torch.float32 else v
+    assert oracle.rope_reshape_and_cache(kin, vin, ko, vo, slots.numpy(), pos.numpy(), table, rot,
+                                         neox, bs, 0.05, 0.04, src_dtype=src) == 0
+    got_k = kc.cpu().numpy()
+    bad = np.argwhere(got_k != ko)
+    assert bad.shape[0] == 0, bad[:5]
+    np.testing.assert_array_equal(vc.cpu().numpy(), vo)
+
+
+def test_rope_changes_k_but_not_v_and_bad_positions_are_flagged():
+    w = workloads.WORKLOADS["llama3_8b"]
+    n = 64
+    k, v = workloads.make_kv(w, n, "cuda")
+    table = torch.from_numpy(_table(128, 128)).cuda()
+    slots = torch.arange(n, dtype=torch.int64, device="cuda")
+    pos = torch.arange(n, dtype=torch.int64, device="cuda") + 1
+    pos[5] = 128      # out of range
+    pos[9] = -3
+    kc = torch.zeros(4, 16, 8, 128, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    kp, vp = kc.clone(), vc.clone()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kv.rope_reshape_and_cache(k, v, kc, vc, slots, pos, table, True, status=st)
+    kv.reshape_and_cache(k, v, kp, vp, slots)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kv.DEV_BAD_SLOT
+    flat_k, flat_v = kc.view(64, -1), vc.view(64, -1)
+    assert torch.all(flat_k[[5, 9]] == 0) and torch.all(flat_v[[5, 9]] == 0)  # skipped
+    ok = [i for i in range(64) if i not in (5, 9)]
+    assert torch.equal(flat_v[ok], vp.view(64, -1)[ok])                      # V untouched by rope
+    assert not torch.equal(flat_k[ok], kp.view(64, -1)[ok])                  # K rotated
