@@ -419,6 +419,52 @@ uint32_t kvo_paged_decode_attention(double *out, const uint16_t *query, const ui
     return status;
 }
 
+/* Multi-query (causal) paged attention: sequence b holds seq_lens[b] cached tokens, the
+ * last n_b = query_start_loc[b+1] - query_start_loc[b] of which are new; its query token
+ * j (0 <= j < n_b) sits at position p = seq_lens[b] - n_b + j and attends to the cached
+ * tokens t <= p.  [P1] tests/test-fp8.cpp check_fp8_attention: a batch of 4 tokens,
+ * each attending to every past token up to and including itself (past <= token).
+ * query and out are [total_q][n_q][head_dim] with sequence b's rows starting at
+ * query_start_loc[b].  n_b > seq_lens[b] flags KVO_BAD_BLOCK (positions below 0 attend to
+ * nothing and give zeros). */
+uint32_t kvo_paged_attention_multi(double *out, const uint16_t *query,
+                                   const int32_t *query_start_loc, const uint8_t *key_cache,
+                                   const uint8_t *value_cache, const int32_t *block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                   int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, double sm_scale,
+                                   float k_scale, float v_scale)
+{
+    uint32_t status = 0;
+    if (!kvo_scale_ok(k_scale) || !kvo_scale_ok(v_scale))
+        return KVO_BAD_SCALE;
+    if (sm_scale <= 0.0)
+        sm_scale = 1.0 / sqrt((double)head_dim);
+    const int32_t group = n_q / n_kv;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int32_t len = seq_lens[b];
+        if (len > max_blocks_per_seq * block_size) {
+            status |= KVO_BAD_BLOCK;
+            len = max_blocks_per_seq * block_size;
+        }
+        const int32_t q0 = query_start_loc[b];
+        const int32_t nb = query_start_loc[b + 1] - q0;
+        if (nb > len)
+            status |= KVO_BAD_BLOCK;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int32_t p = len - nb + j;  /* attends to tokens 0..p */
+            for (int32_t h = 0; h < n_q; ++h) {
+                const int64_t row = ((int64_t)(q0 + j) * n_q + h) * head_dim;
+                status |= kvo_decode_one(out + row, query + row, key_cache, value_cache,
+                                         block_tables + (int64_t)b * max_blocks_per_seq,
+                                         p + 1 > 0 ? p + 1 : 0, n_kv, h / group, head_dim,
+                                         block_size, num_blocks, sm_scale, k_scale, v_scale);
+            }
+        }
+    }
+    return status;
+}
+
 /* Attention for a chosen list of (sequence, q head) pairs only, for sampled
  * checks at full size: pairs holds n_pairs (seq, head) int32 pairs and out is
  * [n_pairs][head_dim]. */
