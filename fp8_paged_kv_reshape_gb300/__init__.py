@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     LIB_PATH,
     check_scale_host,
     dequant,
+    paged_attention_multi,
     paged_decode_attention,
     paged_decode_attention_noalloc,
     paged_decode_workspace_size,

@@ -31,6 +31,7 @@ ABI_FUNCTIONS = (
     "kvfp8_paged_decode_workspace_size",
     "kvfp8_paged_decode_attention",
     "kvfp8_paged_decode_attention_noalloc",
+    "kvfp8_paged_attention_multi",
     "kvfp8_dequant",
     "kvfp8_check_scale_host",
     "kvfp8_status_string",
@@ -67,6 +68,10 @@ def _load() -> ctypes.CDLL:
     lib.kvfp8_paged_decode_attention_noalloc.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                          i32, i32, f32, P, P, ctypes.c_int, P, P]
     lib.kvfp8_paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.kvfp8_paged_attention_multi.argtypes = [P, P, P, i32, i32, P, P, P, i32, P, i32, i32, i32,
+                                                i32, i32, i32, f32, P, P, ctypes.c_int, P, sz, P,
+                                                P]
+    lib.kvfp8_paged_attention_multi.restype = ctypes.c_int
     lib.kvfp8_dequant.argtypes = [P, ctypes.c_int, P, i64, P, ctypes.c_int, P]
     lib.kvfp8_dequant.restype = ctypes.c_int
     lib.kvfp8_check_scale_host.argtypes = [f32]
@@ -229,6 +234,42 @@ def paged_decode_attention(query: torch.Tensor, key_cache: torch.Tensor, value_c
         float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     _check(rc, "kvfp8_paged_decode_attention")
+    return out
+
+
+def paged_attention_multi(query: torch.Tensor, query_start_loc: torch.Tensor, max_query_len: int,
+                          key_cache: torch.Tensor, value_cache: torch.Tensor,
+                          block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                          k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None,
+                          sm_scale: float = 0.0, out: torch.Tensor | None = None,
+                          workspace: torch.Tensor | None = None,
+                          status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvfp8_paged_attention_multi: causal multi-query attention; query/out bf16
+    [num_query_rows, n_q, head_dim], sequence b's rows from query_start_loc[b] (int32
+    [num_seqs + 1])."""
+    if query.dtype != torch.bfloat16 or query.dim() != 3 or not query.is_contiguous():
+        raise ValueError("query must be a contiguous bf16 [rows, n_q, head_dim] tensor")
+    rows, n_q, hd = query.shape
+    num_seqs = seq_lens.numel()
+    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != num_seqs + 1:
+        raise ValueError("query_start_loc must be int32 [num_seqs + 1]")
+    if key_cache.dtype != torch.uint8 or key_cache.shape != value_cache.shape or \
+            key_cache.dim() != 4 or key_cache.shape[3] != hd:
+        raise ValueError("caches must be uint8 [num_blocks, block_size, n_kv, head_dim]")
+    num_blocks, bs, n_kv, _ = key_cache.shape
+    if out is None:
+        out = torch.empty_like(query)
+    need = paged_decode_workspace_size(num_seqs, n_q * max_query_len, hd)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
+    sdt = _scale_args(k_scale, v_scale)
+    rc = LIB.kvfp8_paged_attention_multi(
+        _ptr(out), _ptr(query), _ptr(query_start_loc), rows, max_query_len, _ptr(key_cache),
+        _ptr(value_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
+        n_q, n_kv, hd, bs, num_blocks, float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+        _stream(stream))
+    _check(rc, "kvfp8_paged_attention_multi")
     return out
 
 

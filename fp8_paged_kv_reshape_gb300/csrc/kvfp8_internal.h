@@ -61,13 +61,19 @@ struct DecodeArgs {
     int scale_dtype;
     void *workspace;
     uint32_t *status;
+    // multi-query (causal) form: sequence b's query rows start at qsl[b]; qmax is the
+    // largest per-sequence query count.  Decode: qsl == nullptr, qmax == 1.
+    const int32_t *qsl;
+    int32_t qmax;
+    int32_t qrows;  // rows of query and out
 };
 
-// Workspace layout, shared by the size query and the launcher.
+// Workspace layout, shared by the size query and the launcher; rows = query rows per
+// sequence (n_q for decode, max query count * n_q for the multi-query form).
 struct DecodeWorkspace {
     size_t cstart_off, lse_off, o_off, total;
 };
-DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t head_dim);
+DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t rows, int32_t head_dim);
 
 // Returns cudaErrorNotSupported for a shape without a kernel instance, or the first
 // CUDA error met while encoding tensor maps / launching.

@@ -83,7 +83,23 @@ struct KernelArgs {
     int32_t num_ctas;
     int32_t stages;
     int32_t box_rows;  // 16, or 8 for 8-token blocks
+    // multi-query (causal) form: sequence b's query rows start at qsl[b] (nullptr: one
+    // query per sequence, row b); rows_per_seq = max query count * n_q
+    const int32_t *qsl;
+    int32_t rows_per_seq;
+    int32_t qrows;  // rows of query and out (multi-query form)
 };
+
+// Query rows [q0, q0 + count) of sequence b in the multi-query form, or count 0 when the
+// sequence's query_start_loc entries are out of range (flagged by the plan kernel).
+struct QueryRange {
+    int q0, count;
+};
+__device__ __forceinline__ QueryRange query_range(const int32_t *qsl, int b, int qmax, int qrows) {
+    const int q0 = qsl[b], n = qsl[b + 1] - q0;
+    if (q0 < 0 || n < 0 || n > qmax || q0 + n > qrows) return QueryRange{0, 0};
+    return QueryRange{q0, n};
+}
 
 // ---------------------------------------------------------------- PTX wrappers
 
@@ -196,8 +212,9 @@ __device__ __forceinline__ void pdl_trigger() {
 //    counts), cstart[num_seqs] = total;
 //  * the output rows of empty sequences are zeroed (no CTA visits them).
 __global__ void __launch_bounds__(1024)
-plan_kernel(const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, int32_t *cstart,
-            __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
+plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t qrows,
+            int32_t num_seqs, int32_t max_len, int32_t *cstart, __nv_bfloat16 *out,
+            int32_t out_row_elems, uint32_t *status) {
     pdl_trigger();  // the decode grid may start its prologue; it waits for this grid's writes
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
@@ -213,15 +230,24 @@ plan_kernel(const int32_t *seq_lens, int32_t num_seqs, int32_t max_len, int32_t 
                 flag(status, KVFP8_DEV_BAD_BLOCK);
                 L = L < 0 ? 0 : max_len;
             }
-            n = (L + kChunkTokens - 1) / kChunkTokens;
+            int nq = 1;  // query rows of the sequence
+            if (qsl) {
+                const int raw = qsl[i + 1] - qsl[i];
+                nq = query_range(qsl, i, qmax, qrows).count;
+                if (nq != raw) flag(status, KVFP8_DEV_BAD_BLOCK);  // rows out of range: skipped
+                if (nq > L) flag(status, KVFP8_DEV_BAD_BLOCK);     // positions below zero
+            }
+            n = nq > 0 ? (L + kChunkTokens - 1) / kChunkTokens : 0;
         }
         unsigned empty = __ballot_sync(0xFFFFFFFFu, i < num_seqs && n == 0);
         while (empty) {  // this warp zeroes the output rows of its empty sequences
-            const int b = __ffs(empty) - 1;
+            const int b = base + warp * 32 + __ffs(empty) - 1;
             empty &= empty - 1;
-            uint4 *row = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(base + warp * 32 + b) *
-                                                             out_row_elems);
-            for (int k = lane; k < out_row_elems / 8; k += 32) row[k] = make_uint4(0u, 0u, 0u, 0u);
+            const QueryRange qr = qsl ? query_range(qsl, b, qmax, qrows) : QueryRange{b, 1};
+            const int64_t r0 = qr.q0, nr = qr.count;
+            uint4 *rows = reinterpret_cast<uint4 *>(out + r0 * out_row_elems);
+            for (int64_t k = lane; k < nr * out_row_elems / 8; k += 32)
+                rows[k] = make_uint4(0u, 0u, 0u, 0u);
         }
         int x = n;
 #pragma unroll
@@ -265,22 +291,28 @@ __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
     constexpr int TPH = HD / 4;     // threads per head
     constexpr int HPB = 256 / TPH;  // heads per CTA
     const int seq = blockIdx.x;
-    const int head = blockIdx.y * HPB + threadIdx.x / TPH;
+    const int row = blockIdx.y * HPB + threadIdx.x / TPH;  // row of the sequence
     const int d = (threadIdx.x % TPH) * 4;
     pdl_wait();  // the decode grid's partials are visible from here on
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
     const int64_t cs = a.cstart[seq], ce = a.cstart[seq + 1], T = a.cstart[a.num_seqs];
-    if (!scale_ok(sk) || !scale_ok(sv) || head >= a.n_q) return;
+    if (!scale_ok(sk) || !scale_ok(sv) || row >= a.rows_per_seq) return;
     if (ce == cs) return;  // empty: zeroed by the plan kernel
+    int64_t out_row = static_cast<int64_t>(seq) * a.n_q + row;
+    if (a.qsl != nullptr) {
+        const QueryRange qr = query_range(a.qsl, seq, a.rows_per_seq / a.n_q, a.qrows);
+        if (row / a.n_q >= qr.count) return;  // past this sequence's queries
+        out_row = static_cast<int64_t>(qr.q0) * a.n_q + row;
+    }
     const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);  // the effective grid
     const int cf = cta_of(cs, T, P), cl = cta_of(ce - 1, T, P);
     if (cf == cl) return;  // finished inside one CTA
     const int k = cl - cf + 1;
     const int64_t p0 = static_cast<int64_t>(seq) + cf;
-    const float *lse = a.part_lse + p0 * a.n_q + head;
-    const float *o = a.part_o + (p0 * a.n_q + head) * HD + d;
-    const int64_t lse_stride = a.n_q, o_stride = static_cast<int64_t>(a.n_q) * HD;
+    const float *lse = a.part_lse + p0 * a.rows_per_seq + row;
+    const float *o = a.part_o + (p0 * a.rows_per_seq + row) * HD + d;
+    const int64_t lse_stride = a.rows_per_seq, o_stride = static_cast<int64_t>(a.rows_per_seq) * HD;
     float M = -INFINITY, den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 8
@@ -308,7 +340,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
     uint2 r;
     r.x = bf16x2_from_f32(acc.x * inv, acc.y * inv);
     r.y = bf16x2_from_f32(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(a.out + (static_cast<int64_t>(seq) * a.n_q + head) * HD + d) = r;
+    *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = r;
 }
 
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
@@ -316,7 +348,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
 template <int HD, int NT>
 constexpr int min_ctas_per_sm() { return HD * NT <= 128 ? 2 : 1; }
 
-template <int HD, int NT>
+template <int HD, int NT, bool kMulti>
 __global__ void __launch_bounds__(kThreadsMax, min_ctas_per_sm<HD, NT>())
 decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
               const KernelArgs a) {
@@ -490,6 +522,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         float o[KP][2][NT][4];
         float m[NT][2], l[NT][2];
         uint32_t qb[2 * KP][NT][2];
+        // multi-query form: per score column (query token j, head g) the last cache
+        // position it may see, and its row within the sequence (-1: a padding column)
+        int plim[NT][2], crow[NT][2];
+        int q0 = 0;
 #pragma unroll
         for (int e = 0; e < KP; ++e)
 #pragma unroll
@@ -522,16 +558,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             if (mt.flags & kDone) break;
 
             if (mt.flags & kFirst) {
-                const __nv_bfloat16 *qrow =
-                    a.query + (static_cast<int64_t>(mt.seq) * a.n_q + kvh * a.group) * HD;
+                int nq = 1;
+                if (kMulti) {
+                    const QueryRange qr = query_range(a.qsl, mt.seq, a.rows_per_seq / a.n_q, a.qrows);
+                    q0 = qr.q0;
+                    nq = qr.count;
+                    const int L = min(max(a.seq_lens[mt.seq], 0), a.max_len);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            const int n = nt * 8 + 2 * tig + c;
+                            const int j = n / a.group, g = n % a.group;
+                            plim[nt][c] = j < nq ? L - nq + j : -1;
+                            crow[nt][c] = j < nq ? j * a.n_q + kvh * a.group + g : -1;
+                        }
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int g = nt * 8 + gid;
+                    // column gid of n-tile nt: query token jq, head gq of the group
+                    const int n = nt * 8 + gid;
+                    const int jq = kMulti ? n / a.group : 0;
+                    const int gq = kMulti ? n % a.group : n;
+                    const bool qv = kMulti ? jq < nq : n < a.group;
+                    const __nv_bfloat16 *qrow =
+                        a.query +
+                        ((static_cast<int64_t>(kMulti ? q0 + jq : mt.seq)) * a.n_q + kvh * a.group + gq) *
+                            HD;
 #pragma unroll
                     for (int c = 0; c < 2 * KP; ++c) {
                         uint2 w = make_uint2(0u, 0u);
-                        if (g < a.group)
-                            w = *reinterpret_cast<const uint2 *>(qrow + g * HD + 16 * c + 4 * tig);
+                        if (qv) w = *reinterpret_cast<const uint2 *>(qrow + 16 * c + 4 * tig);
                         qb[c][nt][0] = f16x2_from_f32(bf16lo(w.x), bf16hi(w.x));
                         qb[c][nt][1] = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
                     }
@@ -586,17 +643,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                     float p[4];
 #pragma unroll
                     for (int c = 0; c < 2; ++c) {
-                        const float s_lo = lo_ok ? sacc[nt][c] * score_scale : -INFINITY;
-                        const float s_hi = hi_ok ? sacc[nt][c + 2] * score_scale : -INFINITY;
+                        bool lo_c = lo_ok, hi_c = hi_ok;
+                        if (kMulti) {  // causal: token tok0+row is visible up to plim
+                            lo_c = lo_c && mt.tok0 + gid <= plim[nt][c];
+                            hi_c = hi_c && mt.tok0 + gid + 8 <= plim[nt][c];
+                        }
+                        const float s_lo = lo_c ? sacc[nt][c] * score_scale : -INFINITY;
+                        const float s_hi = hi_c ? sacc[nt][c + 2] * score_scale : -INFINITY;
                         float mx = fmaxf(s_lo, s_hi);
                         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
                         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
                         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
                         const float m_old = m[nt][c];
-                        const float m_new = fmaxf(m_old, mx);
+                        float m_new = fmaxf(m_old, mx);
                         const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);
-                        p[c] = ex2(s_lo - m_new);
-                        p[c + 2] = ex2(s_hi - m_new);
+                        // a column that has seen no visible token yet keeps weight 0
+                        const float m_sub = (kMulti && m_new == -INFINITY) ? 0.f : m_new;
+                        p[c] = ex2(s_lo - m_sub);
+                        p[c + 2] = ex2(s_hi - m_sub);
                         l[nt][c] = l[nt][c] * alpha + p[c] + p[c + 2];
                         m[nt][c] = m_new;
                         if (alpha != 1.f) {
@@ -667,12 +731,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                         lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 8);
                         lt += __shfl_xor_sync(0xFFFFFFFFu, lt, 16);
                         const int g = nt * 8 + 2 * tig + c;
-                        if (g >= a.group) continue;
-                        const int head = kvh * a.group + g;
+                        if (kMulti ? crow[nt][c] < 0 : g >= a.group) continue;  // padding column
+                        // the row of this column within the sequence's rows, and in out
+                        const int srow = kMulti ? crow[nt][c] : kvh * a.group + g;
+                        const int64_t orow_idx = kMulti ? static_cast<int64_t>(q0) * a.n_q + srow
+                                                        : static_cast<int64_t>(mt.seq) * a.n_q + srow;
                         if (direct) {
                             const float inv = lt > 0.f ? sv / lt : 0.f;
-                            __nv_bfloat16 *orow =
-                                a.out + (static_cast<int64_t>(mt.seq) * a.n_q + head) * HD;
+                            __nv_bfloat16 *orow = a.out + orow_idx * HD;
 #pragma unroll
                             for (int e = 0; e < KP; ++e) {
                                 const int d = 32 * e + 2 * gid;
@@ -683,7 +749,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                             }
                         } else {
                             const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                            float *prow = a.part_o + (pidx * a.n_q + head) * HD;
+                            float *prow = a.part_o + (pidx * a.rows_per_seq + srow) * HD;
 #pragma unroll
                             for (int e = 0; e < KP; ++e) {
                                 const int d = 32 * e + 2 * gid;
@@ -693,7 +759,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                                     o[e][0][nt][c + 2] * inv, o[e][1][nt][c + 2] * inv);
                             }
                             if (gid == 0)
-                                a.part_lse[pidx * a.n_q + head] =
+                                a.part_lse[pidx * a.rows_per_seq + srow] =
                                     lt > 0.f ? m[nt][c] + __log2f(lt) : -INFINITY;
                         }
                     }
@@ -745,7 +811,7 @@ int env_int(const char *name, int dflt) {
     return v ? std::atoi(v) : dflt;
 }
 
-template <int HD, int NT>
+template <int HD, int NT, bool kMulti>
 cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t stream) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -773,7 +839,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     const size_t smem = smem_for(stages);
     if (smem > static_cast<size_t>(smem_optin)) return cudaErrorNotSupported;
 
-    auto kern = decode_kernel<HD, NT>;
+    auto kern = decode_kernel<HD, NT, kMulti>;
     if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem))) != cudaSuccess)
         return err;
@@ -818,8 +884,11 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.num_ctas = num_ctas;
     k.stages = stages;
     k.box_rows = box_rows;
+    k.qsl = d.qsl;
+    k.rows_per_seq = d.qmax * d.n_q;
+    k.qrows = d.qrows;
 
-    plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.num_seqs, k.max_len,
+    plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs, k.max_len,
                                         reinterpret_cast<int32_t *>(w + ws.cstart_off), k.out,
                                         d.n_q * HD, d.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
@@ -840,7 +909,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
 
     constexpr int kHeadsPerCta = 256 / (HD / 4);
     cudaLaunchConfig_t ccfg = cfg;
-    ccfg.gridDim = dim3(d.num_seqs, (d.n_q + kHeadsPerCta - 1) / kHeadsPerCta);
+    ccfg.gridDim = dim3(d.num_seqs, (k.rows_per_seq + kHeadsPerCta - 1) / kHeadsPerCta);
     ccfg.blockDim = dim3(256);
     ccfg.dynamicSmemBytes = 0;
     return cudaLaunchKernelEx(&ccfg, combine_kernel<HD>, k);
@@ -861,14 +930,24 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
 
 cudaError_t launch_paged_decode(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
-    const DecodeWorkspace ws = decode_workspace_layout(d.num_seqs, d.n_q, d.head_dim);
+    const DecodeWorkspace ws = decode_workspace_layout(d.num_seqs, d.qmax * d.n_q, d.head_dim);
     const int group = d.n_q / d.n_kv;
     if (d.n_kv > kMaxKvHeads) return cudaErrorNotSupported;
-    const int nt = group <= 8 ? 1 : 2;
+    const int cols = d.qmax * group;  // score columns per kv head
+    if (cols > 16) return cudaErrorNotSupported;
+    const int nt = cols <= 8 ? 1 : 2;
+    if (d.qsl == nullptr) {
+        switch (d.head_dim) {
+            case 64: return nt == 1 ? run<64, 1, false>(d, ws, stream) : run<64, 2, false>(d, ws, stream);
+            case 128: return nt == 1 ? run<128, 1, false>(d, ws, stream) : run<128, 2, false>(d, ws, stream);
+            case 256: return nt == 1 ? run<256, 1, false>(d, ws, stream) : cudaErrorNotSupported;
+            default: return cudaErrorNotSupported;
+        }
+    }
     switch (d.head_dim) {
-        case 64: return nt == 1 ? run<64, 1>(d, ws, stream) : run<64, 2>(d, ws, stream);
-        case 128: return nt == 1 ? run<128, 1>(d, ws, stream) : run<128, 2>(d, ws, stream);
-        case 256: return nt == 1 ? run<256, 1>(d, ws, stream) : cudaErrorNotSupported;
+        case 64: return nt == 1 ? run<64, 1, true>(d, ws, stream) : run<64, 2, true>(d, ws, stream);
+        case 128: return nt == 1 ? run<128, 1, true>(d, ws, stream) : run<128, 2, true>(d, ws, stream);
+        case 256: return nt == 1 ? run<256, 1, true>(d, ws, stream) : cudaErrorNotSupported;
         default: return cudaErrorNotSupported;
     }
 }

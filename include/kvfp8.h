@@ -226,6 +226,41 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
     kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream);
 
 /*
+ * Multi-query (causal) paged attention over the FP8 cache: several new tokens per
+ * sequence, each attending to the cached tokens up to and including itself.
+ *
+ * Defined by: [P1] tests/test-fp8.cpp check_fp8_attention (a batch of new tokens, each
+ * attending to every past token up to itself, on K/V rounded through the cache format);
+ * the arithmetic is that of kvfp8_paged_decode_attention.
+ *
+ * Sequence b holds L = seq_lens[b] cached tokens (the new tokens already written), the last
+ * n_b = query_start_loc[b+1] - query_start_loc[b] of them new.  Its query token j
+ * (0 <= j < n_b) is row query_start_loc[b] + j of query and out, sits at position
+ * p = L - n_b + j, and attends to tokens t <= p:
+ *   out[row][h] = v_scale * sum_{t<=p} softmax_t(sm_scale*k_scale*q[row][h].dec(K_t)) dec(V_t)
+ * n_b = 1 for every sequence is kvfp8_paged_decode_attention.
+ *
+ * out, query        device bf16 [num_query_rows][n_q][head_dim]
+ * query_start_loc   device int32 [num_seqs + 1], non-decreasing; a sequence whose rows
+ *                   fall outside [0, num_query_rows) or number more than max_query_len is
+ *                   skipped and sets KVFP8_DEV_BAD_BLOCK; n_b > L also sets it (positions
+ *                   below zero attend to nothing and give zero rows)
+ * max_query_len     >= 1 with max_query_len * (n_q / n_kv) <= 16 (<= 8 at head_dim 256);
+ *                   larger prefill chunks return KVFP8_ERR_UNSUPPORTED
+ * workspace         >= kvfp8_paged_decode_workspace_size(num_seqs, n_q * max_query_len,
+ *                   head_dim) bytes
+ * Everything else as kvfp8_paged_decode_attention.
+ */
+KVFP8_API kvfp8_status kvfp8_paged_attention_multi(
+    void *out, const void *query, const int32_t *query_start_loc, int32_t num_query_rows,
+    int32_t max_query_len, const uint8_t *key_cache, const uint8_t *value_cache,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const int32_t *seq_lens,
+    int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float sm_scale, const void *k_scale, const void *v_scale,
+    kvfp8_dtype scale_dtype, void *workspace, size_t workspace_bytes, uint32_t *status,
+    kvfp8_stream_t stream);
+
+/*
  * Dequantize n E4M3 bytes: dst[i] = scale * E4M3dec(src[i]), product in fp32, then
  * rounded to dst_dtype (bf16: round to nearest even).  NaN codes give NaN.
  *
