@@ -71,7 +71,7 @@ struct DecodeArgs {
 // Workspace layout, shared by the size query and the launcher; rows = query rows per
 // sequence (n_q for decode, max query count * n_q for the multi-query form).
 struct DecodeWorkspace {
-    size_t cstart_off, lse_off, o_off, total;
+    size_t cstart_off, cta_off, lse_off, o_off, total;
 };
 DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t rows, int32_t head_dim);
 

@@ -77,12 +77,14 @@ struct KernelArgs {
     const void *v_scale;
     int32_t scale_dtype;
     const int32_t *cstart;
+    const int32_t *cta_seq;  // first sequence of each CTA's chunk range
     float *part_lse;
     float *part_o;
     uint32_t *status;
     int32_t num_ctas;
     int32_t stages;
     int32_t box_rows;  // 16, or 8 for 8-token blocks
+    int32_t whole_box;  // 1: one TMA box covers a chunk's rows for all heads (see host)
     // multi-query (causal) form: sequence b's query rows start at qsl[b] (nullptr: one
     // query per sequence, row b); rows_per_seq = max query count * n_q
     const int32_t *qsl;
@@ -213,8 +215,8 @@ __device__ __forceinline__ void pdl_trigger() {
 //  * the output rows of empty sequences are zeroed (no CTA visits them).
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t qrows,
-            int32_t num_seqs, int32_t max_len, int32_t *cstart, __nv_bfloat16 *out,
-            int32_t out_row_elems, uint32_t *status) {
+            int32_t num_seqs, int32_t max_len, int32_t num_ctas, int32_t *cstart,
+            int32_t *cta_seq, __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
     pdl_trigger();  // the decode grid may start its prologue; it waits for this grid's writes
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
@@ -274,6 +276,20 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
         __syncthreads();
     }
     if (tid == 0) cstart[num_seqs] = carry;
+    __syncthreads();  // cstart complete (block-visible)
+    // The first sequence of every decode CTA's chunk range: the last s with
+    // cstart[s] <= c*T/P, so a CTA starts with one load instead of a search.
+    const int64_t T = carry;
+    const int64_t P = T < num_ctas ? T : num_ctas;
+    for (int c = tid; c < P; c += blockDim.x) {
+        const int64_t lo_chunk = static_cast<int64_t>(c) * T / P;
+        int lo = 0, hi = num_seqs;  // invariant: cstart[lo] <= lo_chunk < cstart[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (cstart[mid] <= lo_chunk) lo = mid; else hi = mid;
+        }
+        cta_seq[c] = lo;
+    }
 }
 
 // The CTA whose chunk range contains chunk x (ranges are [c*T/P, (c+1)*T/P), P <= T).
@@ -408,13 +424,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         uint32_t phase = 0;
         bool aborted = false;
         if (chunk_lo < chunk_hi) {
-            // sequence holding chunk_lo: last s with cstart[s] <= chunk_lo
-            int lo = 0, hi = a.num_seqs;  // invariant: cstart[lo] <= chunk_lo < cstart[hi]
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (a.cstart[mid] <= chunk_lo) lo = mid; else hi = mid;
-            }
-            int s = lo;
+            int s = a.cta_seq[blockIdx.x];  // sequence holding chunk_lo (from the plan)
             int64_t cs = a.cstart[s], ce = a.cstart[s + 1];
             int L = min(max(a.seq_lens[s], 0), a.max_len);
             int wbase = -1 << 30;  // first block-table entry held in the lane window
@@ -469,12 +479,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                             mbar_arrive_tx(full, 2u * nloads * rows_bytes);
                             const uint32_t kst = base + static_cast<uint32_t>(stage) * stage_bytes;
                             const uint32_t vst = kst + chunk_bytes;
-                            for (int p = 0; p < nloads; ++p) {
-                                for (int g = 0; g < a.n_kv * SEGS; ++g) {
-                                    const uint32_t off = static_cast<uint32_t>(
-                                        g * kChunkTokens * SEG + p * a.box_rows * SEG);
-                                    tma_load_3d(kst + off, &tmk, 0, g, rows0[p], full);
-                                    tma_load_3d(vst + off, &tmv, 0, g, rows0[p], full);
+                            if (a.whole_box) {  // one box: every head segment, 16 rows
+                                tma_load_3d(kst, &tmk, 0, rows0[0], 0, full);
+                                tma_load_3d(vst, &tmv, 0, rows0[0], 0, full);
+                            } else {
+                                for (int p = 0; p < nloads; ++p) {
+                                    for (int g = 0; g < a.n_kv * SEGS; ++g) {
+                                        const uint32_t off = static_cast<uint32_t>(
+                                            g * kChunkTokens * SEG + p * a.box_rows * SEG);
+                                        tma_load_3d(kst + off, &tmk, 0, g, rows0[p], full);
+                                        tma_load_3d(vst + off, &tmv, 0, g, rows0[p], full);
+                                    }
                                 }
                             }
                         } else {
@@ -806,6 +821,30 @@ cudaError_t encode_cache_map(CUtensorMap *map, const uint8_t *cache, int64_t row
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The same bytes as a 3-D tensor ordered (SEG bytes, rows, segments) -- the segment
+// stride (SEG) below the row stride -- so that one [SEG x 16 rows x all segments] box
+// fetches a whole 16-token chunk into the same [segment][row][SEG] swizzled layout that
+// the per-segment boxes produce, with one TMA instruction instead of n_kv*head_dim/SEG.
+cudaError_t encode_cache_map_whole(CUtensorMap *map, const uint8_t *cache, int64_t rows,
+                                   int row_bytes, int seg) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const int segs = row_bytes / seg;
+    if (segs > 256) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seg), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(segs)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                                   static_cast<cuuint64_t>(seg)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(seg), static_cast<cuuint32_t>(kChunkTokens),
+                               static_cast<cuuint32_t>(segs)};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(cache),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           seg == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int env_int(const char *name, int dflt) {
     const char *v = std::getenv(name);
     return v ? std::atoi(v) : dflt;
@@ -854,10 +893,18 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     CUtensorMap tmk, tmv;
     const int box_rows = d.block_size >= kChunkTokens ? kChunkTokens : d.block_size;
     const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.block_size;
-    if ((err = encode_cache_map(&tmk, d.key_cache, rows, row_bytes, SEG, box_rows)) != cudaSuccess)
-        return err;
-    if ((err = encode_cache_map(&tmv, d.value_cache, rows, row_bytes, SEG, box_rows)) != cudaSuccess)
-        return err;
+    // whole-chunk boxes when a chunk never straddles blocks (and the driver accepts the
+    // map); otherwise one box per head segment
+    bool whole = box_rows == kChunkTokens && env_int("KVFP8_DECODE_SEGMENT_BOXES", 0) == 0 &&
+                 encode_cache_map_whole(&tmk, d.key_cache, rows, row_bytes, SEG) == cudaSuccess &&
+                 encode_cache_map_whole(&tmv, d.value_cache, rows, row_bytes, SEG) == cudaSuccess;
+    if (!whole) {
+        if ((err = encode_cache_map(&tmk, d.key_cache, rows, row_bytes, SEG, box_rows)) != cudaSuccess)
+            return err;
+        if ((err = encode_cache_map(&tmv, d.value_cache, rows, row_bytes, SEG, box_rows)) !=
+            cudaSuccess)
+            return err;
+    }
 
     uint8_t *w = static_cast<uint8_t *>(d.workspace);
     KernelArgs k;
@@ -878,18 +925,21 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.v_scale = d.v_scale;
     k.scale_dtype = d.scale_dtype;
     k.cstart = reinterpret_cast<const int32_t *>(w + ws.cstart_off);
+    k.cta_seq = reinterpret_cast<const int32_t *>(w + ws.cta_off);
     k.part_lse = reinterpret_cast<float *>(w + ws.lse_off);
     k.part_o = reinterpret_cast<float *>(w + ws.o_off);
     k.status = d.status;
     k.num_ctas = num_ctas;
     k.stages = stages;
     k.box_rows = box_rows;
+    k.whole_box = whole ? 1 : 0;
     k.qsl = d.qsl;
     k.rows_per_seq = d.qmax * d.n_q;
     k.qrows = d.qrows;
 
     plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs, k.max_len,
-                                        reinterpret_cast<int32_t *>(w + ws.cstart_off), k.out,
+                                        num_ctas, reinterpret_cast<int32_t *>(w + ws.cstart_off),
+                                        reinterpret_cast<int32_t *>(w + ws.cta_off), k.out,
                                         d.n_q * HD, d.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
@@ -922,7 +972,8 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
     const size_t parts = static_cast<size_t>(num_seqs) + kMaxDecodeCtas;
     DecodeWorkspace w;
     w.cstart_off = 0;
-    w.lse_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
+    w.cta_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
+    w.lse_off = w.cta_off + up(sizeof(int32_t) * kMaxDecodeCtas);
     w.o_off = w.lse_off + up(sizeof(float) * parts * n_q);
     w.total = w.o_off + up(sizeof(float) * parts * n_q * head_dim);
     return w;
