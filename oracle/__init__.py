@@ -68,6 +68,13 @@ def _load():
         lib.kvo_paged_attention_multi.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                                   i32, i32, f64, f32, f32]
         lib.kvo_paged_attention_multi.restype = u32
+        lib.kvo_reshape_and_cache_mixed.argtypes = [P, P, ctypes.c_int, i64, P, ctypes.c_int, P,
+                                                    ctypes.c_int, i32, i32, i32, i32, P, f32, f32]
+        lib.kvo_reshape_and_cache_mixed.restype = u32
+        lib.kvo_paged_decode_attention_mixed.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, P,
+                                                         i32, P, i32, i32, i32, i32, i32, i32, f64,
+                                                         f32, f32]
+        lib.kvo_paged_decode_attention_mixed.restype = u32
         lib.kvo_paged_decode_attention_pairs.argtypes = [P, P, i32, P, P, P, P, i32, P, i32, i32,
                                                          i32, i32, i32, f64, f32, f32]
         lib.kvo_paged_decode_attention_pairs.restype = u32
@@ -244,6 +251,50 @@ def paged_attention_multi(query, query_start_loc: np.ndarray, key_cache: np.ndar
         _ptr(out), _ptr(q), _ptr(qsl), _ptr(np.ascontiguousarray(key_cache)),
         _ptr(np.ascontiguousarray(value_cache)), _ptr(bt), bt.shape[1], _ptr(sl), sl.size, n_q,
         n_kv, hd, bs, num_blocks, float(sm_scale), float(np.float32(k_scale)),
+        float(np.float32(v_scale)))
+    return out, int(st)
+
+
+E4M3 = 0      # cache kinds for the mixed-dtype functions
+CACHE_BF16 = 1
+
+
+def reshape_and_cache_mixed(key, value, key_cache: np.ndarray, k_kind: int,
+                            value_cache: np.ndarray, v_kind: int, slot_mapping: np.ndarray,
+                            block_size: int, k_scale: float, v_scale: float,
+                            src_dtype: int = BF16) -> int:
+    """Store with a per-side cache kind: E4M3 (uint8 cache, scaled) or CACHE_BF16 (uint16
+    cache holding bf16 bits, unscaled).  Caches [num_blocks, block_size, n_kv, head_dim]."""
+    if src_dtype == BF16:
+        k, v = _as_u16(key), _as_u16(value)
+    else:
+        k = np.ascontiguousarray(key, dtype=np.float32)
+        v = np.ascontiguousarray(value, dtype=np.float32)
+    for c, kind in ((key_cache, k_kind), (value_cache, v_kind)):
+        assert c.dtype == (np.uint8 if kind == E4M3 else np.uint16) and c.flags["C_CONTIGUOUS"]
+    num_blocks, bs, n_kv, hd = key_cache.shape
+    assert bs == block_size and value_cache.shape == key_cache.shape
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return int(_load().kvo_reshape_and_cache_mixed(
+        _ptr(k), _ptr(v), src_dtype, k.shape[0], _ptr(key_cache), k_kind, _ptr(value_cache),
+        v_kind, num_blocks, block_size, n_kv, hd, _ptr(slots), float(np.float32(k_scale)),
+        float(np.float32(v_scale))))
+
+
+def paged_decode_attention_mixed(query, key_cache: np.ndarray, k_kind: int,
+                                 value_cache: np.ndarray, v_kind: int, block_tables: np.ndarray,
+                                 seq_lens: np.ndarray, k_scale: float, v_scale: float,
+                                 sm_scale: float = 0.0):
+    q = _as_u16(query)
+    num_seqs, n_q, hd = q.shape
+    num_blocks, bs, n_kv, _ = key_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    out = np.zeros((num_seqs, n_q, hd), dtype=np.float64)
+    st = _load().kvo_paged_decode_attention_mixed(
+        _ptr(out), _ptr(q), _ptr(np.ascontiguousarray(key_cache)), k_kind,
+        _ptr(np.ascontiguousarray(value_cache)), v_kind, _ptr(bt), bt.shape[1], _ptr(sl),
+        num_seqs, n_q, n_kv, hd, bs, num_blocks, float(sm_scale), float(np.float32(k_scale)),
         float(np.float32(v_scale)))
     return out, int(st)
 

@@ -385,6 +385,127 @@ uint32_t kvo_decode_one(double *out, const uint16_t *q_row, const uint8_t *key_c
     return status;
 }
 
+/* Mixed cache dtypes.  [P1] tests/test-fp8.cpp check_fp8_attention runs the FP8 cache on
+ * K only, on V only, or on both (type_k / type_v F8_E4M3 or F16), each FP8 side with its
+ * own scale and the other side unscaled; test-backend-ops adds the F8/F16 mixes.  Here the
+ * 16-bit side is bf16: the cache holds the source value rounded to bf16 (RNE; exact for a
+ * bf16 source) and reads back as that value, with no scale.
+ * kind: 0 = E4M3 bytes (scaled), 1 = bf16 (unscaled). */
+static double kvo_cache_value(const void *cache, int kind, int64_t idx, float scale)
+{
+    if (kind == 0)
+        return (double)scale * kvo_e4m3_decode(((const uint8_t *)cache)[idx]);
+    return (double)kvo_bf16_to_f32(((const uint16_t *)cache)[idx]);
+}
+
+/* reshape_and_cache with a per-side cache kind (see kvo_cache_value). */
+uint32_t kvo_reshape_and_cache_mixed(const void *key, const void *value, int src_dtype,
+                                     int64_t num_tokens, void *key_cache, int k_kind,
+                                     void *value_cache, int v_kind, int32_t num_blocks,
+                                     int32_t block_size, int32_t n_kv, int32_t head_dim,
+                                     const int64_t *slot_mapping, float k_scale, float v_scale)
+{
+    if ((k_kind == 0 && !kvo_scale_ok(k_scale)) || (v_kind == 0 && !kvo_scale_ok(v_scale)))
+        return KVO_BAD_SCALE;
+    uint32_t status = 0;
+    const int64_t row = (int64_t)n_kv * head_dim;
+    const int64_t num_slots = (int64_t)num_blocks * block_size;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot == -1)
+            continue;
+        if (slot < 0 || slot >= num_slots) {
+            status |= KVO_BAD_SLOT;
+            continue;
+        }
+        for (int64_t e = 0; e < row; ++e) {
+            const float kx = kvo_load_src(key, src_dtype, i * row + e);
+            const float vx = kvo_load_src(value, src_dtype, i * row + e);
+            if (k_kind == 0)
+                ((uint8_t *)key_cache)[slot * row + e] = kvo_store_code(kx, k_scale);
+            else
+                ((uint16_t *)key_cache)[slot * row + e] = kvo_f32_to_bf16(kx);
+            if (v_kind == 0)
+                ((uint8_t *)value_cache)[slot * row + e] = kvo_store_code(vx, v_scale);
+            else
+                ((uint16_t *)value_cache)[slot * row + e] = kvo_f32_to_bf16(vx);
+        }
+    }
+    return status;
+}
+
+/* Decode attention with a per-side cache kind; otherwise as kvo_paged_decode_attention. */
+uint32_t kvo_paged_decode_attention_mixed(double *out, const uint16_t *query,
+                                          const void *key_cache, int k_kind,
+                                          const void *value_cache, int v_kind,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+                                          int32_t n_kv, int32_t head_dim, int32_t block_size,
+                                          int32_t num_blocks, double sm_scale, float k_scale,
+                                          float v_scale)
+{
+    if ((k_kind == 0 && !kvo_scale_ok(k_scale)) || (v_kind == 0 && !kvo_scale_ok(v_scale)))
+        return KVO_BAD_SCALE;
+    if (sm_scale <= 0.0)
+        sm_scale = 1.0 / sqrt((double)head_dim);
+    uint32_t status = 0;
+    const int32_t group = n_q / n_kv;
+    const int64_t row = (int64_t)n_kv * head_dim;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int32_t len = seq_lens[b];
+        if (len > max_blocks_per_seq * block_size) {
+            status |= KVO_BAD_BLOCK;
+            len = max_blocks_per_seq * block_size;
+        }
+        if (len < 0)
+            len = 0;
+        const int32_t *bt = block_tables + (int64_t)b * max_blocks_per_seq;
+        double *score = (double *)malloc(sizeof(double) * (size_t)(len > 0 ? len : 1));
+        for (int32_t h = 0; h < n_q; ++h) {
+            const int32_t kvh = h / group;
+            const uint16_t *q = query + ((int64_t)b * n_q + h) * head_dim;
+            double *o = out + ((int64_t)b * n_q + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            if (len == 0)
+                continue;
+            double best = -INFINITY;
+            for (int32_t t = 0; t < len; ++t) {
+                const int32_t phys = bt[t / block_size];
+                if (phys < 0 || phys >= num_blocks) {  /* token left out, flagged */
+                    status |= KVO_BAD_BLOCK;
+                    score[t] = -INFINITY;
+                    continue;
+                }
+                const int64_t base = ((int64_t)phys * block_size + t % block_size) * row +
+                                     (int64_t)kvh * head_dim;
+                double dot = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    dot += (double)kvo_bf16_to_f32(q[d]) * kvo_cache_value(key_cache, k_kind, base + d, k_scale);
+                score[t] = sm_scale * dot;
+                if (score[t] > best)
+                    best = score[t];
+            }
+            double denom = 0.0;
+            for (int32_t t = 0; t < len; ++t) {
+                score[t] = exp(score[t] - best);
+                denom += score[t];
+            }
+            for (int32_t t = 0; t < len; ++t) {
+                if (score[t] == 0.0)
+                    continue;
+                const int64_t base = ((int64_t)bt[t / block_size] * block_size + t % block_size) * row +
+                                     (int64_t)kvh * head_dim;
+                const double p = score[t] / denom;
+                for (int32_t d = 0; d < head_dim; ++d)
+                    o[d] += p * kvo_cache_value(value_cache, v_kind, base + d, v_scale);
+            }
+        }
+        free(score);
+    }
+    return status;
+}
+
 /* Whole-batch decode attention: out is [num_seqs][n_q][head_dim] doubles,
  * query is [num_seqs][n_q][head_dim] bf16, block_tables is
  * [num_seqs][max_blocks_per_seq] int32.  sm_scale <= 0 selects
