@@ -6,6 +6,8 @@ built library and fails loudly without it.
 """
 from .binding import (  # noqa: F401
     ABI_FUNCTIONS,
+    CACHE_BF16,
+    CACHE_E4M3,
     DEV_BAD_BLOCK,
     DEV_BAD_SCALE,
     DEV_BAD_SLOT,
@@ -17,9 +19,11 @@ from .binding import (  # noqa: F401
     dequant,
     paged_attention_multi,
     paged_decode_attention,
+    paged_decode_attention_mixed,
     paged_decode_attention_noalloc,
     paged_decode_workspace_size,
     reshape_and_cache,
+    reshape_and_cache_mixed,
     rope_reshape_and_cache,
     status_string,
 )

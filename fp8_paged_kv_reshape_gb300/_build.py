@@ -15,9 +15,9 @@ LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libkvfp8.so")
 HEADER = os.path.join(ROOT, "include", "kvfp8.h")
 
-SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "dequant.cu",
-           "decode_noalloc.cu"]
-DEPS = ["kvfp8_device.cuh", "kvfp8_internal.h"]
+SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "paged_decode_mixed.cu",
+           "dequant.cu", "decode_noalloc.cu"]
+DEPS = ["kvfp8_device.cuh", "kvfp8_internal.h", "paged_decode_kernel.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -18,6 +18,8 @@ ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_SCALE, ERR_ALIGN, ERR_WORKSPACE, ERR_CUDA, E
     range(1, 9)
 BF16 = 0
 F32 = 1
+CACHE_E4M3 = 0
+CACHE_BF16 = 1
 
 DEV_BAD_SCALE = 1 << 0
 DEV_BAD_SLOT = 1 << 1
@@ -32,6 +34,8 @@ ABI_FUNCTIONS = (
     "kvfp8_paged_decode_attention",
     "kvfp8_paged_decode_attention_noalloc",
     "kvfp8_paged_attention_multi",
+    "kvfp8_reshape_and_cache_mixed",
+    "kvfp8_paged_decode_attention_mixed",
     "kvfp8_dequant",
     "kvfp8_check_scale_host",
     "kvfp8_status_string",
@@ -72,6 +76,14 @@ def _load() -> ctypes.CDLL:
                                                 i32, i32, i32, f32, P, P, ctypes.c_int, P, sz, P,
                                                 P]
     lib.kvfp8_paged_attention_multi.restype = ctypes.c_int
+    lib.kvfp8_reshape_and_cache_mixed.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P,
+                                                  ctypes.c_int, P, ctypes.c_int, i32, i32, i32,
+                                                  i32, P, P, P, ctypes.c_int, P, P]
+    lib.kvfp8_reshape_and_cache_mixed.restype = ctypes.c_int
+    lib.kvfp8_paged_decode_attention_mixed.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_int, P,
+                                                       i32, P, i32, i32, i32, i32, i32, i32, f32,
+                                                       P, P, ctypes.c_int, P, sz, P, P]
+    lib.kvfp8_paged_decode_attention_mixed.restype = ctypes.c_int
     lib.kvfp8_dequant.argtypes = [P, ctypes.c_int, P, i64, P, ctypes.c_int, P]
     lib.kvfp8_dequant.restype = ctypes.c_int
     lib.kvfp8_check_scale_host.argtypes = [f32]
@@ -298,6 +310,88 @@ def paged_decode_attention_noalloc(query: torch.Tensor, key_cache: torch.Tensor,
         block_tables.shape[1], _ptr(seq_lens), num_seqs, n_q, n_kv, hd, bs, num_blocks,
         float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(status), _stream(stream))
     _check(rc, "kvfp8_paged_decode_attention_noalloc")
+    return out
+
+
+def _cache_kind(t: torch.Tensor) -> int:
+    if t.dtype == torch.uint8:
+        return CACHE_E4M3
+    if t.dtype == torch.bfloat16:
+        return CACHE_BF16
+    raise TypeError("a cache is uint8 (E4M3 codes) or bfloat16")
+
+
+def _check_mixed_caches(key_cache: torch.Tensor, value_cache: torch.Tensor):
+    if key_cache.dim() != 4 or value_cache.shape != key_cache.shape:
+        raise ValueError("caches must be [num_blocks, block_size, n_kv, head_dim]")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
+    return _cache_kind(key_cache), _cache_kind(value_cache)
+
+
+def reshape_and_cache_mixed(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                            k_scale: torch.Tensor | None = None,
+                            v_scale: torch.Tensor | None = None,
+                            status: torch.Tensor | None = None, stream=None) -> None:
+    """kvfp8_reshape_and_cache_mixed: each cache's dtype picks its side's format (uint8 =
+    E4M3 with that side's scale, bfloat16 = the value rounded to bf16, no scale)."""
+    if key.dtype != value.dtype or key.dtype not in (torch.bfloat16, torch.float32):
+        raise TypeError("key and value must share one dtype, bfloat16 or float32")
+    if key.dim() != 3 or value.shape != key.shape:
+        raise ValueError("key/value must be [num_tokens, n_kv, head_dim] with equal shapes")
+    n, n_kv, hd = key.shape
+    for t in (key, value):
+        if t.stride(2) != 1 or t.stride(1) != hd:
+            raise ValueError("key/value inner dims [n_kv, head_dim] must be dense")
+    kk, vk = _check_mixed_caches(key_cache, value_cache)
+    if tuple(key_cache.shape[2:]) != (n_kv, hd):
+        raise ValueError("caches must be [num_blocks, block_size, n_kv, head_dim]")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != n or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 [num_tokens] tensor")
+    sdt = _scale_args(k_scale, v_scale)
+    rc = LIB.kvfp8_reshape_and_cache_mixed(
+        _ptr(key), _ptr(value), F32 if key.dtype == torch.float32 else BF16,
+        key.stride(0) if n > 0 else n_kv * hd, value.stride(0) if n > 0 else n_kv * hd, n,
+        _ptr(key_cache), kk, _ptr(value_cache), vk, key_cache.shape[0], key_cache.shape[1], n_kv,
+        hd, _ptr(slot_mapping), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(status), _stream(stream))
+    _check(rc, "kvfp8_reshape_and_cache_mixed")
+
+
+def paged_decode_attention_mixed(query: torch.Tensor, key_cache: torch.Tensor,
+                                 value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                 seq_lens: torch.Tensor, k_scale: torch.Tensor | None = None,
+                                 v_scale: torch.Tensor | None = None, sm_scale: float = 0.0,
+                                 out: torch.Tensor | None = None,
+                                 workspace: torch.Tensor | None = None,
+                                 status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvfp8_paged_decode_attention_mixed: decode attention where each cache's dtype picks
+    its side's format (uint8 = E4M3, scaled; bfloat16 = unscaled)."""
+    if query.dtype != torch.bfloat16 or query.dim() != 3 or not query.is_contiguous():
+        raise ValueError("query must be a contiguous bf16 [num_seqs, n_q, head_dim] tensor")
+    num_seqs, n_q, hd = query.shape
+    kk, vk = _check_mixed_caches(key_cache, value_cache)
+    if key_cache.shape[3] != hd:
+        raise ValueError("caches must be [num_blocks, block_size, n_kv, head_dim]")
+    num_blocks, bs, n_kv, _ = key_cache.shape
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != num_seqs or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks] tensor")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != num_seqs or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 [num_seqs] tensor")
+    if out is None:
+        out = torch.empty_like(query)
+    need = paged_decode_workspace_size(num_seqs, n_q, hd)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
+    sdt = _scale_args(k_scale, v_scale)
+    rc = LIB.kvfp8_paged_decode_attention_mixed(
+        _ptr(out), _ptr(query), _ptr(key_cache), kk, _ptr(value_cache), vk, _ptr(block_tables),
+        block_tables.shape[1], _ptr(seq_lens), num_seqs, n_q, n_kv, hd, bs, num_blocks,
+        float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    _check(rc, "kvfp8_paged_decode_attention_mixed")
     return out
 
 

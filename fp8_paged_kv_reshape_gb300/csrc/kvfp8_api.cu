@@ -21,6 +21,8 @@ kvfp8_status from_cuda(cudaError_t e) {
     return KVFP8_ERR_CUDA;
 }
 
+bool cache_dtype_ok(kvfp8_cache_dtype t) { return t == KVFP8_CACHE_E4M3 || t == KVFP8_CACHE_BF16; }
+
 bool block_size_ok_for_decode(int32_t bs) {
     return bs == 8 || bs == 16 || bs == 32 || bs == 64 || bs == 128 || bs == 256;
 }
@@ -71,6 +73,8 @@ kvfp8_status kvfp8_reshape_and_cache(const void *key, const void *value, kvfp8_d
     a.rot = 0;
     a.neox = 0;
     a.head_dim = head_dim;
+    a.k_bf16 = 0;
+    a.v_bf16 = 0;
     return from_cuda(kvfp8::launch_reshape_and_cache(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -121,6 +125,8 @@ kvfp8_status kvfp8_rope_reshape_and_cache(
     a.rot = rot_dim;
     a.neox = is_neox ? 1 : 0;
     a.head_dim = head_dim;
+    a.k_bf16 = 0;
+    a.v_bf16 = 0;
     return from_cuda(kvfp8::launch_reshape_and_cache(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -183,6 +189,8 @@ kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const ui
     d.qsl = nullptr;
     d.qmax = 1;
     d.qrows = num_seqs;
+    d.k_bf16 = 0;
+    d.v_bf16 = 0;
     return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -241,6 +249,118 @@ kvfp8_status kvfp8_paged_attention_multi(
     d.qsl = query_start_loc;
     d.qmax = max_query_len;
     d.qrows = num_query_rows;
+    d.k_bf16 = 0;
+    d.v_bf16 = 0;
+    return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvfp8_status kvfp8_reshape_and_cache_mixed(
+    const void *key, const void *value, kvfp8_dtype src_dtype, int64_t key_stride,
+    int64_t value_stride, int64_t num_tokens, void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    void *value_cache, kvfp8_cache_dtype v_cache_dtype, int32_t num_blocks, int32_t block_size,
+    int32_t n_kv, int32_t head_dim, const int64_t *slot_mapping, const void *k_scale,
+    const void *v_scale, kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream) {
+    if (!dtype_ok(src_dtype) || !dtype_ok(scale_dtype) || !cache_dtype_ok(k_cache_dtype) ||
+        !cache_dtype_ok(v_cache_dtype))
+        return KVFP8_ERR_DTYPE;
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || block_size > 1024 || n_kv < 1 ||
+        head_dim < 1)
+        return KVFP8_ERR_SHAPE;
+    const int64_t row = static_cast<int64_t>(n_kv) * head_dim;
+    if (row % 8 != 0 || key_stride < row || value_stride < row) return KVFP8_ERR_SHAPE;
+    if (row > 2048) return KVFP8_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return KVFP8_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping) return KVFP8_ERR_NULL;
+    const int64_t esz = src_dtype == KVFP8_F32 ? 4 : 2;
+    if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache) ||
+        (key_stride * esz) % 16 != 0 || (value_stride * esz) % 16 != 0 || !aligned(slot_mapping, 8))
+        return KVFP8_ERR_ALIGN;
+    kvfp8::ReshapeArgs a;
+    a.key = key;
+    a.value = value;
+    a.src_dtype = src_dtype;
+    a.key_stride = key_stride;
+    a.value_stride = value_stride;
+    a.num_tokens = num_tokens;
+    a.key_cache = static_cast<uint8_t *>(key_cache);
+    a.value_cache = static_cast<uint8_t *>(value_cache);
+    a.num_slots = static_cast<int64_t>(num_blocks) * block_size;
+    a.row_elems = static_cast<int32_t>(row);
+    a.slot_mapping = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.scale_dtype = scale_dtype;
+    a.status = status;
+    a.positions = nullptr;
+    a.cos_sin = nullptr;
+    a.max_pos = 0;
+    a.rot = 0;
+    a.neox = 0;
+    a.head_dim = head_dim;
+    a.k_bf16 = k_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
+    a.v_bf16 = v_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
+    return from_cuda(kvfp8::launch_reshape_and_cache(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvfp8_status kvfp8_paged_decode_attention_mixed(
+    void *out, const void *query, const void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    const void *value_cache, kvfp8_cache_dtype v_cache_dtype, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+    int32_t n_kv, int32_t head_dim, int32_t block_size, int32_t num_blocks, float sm_scale,
+    const void *k_scale, const void *v_scale, kvfp8_dtype scale_dtype, void *workspace,
+    size_t workspace_bytes, uint32_t *status, kvfp8_stream_t stream) {
+    if (!cache_dtype_ok(k_cache_dtype) || !cache_dtype_ok(v_cache_dtype)) return KVFP8_ERR_DTYPE;
+    if (k_cache_dtype == KVFP8_CACHE_E4M3 && v_cache_dtype == KVFP8_CACHE_E4M3)
+        return kvfp8_paged_decode_attention(
+            out, query, static_cast<const uint8_t *>(key_cache),
+            static_cast<const uint8_t *>(value_cache), block_tables, max_blocks_per_seq, seq_lens,
+            num_seqs, n_q, n_kv, head_dim, block_size, num_blocks, sm_scale, k_scale, v_scale,
+            scale_dtype, workspace, workspace_bytes, status, stream);
+    if (!dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || n_q / n_kv > 16 ||
+        num_blocks < 1 || max_blocks_per_seq < 1)
+        return KVFP8_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
+    if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
+    if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
+        static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
+        return KVFP8_ERR_SHAPE;
+    if (k_cache_dtype == v_cache_dtype || head_dim == 256 || n_kv > 8) return KVFP8_ERR_UNSUPPORTED;
+    if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
+    if (num_seqs == 0) return KVFP8_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !workspace)
+        return KVFP8_ERR_NULL;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
+        !aligned16(value_cache) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+        !aligned16(workspace))
+        return KVFP8_ERR_ALIGN;
+    if (workspace_bytes < kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim))
+        return KVFP8_ERR_WORKSPACE;
+    kvfp8::DecodeArgs d;
+    d.out = out;
+    d.query = query;
+    d.key_cache = static_cast<const uint8_t *>(key_cache);
+    d.value_cache = static_cast<const uint8_t *>(value_cache);
+    d.block_tables = block_tables;
+    d.max_blocks_per_seq = max_blocks_per_seq;
+    d.seq_lens = seq_lens;
+    d.num_seqs = num_seqs;
+    d.n_q = n_q;
+    d.n_kv = n_kv;
+    d.head_dim = head_dim;
+    d.block_size = block_size;
+    d.num_blocks = num_blocks;
+    d.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    d.k_scale = k_scale;
+    d.v_scale = v_scale;
+    d.scale_dtype = scale_dtype;
+    d.workspace = workspace;
+    d.status = status;
+    d.qsl = nullptr;
+    d.qmax = 1;
+    d.qrows = num_seqs;
+    d.k_bf16 = k_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
+    d.v_bf16 = v_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
     return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -31,6 +31,9 @@ struct ReshapeArgs {
     int32_t rot;
     int32_t neox;
     int32_t head_dim;
+    // mixed cache dtypes: 1 = that side's cache is bf16 (unscaled), 0 = E4M3
+    int32_t k_bf16;
+    int32_t v_bf16;
 };
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream);
@@ -66,6 +69,9 @@ struct DecodeArgs {
     const int32_t *qsl;
     int32_t qmax;
     int32_t qrows;  // rows of query and out
+    // mixed cache dtypes: 1 = that side's cache is bf16 (2 bytes per element, no scale)
+    int32_t k_bf16;
+    int32_t v_bf16;
 };
 
 // Workspace layout, shared by the size query and the launcher; rows = query rows per
@@ -78,6 +84,8 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t rows, int32_t 
 // Returns cudaErrorNotSupported for a shape without a kernel instance, or the first
 // CUDA error met while encoding tensor maps / launching.
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t stream);
+// The mixed-dtype instances (exactly one of k_bf16 / v_bf16 set); called by the above.
+cudaError_t launch_paged_decode_mixed(const DecodeArgs &a, cudaStream_t stream);
 
 cudaError_t launch_dequant(void *dst, int dst_dtype, const uint8_t *src, int64_t n,
                            const void *scale, int scale_dtype, cudaStream_t stream);

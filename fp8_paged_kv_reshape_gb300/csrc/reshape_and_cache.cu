@@ -158,6 +158,30 @@ __device__ __forceinline__ void load_row(Group<kF32> (&buf)[U], const RowCtx &c,
     }
 }
 
+// A side whose cache is bf16 (mixed cache dtypes): the row is stored at 16 bits, rounded to
+// bf16 (a bf16 source is copied unchanged), with no scale.
+template <bool kF32, int U>
+__device__ __forceinline__ void store_row_bf16(const Group<kF32> (&buf)[U], const RowCtx &c,
+                                               int64_t slot, int row_elems, int groups, int lane) {
+    uint8_t *dst = c.cache + slot * row_elems * 2;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int g = lane + 32 * u;
+        if (g < groups) {
+            uint4 w;
+            if constexpr (kF32) {
+                float x[8];
+                buf[u].unpack(x);
+                w = make_uint4(bf16x2_from_f32(x[0], x[1]), bf16x2_from_f32(x[2], x[3]),
+                               bf16x2_from_f32(x[4], x[5]), bf16x2_from_f32(x[6], x[7]));
+            } else {
+                w = buf[u].v;
+            }
+            *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * 16) = w;
+        }
+    }
+}
+
 template <bool kF32, int U, bool kFast>
 __device__ __forceinline__ void store_row(const Group<kF32> (&buf)[U], const RowCtx &c,
                                           const FastDiv &fd, int64_t slot, int row_elems,
@@ -180,10 +204,12 @@ __device__ __forceinline__ bool fast_range(float s) {
     return sa >= 0x1p-60f && sa <= 0x1p60f;
 }
 
-// The rows of one warp (every stride-th row from r), two in flight.
-template <bool kF32, int U, bool kFast>
+// The rows of one warp (every stride-th row from r), two in flight.  kMode: 0 = E4M3 with
+// the fast divide, 1 = E4M3 with __fdiv_rn, 2 = bf16 cache (mixed cache dtypes).
+template <bool kF32, int U, int kMode>
 __device__ __forceinline__ void pipelined_rows(const ReshapeArgs &a, const RowCtx &c, int64_t r,
                                                int64_t stride, int64_t rows, int lane) {
+    constexpr bool kFast = kMode == 0;
     const FastDiv fd(c.s);
     const int groups = a.row_elems >> 3;
     Group<kF32> A[U], B[U];
@@ -196,14 +222,20 @@ __device__ __forceinline__ void pipelined_rows(const ReshapeArgs &a, const RowCt
         bool ok2 = rn < rows && row_ok(a, rn, s2, lane);
         if (ok2) load_row<kF32, U>(B, c, rn, groups, lane);
         int64_t s3 = slot_of(a, rn + stride, rows);
-        if (ok1) store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
+        if (ok1) {
+            if (kMode == 2) store_row_bf16<kF32, U>(A, c, s1, a.row_elems, groups, lane);
+            else store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
+        }
         r = rn; s1 = s2; s2 = s3; ok1 = ok2;
         if (r >= rows) break;
         rn = r + stride;
         ok2 = rn < rows && row_ok(a, rn, s2, lane);
         if (ok2) load_row<kF32, U>(A, c, rn, groups, lane);
         s3 = slot_of(a, rn + stride, rows);
-        if (ok1) store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
+        if (ok1) {
+            if (kMode == 2) store_row_bf16<kF32, U>(B, c, s1, a.row_elems, groups, lane);
+            else store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
+        }
         r = rn; s1 = s2; s2 = s3; ok1 = ok2;
     }
 }
@@ -213,7 +245,7 @@ template <bool kF32, int U>
 __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const ReshapeArgs a) {
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
-    if (!scale_ok(sk) || !scale_ok(sv)) {
+    if ((!a.k_bf16 && !scale_ok(sk)) || (!a.v_bf16 && !scale_ok(sv))) {
         if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
         return;
     }
@@ -227,10 +259,12 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const Re
     c.cache = is_v ? a.value_cache : a.key_cache;
     c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
     c.s = is_v ? sv : sk;
-    if (fast_range(c.s))  // uniform per warp
-        pipelined_rows<kF32, U, true>(a, c, r, stride, rows, lane);
+    if (is_v ? a.v_bf16 : a.k_bf16)  // uniform per warp
+        pipelined_rows<kF32, U, 2>(a, c, r, stride, rows, lane);
+    else if (fast_range(c.s))
+        pipelined_rows<kF32, U, 0>(a, c, r, stride, rows, lane);
     else
-        pipelined_rows<kF32, U, false>(a, c, r, stride, rows, lane);
+        pipelined_rows<kF32, U, 1>(a, c, r, stride, rows, lane);
 }
 
 // ---------------------------------------------------------------- rope + cache write
@@ -451,6 +485,8 @@ cudaError_t dispatch_rope(const ReshapeArgs &a, cudaStream_t stream) {
 
 cudaError_t launch_reshape_and_cache(const ReshapeArgs &a, cudaStream_t stream) {
     if (a.num_tokens == 0) return cudaSuccess;
+    if ((a.k_bf16 || a.v_bf16) && (a.cos_sin != nullptr || a.row_elems > 2048))
+        return cudaErrorNotSupported;  // mixed dtypes: the pipelined plain store only
     if (a.cos_sin != nullptr)
         return a.src_dtype == KVFP8_F32 ? dispatch_rope<true>(a, stream)
                                         : dispatch_rope<false>(a, stream);

@@ -72,6 +72,12 @@ typedef enum {
     KVFP8_F32 = 1
 } kvfp8_dtype;
 
+/* Element type of one side's cache in the mixed-dtype calls. */
+typedef enum {
+    KVFP8_CACHE_E4M3 = 0, /* uint8 E4M3 codes, dequantized by that side's scale */
+    KVFP8_CACHE_BF16 = 1  /* bf16 values, no scale */
+} kvfp8_cache_dtype;
+
 /* Bits ORed into the optional device status word. */
 #define KVFP8_DEV_BAD_SCALE (1u << 0) /* a device scale was zero or not finite: nothing written */
 #define KVFP8_DEV_BAD_SLOT  (1u << 1) /* a slot outside [-1, num_blocks*block_size): row skipped */
@@ -259,6 +265,50 @@ KVFP8_API kvfp8_status kvfp8_paged_attention_multi(
     int32_t num_blocks, float sm_scale, const void *k_scale, const void *v_scale,
     kvfp8_dtype scale_dtype, void *workspace, size_t workspace_bytes, uint32_t *status,
     kvfp8_stream_t stream);
+
+/*
+ * Mixed cache dtypes: FP8 on one side only.
+ *
+ * Defined by: [P1] tests/test-fp8.cpp check_fp8_attention, which quantizes K only, V only
+ * or both (type_k / type_v F8_E4M3 or F16, the FP8 side with its own scale, the other
+ * unscaled), and tests/test-backend-ops.cpp, which adds the F8/F16 cache mixes.  Here the
+ * 16-bit side is bf16.
+ *
+ * A KVFP8_CACHE_BF16 side's cache is bf16 [num_blocks][block_size][n_kv][head_dim] (two
+ * bytes per element, so slot s owns the 2*n_kv*head_dim bytes at 2*s*n_kv*head_dim); its
+ * scale pointer is ignored (may be NULL) and never checked.  The KVFP8_CACHE_E4M3 side is
+ * exactly as in the all-FP8 calls.
+ *
+ * kvfp8_reshape_and_cache_mixed: as kvfp8_reshape_and_cache; a bf16 side stores the
+ * source value rounded to bf16 (round to nearest even; a bf16 source is copied as it is;
+ * a NaN stays a NaN, its payload unspecified).  n_kv*head_dim <= 2048, else
+ * KVFP8_ERR_UNSUPPORTED.
+ */
+KVFP8_API kvfp8_status kvfp8_reshape_and_cache_mixed(
+    const void *key, const void *value, kvfp8_dtype src_dtype, int64_t key_stride,
+    int64_t value_stride, int64_t num_tokens, void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    void *value_cache, kvfp8_cache_dtype v_cache_dtype, int32_t num_blocks, int32_t block_size,
+    int32_t n_kv, int32_t head_dim, const int64_t *slot_mapping, const void *k_scale,
+    const void *v_scale, kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream);
+
+/*
+ * kvfp8_paged_decode_attention with a per-side cache dtype:
+ *   s_t = sm_scale * sum_d q[b][h][d] * Kval(t, kv, d),  out = sum_t softmax(s)_t Vval(t, kv, d)
+ * where an E4M3 side's value is scale * E4M3dec(byte) and a bf16 side's is the stored bf16.
+ * A bf16 K enters the tensor cores against bf16 q (exact products); a bf16 V against the
+ * probabilities split into two bf16 parts (16 significant bits).
+ * This build: exactly one side bf16 (both E4M3 is kvfp8_paged_decode_attention; both
+ * bf16 returns KVFP8_ERR_UNSUPPORTED), head_dim 64 or 128, n_q/n_kv <= 16, n_kv <= 8.
+ * Workspace: kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim).  Everything else
+ * as kvfp8_paged_decode_attention.
+ */
+KVFP8_API kvfp8_status kvfp8_paged_decode_attention_mixed(
+    void *out, const void *query, const void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    const void *value_cache, kvfp8_cache_dtype v_cache_dtype, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+    int32_t n_kv, int32_t head_dim, int32_t block_size, int32_t num_blocks, float sm_scale,
+    const void *k_scale, const void *v_scale, kvfp8_dtype scale_dtype, void *workspace,
+    size_t workspace_bytes, uint32_t *status, kvfp8_stream_t stream);
 
 /*
  * Dequantize n E4M3 bytes: dst[i] = scale * E4M3dec(src[i]), product in fp32, then

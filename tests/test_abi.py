@@ -130,3 +130,47 @@ def test_dequant_host_validation():
     assert lib.kvfp8_dequant(ctypes.c_void_p(16), binding.F32, ctypes.c_void_p(16), -1, None, 0, None) == binding.ERR_SHAPE
     assert lib.kvfp8_dequant(ctypes.c_void_p(16), binding.F32, ctypes.c_void_p(17), 16, None, 0, None) == binding.ERR_ALIGN
     assert lib.kvfp8_dequant(None, binding.F32, None, 0, None, 0, None) == binding.OK
+
+
+def test_mixed_reshape_host_validation():
+    def call(**over):
+        args = dict(key=ctypes.c_void_p(16), value=ctypes.c_void_p(16), src_dtype=binding.BF16,
+                    key_stride=1024, value_stride=1024, num_tokens=4,
+                    key_cache=ctypes.c_void_p(16), k_kind=binding.CACHE_BF16,
+                    value_cache=ctypes.c_void_p(16), v_kind=binding.CACHE_E4M3, num_blocks=4,
+                    block_size=16, n_kv=8, head_dim=128, slot_mapping=ctypes.c_void_p(16),
+                    k_scale=None, v_scale=None, scale_dtype=binding.F32, status=None, stream=None)
+        args.update(over)
+        return kv.LIB.kvfp8_reshape_and_cache_mixed(*args.values())
+    assert call(k_kind=2) == binding.ERR_DTYPE
+    assert call(v_kind=-1) == binding.ERR_DTYPE
+    assert call(key_cache=None) == binding.ERR_NULL
+    assert call(n_kv=1, head_dim=3) == binding.ERR_SHAPE
+    assert call(n_kv=32, key_stride=4096, value_stride=4096) == binding.ERR_UNSUPPORTED
+    assert call(value_cache=ctypes.c_void_p(8)) == binding.ERR_ALIGN
+    assert call(num_tokens=0, key=None) == binding.OK
+
+
+def test_mixed_decode_host_validation():
+    def call(**over):
+        args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16),
+                    key_cache=ctypes.c_void_p(16), k_kind=binding.CACHE_E4M3,
+                    value_cache=ctypes.c_void_p(16), v_kind=binding.CACHE_BF16,
+                    block_tables=ctypes.c_void_p(16), max_blocks_per_seq=256,
+                    seq_lens=ctypes.c_void_p(16), num_seqs=4, n_q=32, n_kv=8, head_dim=128,
+                    block_size=16, num_blocks=1024, sm_scale=0.0, k_scale=None, v_scale=None,
+                    scale_dtype=binding.F32, workspace=ctypes.c_void_p(16),
+                    workspace_bytes=1 << 30, status=None, stream=None)
+        args.update(over)
+        return kv.LIB.kvfp8_paged_decode_attention_mixed(*args.values())
+    assert call(k_kind=5) == binding.ERR_DTYPE
+    assert call(k_kind=binding.CACHE_BF16, v_kind=binding.CACHE_BF16) == binding.ERR_UNSUPPORTED
+    assert call(head_dim=256) == binding.ERR_UNSUPPORTED
+    assert call(head_dim=96) == binding.ERR_SHAPE
+    assert call(n_q=30) == binding.ERR_SHAPE
+    assert call(query=None) == binding.ERR_NULL
+    assert call(value_cache=ctypes.c_void_p(24)) == binding.ERR_ALIGN
+    assert call(workspace_bytes=100) == binding.ERR_WORKSPACE
+    assert call(num_seqs=0, query=None) == binding.OK
+    # both sides E4M3 is the all-FP8 call, with its own validation
+    assert call(v_kind=binding.CACHE_E4M3, head_dim=96) == binding.ERR_SHAPE
