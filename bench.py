@@ -10,6 +10,15 @@ Default workload: llama3_8b (32 q / 8 kv heads, head_dim 128, block 16, 64 seque
 4096 tokens; the step writes all 262144 context rows and decodes 64 queries).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--variant fp8|rope|k_bf16|v_bf16|multi]
+
+--variant swaps in one of the widened forms of the path (same workload, same metric):
+  fp8     (default) reshape_and_cache + paged_decode_attention, both caches E4M3
+  rope    rope on K fused into the cache write (rope_reshape_and_cache), then decode
+  k_bf16  mixed cache dtypes, K cache bf16 and V E4M3 (reshape_and_cache_mixed +
+          paged_decode_attention_mixed); v_bf16 the other way round
+  multi   causal multi-query attention (paged_attention_multi) with 16 // G query
+          tokens per sequence (G = n_q / n_kv), after the same cache write
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, weak
 scaling, no collective on the data path); the time is the max over ranks.
@@ -39,30 +48,63 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
     "reshape_and_cache": ["fp8_paged_kv_reshape_gb300/csrc/reshape_and_cache.cu",
                           "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
-    "paged_decode_attention": ["fp8_paged_kv_reshape_gb300/csrc/paged_decode.cu",
+    "paged_decode_attention": ["fp8_paged_kv_reshape_gb300/csrc/paged_decode_kernel.cuh",
                                "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
 }
+VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi")
+METRIC = "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak"
 
 
 # ----------------------------------------------------------------- byte accounting
 
-def reshape_bytes(w: workloads.Workload, slot_mapping: np.ndarray, src_elem: int = 2) -> int:
-    """Algorithmic bytes of one reshape_and_cache: per valid row K+V read at src_elem bytes and
-    written at 1 byte each, plus the 8-byte slot of every row (padding rows read only it)."""
+def reshape_bytes(w: workloads.Workload, slot_mapping: np.ndarray, src_elem: int = 2,
+                  k_elem: int = 1, v_elem: int = 1, positions: np.ndarray | None = None,
+                  rot: int = 0) -> int:
+    """Algorithmic bytes of one cache write: per valid row K+V read at src_elem bytes and
+    written at k_elem / v_elem bytes (1 for E4M3, 2 for a bf16 side), plus the 8-byte slot of
+    every row (padding rows read only it).  The rope-fused write also reads every row's
+    8-byte position and, once, the float32 table row of every distinct position."""
     row = w.n_kv * w.head_dim
-    valid = int(np.count_nonzero(slot_mapping >= 0))
-    return valid * row * (2 * src_elem + 2) + 8 * int(slot_mapping.size)
+    ok = slot_mapping >= 0
+    valid = int(np.count_nonzero(ok))
+    n = valid * row * (2 * src_elem + k_elem + v_elem) + 8 * int(slot_mapping.size)
+    if positions is not None:
+        n += 8 * int(slot_mapping.size) + 4 * rot * int(np.unique(positions[ok]).size)
+    return n
 
 
-def decode_bytes(w: workloads.Workload, seq_lens: np.ndarray) -> int:
-    """Algorithmic bytes of one decode call: every cached K and V byte of every sequence, its
-    block-table entries and length, the bf16 query in and the bf16 output out."""
+def decode_bytes(w: workloads.Workload, seq_lens: np.ndarray, k_elem: int = 1, v_elem: int = 1,
+                 query_rows: int | None = None) -> int:
+    """Algorithmic bytes of one attention call: every cached K and V byte of every sequence
+    (k_elem / v_elem bytes per element), its block-table entries and length, the bf16 query
+    rows in and the bf16 output rows out; the multi-query form (query_rows given) also reads
+    the num_seqs + 1 query_start_loc entries."""
     L = seq_lens.astype(np.int64)
     row = w.n_kv * w.head_dim
-    kv = int((2 * L * row).sum())
+    kv = int((L * row).sum()) * (k_elem + v_elem)
     tables = int((4 * np.ceil(L / w.block_size)).sum()) + 4 * L.size
-    qo = 2 * 2 * L.size * w.n_q * w.head_dim
-    return kv + tables + qo
+    rows = L.size if query_rows is None else query_rows
+    qo = 2 * 2 * rows * w.n_q * w.head_dim
+    qsl = 0 if query_rows is None else 4 * (L.size + 1)
+    return kv + tables + qo + qsl
+
+
+def query_len(w: workloads.Workload, variant: str) -> int:
+    """Query tokens per sequence: 16 // G score columns' worth for the multi-query variant."""
+    return max(1, 16 // (w.n_q // w.n_kv)) if variant == "multi" else 1
+
+
+def step_rows(w: workloads.Workload, lay: workloads.Layout, qlen: int):
+    """(slots, positions) of the rows one step writes: every context row, or for a serving
+    step the last qlen tokens of every sequence (sequence-major)."""
+    if w.kind != "mixed":
+        return lay.slot_mapping, np.maximum(lay.row_pos, 0).astype(np.int64)
+    L = lay.seq_lens.astype(np.int64)
+    pos = (L[:, None] - qlen + np.arange(qlen)[None, :]).reshape(-1)
+    seq = np.repeat(np.arange(lay.num_seqs), qlen)
+    slots = lay.block_tables[seq, pos // w.block_size].astype(np.int64) * w.block_size + \
+        pos % w.block_size
+    return slots, pos
 
 
 # ----------------------------------------------------------------- helpers
@@ -166,69 +208,138 @@ class ClockSampler:
 # ----------------------------------------------------------------- problem set-up
 
 class Problem:
-    """Device-resident inputs, caches and outputs of one workload."""
+    """Device-resident inputs, caches and outputs of one workload in one variant."""
 
-    def __init__(self, name: str, device, num_seqs: int | None = None):
+    def __init__(self, name: str, device, num_seqs: int | None = None, variant: str = "fp8"):
+        import fp8_paged_kv_reshape_gb300 as kv
+
+        self.kv = kv
         self.w = w = workloads.WORKLOADS[name]
+        self.variant = variant
+        if variant == "multi" and w.kind == "write":
+            raise ValueError("the %s workload has no attention step" % name)
         self.lay = lay = workloads.make_layout(w, num_seqs=num_seqs)
         self.device = device
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.qlen = query_len(w, variant)
         self.ksc = workloads.scale_tensor(w.k_scale, w.scale_dtype, device)
         self.vsc = workloads.scale_tensor(w.v_scale, w.scale_dtype, device)
-        self.kc = workloads.new_cache(lay.num_blocks, w, device)
-        self.vc = self.kc.clone()
-        ctx_k, ctx_v = workloads.make_kv(w, lay.slot_mapping.size, device)
-        self.ctx_slots = torch.from_numpy(lay.slot_mapping).to(device)
+        self.k_elem = 2 if variant == "k_bf16" else 1
+        self.v_elem = 2 if variant == "v_bf16" else 1
+        self.kc = self._new_cache(self.k_elem)
+        self.vc = self._new_cache(self.v_elem)
+        self.rot = w.head_dim
+        self.table = None
+        if variant == "rope":
+            max_pos = max(1, int(lay.seq_lens.max()) if lay.num_seqs else 1)
+            self.table = torch.from_numpy(workloads.rope_table(max_pos, self.rot)).to(device)
+        slots, pos = step_rows(w, lay, self.qlen)
         if w.kind == "mixed":
-            # the cache holds the context before the timed region; a step writes one new
-            # token per sequence (position len-1) and decodes
-            import fp8_paged_kv_reshape_gb300 as kv
-            kv.reshape_and_cache(ctx_k, ctx_v, self.kc, self.vc, self.ctx_slots, self.ksc, self.vsc)
+            # the cache holds the context before the timed region; a step writes the last
+            # qlen tokens of every sequence and attends
+            ctx_k, ctx_v = workloads.make_kv(w, lay.slot_mapping.size, device)
+            self._write(ctx_k, ctx_v, torch.from_numpy(lay.slot_mapping).to(device),
+                        torch.from_numpy(lay.row_pos.astype(np.int64)).to(device))
             del ctx_k, ctx_v
-            self.k, self.v = workloads.make_new_token_kv(w, lay.num_seqs, device)
-            last = lay.seq_lens.astype(np.int64) - 1
-            slots = lay.block_tables[np.arange(lay.num_seqs), last // w.block_size].astype(np.int64) \
-                * w.block_size + last % w.block_size
-            self.slots_np = slots
+            self.k, self.v = workloads.make_new_token_kv(w, lay.num_seqs * self.qlen, device)
         else:
-            self.k, self.v = ctx_k, ctx_v
-            self.slots_np = lay.slot_mapping
-        self.slots = torch.from_numpy(self.slots_np).to(device)
+            self.k, self.v = workloads.make_kv(w, lay.slot_mapping.size, device)
+        self.slots_np, self.pos_np = slots, pos
+        self.slots = torch.from_numpy(slots).to(device)
+        self.pos = torch.from_numpy(pos).to(device) if variant == "rope" else None
         self.decode = w.kind != "write"
         if self.decode:
-            self.q = workloads.make_query(w, lay.num_seqs, device)
+            rows = lay.num_seqs * self.qlen
+            self.q = workloads.make_query(w, rows, device)
             self.bt = torch.from_numpy(lay.block_tables).to(device)
             self.sl = torch.from_numpy(lay.seq_lens).to(device)
+            self.qsl = torch.arange(0, rows + 1, self.qlen, dtype=torch.int32, device=device) \
+                if variant == "multi" else None
             self.out = torch.empty_like(self.q)
-            import fp8_paged_kv_reshape_gb300 as kv
-            self.ws = torch.empty(kv.paged_decode_workspace_size(lay.num_seqs, w.n_q, w.head_dim),
+            self.ws = torch.empty(kv.paged_decode_workspace_size(lay.num_seqs, w.n_q * self.qlen,
+                                                                 w.head_dim),
                                   dtype=torch.uint8, device=device)
-        self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.rs_bytes = reshape_bytes(w, self.slots_np)
-        self.dec_bytes = decode_bytes(w, lay.seq_lens) if self.decode else 0
+        self.rs_bytes = reshape_bytes(w, slots, 2, self.k_elem, self.v_elem,
+                                      pos if variant == "rope" else None, self.rot)
+        self.dec_bytes = decode_bytes(w, lay.seq_lens, self.k_elem, self.v_elem,
+                                      self.lay.num_seqs * self.qlen if variant == "multi" else None) \
+            if self.decode else 0
+
+    def _new_cache(self, elem: int) -> torch.Tensor:
+        if elem == 1:
+            return workloads.new_cache(self.lay.num_blocks, self.w, self.device)
+        w = self.w
+        return torch.zeros((self.lay.num_blocks, w.block_size, w.n_kv, w.head_dim),
+                           dtype=torch.bfloat16, device=self.device)
+
+    def _write(self, k, v, slots, pos):
+        kv = self.kv
+        if self.variant == "rope":
+            kv.rope_reshape_and_cache(k, v, self.kc, self.vc, slots, pos, self.table, True,
+                                      self.ksc, self.vsc, status=self.status)
+        elif self.variant in ("k_bf16", "v_bf16"):
+            kv.reshape_and_cache_mixed(k, v, self.kc, self.vc, slots, self.ksc, self.vsc,
+                                       status=self.status)
+        else:
+            kv.reshape_and_cache(k, v, self.kc, self.vc, slots, self.ksc, self.vsc,
+                                 status=self.status)
 
     def reshape(self):
-        import fp8_paged_kv_reshape_gb300 as kv
-        kv.reshape_and_cache(self.k, self.v, self.kc, self.vc, self.slots, self.ksc, self.vsc,
-                             status=self.status)
+        self._write(self.k, self.v, self.slots, self.pos)
 
     def attend(self):
-        import fp8_paged_kv_reshape_gb300 as kv
-        kv.paged_decode_attention(self.q, self.kc, self.vc, self.bt, self.sl, self.ksc, self.vsc,
-                                  out=self.out, workspace=self.ws, status=self.status)
+        kv = self.kv
+        if self.variant == "multi":
+            kv.paged_attention_multi(self.q, self.qsl, self.qlen, self.kc, self.vc, self.bt,
+                                     self.sl, self.ksc, self.vsc, out=self.out, workspace=self.ws,
+                                     status=self.status)
+        elif self.variant in ("k_bf16", "v_bf16"):
+            kv.paged_decode_attention_mixed(self.q, self.kc, self.vc, self.bt, self.sl, self.ksc,
+                                            self.vsc, out=self.out, workspace=self.ws,
+                                            status=self.status)
+        else:
+            kv.paged_decode_attention(self.q, self.kc, self.vc, self.bt, self.sl, self.ksc,
+                                      self.vsc, out=self.out, workspace=self.ws,
+                                      status=self.status)
+
+    def step_inputs(self):
+        """The device tensors a step consumes that a caller supplies per step."""
+        ins = [self.k, self.v, self.slots]
+        if self.pos is not None:
+            ins.append(self.pos)
+        if self.decode:
+            ins += [self.q, self.bt, self.sl]
+            if self.qsl is not None:
+                ins.append(self.qsl)
+        return ins
 
     def launches_per_step(self) -> int:
-        return 1 + (3 if self.decode else 0)  # reshape; plan + split-KV decode + combine
+        return 1 + (3 if self.decode else 0)  # write; plan + split-KV attention + combine
 
     def describe(self) -> dict:
         w, lay = self.w, self.lay
-        d = {"workload": w.name, "n_q": w.n_q, "n_kv": w.n_kv, "head_dim": w.head_dim,
-             "block_size": w.block_size, "num_seqs": lay.num_seqs,
+        write = {"fp8": "reshape_and_cache", "multi": "reshape_and_cache",
+                 "rope": "rope_reshape_and_cache", "k_bf16": "reshape_and_cache_mixed",
+                 "v_bf16": "reshape_and_cache_mixed"}[self.variant]
+        attn = {"multi": "paged_attention_multi", "k_bf16": "paged_decode_attention_mixed",
+                "v_bf16": "paged_decode_attention_mixed"}.get(self.variant,
+                                                              "paged_decode_attention")
+        d = {"workload": w.name, "variant": self.variant, "n_q": w.n_q, "n_kv": w.n_kv,
+             "head_dim": w.head_dim, "block_size": w.block_size, "num_seqs": lay.num_seqs,
              "context_tokens": int(lay.seq_lens.sum()),
              "rows_written_per_step": int(self.slots_np.size),
              "k_scale": w.k_scale, "v_scale": w.v_scale, "scale_dtype": w.scale_dtype,
-             "step": ("reshape_and_cache(%d rows) + paged_decode_attention(%d seqs)"
-                      % (self.slots_np.size, lay.num_seqs)) if self.decode else
-                     "reshape_and_cache(%d rows)" % self.slots_np.size}
+             "k_cache": "bf16" if self.k_elem == 2 else "e4m3",
+             "v_cache": "bf16" if self.v_elem == 2 else "e4m3"}
+        if self.decode:
+            d["query_tokens_per_seq"] = self.qlen
+            d["step"] = "%s(%d rows) + %s(%d seqs x %d queries)" % (
+                write, self.slots_np.size, attn, lay.num_seqs, self.qlen)
+        else:
+            d["step"] = "%s(%d rows)" % (write, self.slots_np.size)
+        if self.variant == "rope":
+            d["rope"] = {"rot_dim": self.rot, "neox": True, "theta": 500000.0,
+                         "table": "float32 [%d, %d], resident" % tuple(self.table.shape)}
         per_step = self.rs_bytes + self.dec_bytes
         d["l2"] = ("inputs larger than L2 (%.2f GB of algorithmic traffic per step), no flush"
                    % (per_step / 1e9)) if per_step > L2_BYTES else \
@@ -241,7 +352,7 @@ class Problem:
 def run_ours(args, rank, world, device):
     import fp8_paged_kv_reshape_gb300 as kv  # noqa: F401  (fails loudly without the library)
 
-    p = Problem(args.workload, device, args.num_seqs)
+    p = Problem(args.workload, device, args.num_seqs, args.variant)
     per_step = p.rs_bytes + p.dec_bytes
     flush = None if per_step > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
                                                          device=device)
@@ -310,22 +421,25 @@ def run_ours(args, rank, world, device):
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
-            "traffic": recorded_traffic(dom, args.workload),
+            "traffic": recorded_traffic(dom, args.workload if args.variant == "fp8"
+                                        else "%s:%s" % (args.workload, args.variant)),
             "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
     value = whole_job_gbs(per_step, args.steps, world, total_ms)
     line = {
-        "metric": "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak",
+        "metric": METRIC,
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3",
-        "compute": "f32 divide + E4M3 encode; fp16 mma.sync with f32 accumulate",
+        "compute": "f32 divide + E4M3 encode; fp16 (bf16 for a bf16 cache side) mma.sync "
+                   "with f32 accumulate",
         "data": "synthetic (seeded; see workloads/)",
         "config": p.describe(), "roofline": roof, "kernels": kernels,
         "gpu_launches": p.launches_per_step() * args.steps,
         "clocks": sampler.summary(), "e2e": e2e,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(args.workload, target_s=args.cpu_seconds,
+                                            variant=args.variant)
     return line
 
 
@@ -334,12 +448,8 @@ def run_e2e(args, p: Problem, device):
     from pinned host memory and reads the output back, inside the timed region."""
     import fp8_paged_kv_reshape_gb300 as kv
 
-    hk, hv = p.k.cpu().pin_memory(), p.v.cpu().pin_memory()
-    hs = p.slots.cpu().pin_memory()
-    ins = [(hk, p.k), (hv, p.v), (hs, p.slots)]
+    ins = [(d.cpu().pin_memory(), d) for d in p.step_inputs()]
     if p.decode:
-        ins += [(p.q.cpu().pin_memory(), p.q), (p.bt.cpu().pin_memory(), p.bt),
-                (p.sl.cpu().pin_memory(), p.sl)]
         hout = torch.empty(p.out.shape, dtype=p.out.dtype).pin_memory()
     stream = torch.cuda.current_stream(device)
     h2d = sum(h.numel() * h.element_size() for h, _ in ins)
@@ -375,9 +485,11 @@ def run_e2e(args, p: Problem, device):
 
 # ----------------------------------------------------------------- CPU oracle legs
 
-def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_all, q):
-    """Run the CPU oracle on the given sequences of the workload: reshape their rows into
-    a cache, then decode every head of them.  Returns (seconds, algorithmic bytes)."""
+def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_all, q,
+                   variant: str = "fp8"):
+    """Run the CPU oracle on the given sequences of the workload in the given variant: write
+    their rows into a cache, then attend with every head of them.  Returns (seconds,
+    algorithmic bytes)."""
     import oracle
 
     ks = workloads.stored_scale(w.k_scale, w.scale_dtype)
@@ -386,70 +498,104 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     kh = k_all[torch.from_numpy(rows)].contiguous()
     vh = v_all[torch.from_numpy(rows)].contiguous()
     slots = lay.slot_mapping[rows]
-    kc = np.full((lay.num_blocks, w.block_size, w.n_kv, w.head_dim), workloads.SENTINEL, np.uint8)
-    vc = kc.copy()
+    pos = np.maximum(lay.row_pos[rows], 0).astype(np.int64)
+    shape = (lay.num_blocks, w.block_size, w.n_kv, w.head_dim)
+    k_elem = 2 if variant == "k_bf16" else 1
+    v_elem = 2 if variant == "v_bf16" else 1
+    kc = np.full(shape, workloads.SENTINEL, np.uint8 if k_elem == 1 else np.uint16)
+    vc = np.full(shape, workloads.SENTINEL, np.uint8 if v_elem == 1 else np.uint16)
+    kinds = (oracle.E4M3 if k_elem == 1 else oracle.CACHE_BF16,
+             oracle.E4M3 if v_elem == 1 else oracle.CACHE_BF16)
     decode = w.kind != "write"
     sub_lens = lay.seq_lens[seqs]
+    qlen = query_len(w, variant)
+    seq_idx = np.asarray(seqs)
+    table = workloads.rope_table(max(1, int(lay.seq_lens.max())), w.head_dim) \
+        if variant == "rope" else None
     t0 = time.perf_counter()
-    oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
+    if variant == "rope":
+        oracle.rope_reshape_and_cache(kh, vh, kc, vc, slots, pos, table, w.head_dim, True,
+                                      w.block_size, ks, vs)
+    elif variant in ("k_bf16", "v_bf16"):
+        oracle.reshape_and_cache_mixed(kh, vh, kc, kinds[0], vc, kinds[1], slots, w.block_size,
+                                       ks, vs)
+    else:
+        oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
     if decode:
-        oracle.paged_decode_attention(q[torch.from_numpy(np.asarray(seqs))], kc, vc,
-                                      lay.block_tables[seqs], sub_lens, ks, vs)
+        bt = lay.block_tables[seqs]
+        if variant == "multi":
+            qrows = (seq_idx[:, None] * qlen + np.arange(qlen)[None, :]).reshape(-1)
+            qsl = np.arange(0, qrows.size + 1, qlen, dtype=np.int32)
+            oracle.paged_attention_multi(q[torch.from_numpy(qrows)], qsl, kc, vc, bt, sub_lens,
+                                         ks, vs)
+        elif variant in ("k_bf16", "v_bf16"):
+            oracle.paged_decode_attention_mixed(q[torch.from_numpy(seq_idx)], kc, kinds[0], vc,
+                                                kinds[1], bt, sub_lens, ks, vs)
+        else:
+            oracle.paged_decode_attention(q[torch.from_numpy(seq_idx)], kc, vc, bt, sub_lens,
+                                          ks, vs)
     dt = time.perf_counter() - t0
-    nbytes = reshape_bytes(w, slots) + (decode_bytes(w, sub_lens) if decode else 0)
+    nbytes = reshape_bytes(w, slots, 2, k_elem, v_elem, pos if variant == "rope" else None,
+                           w.head_dim)
+    if decode:
+        nbytes += decode_bytes(w, sub_lens, k_elem, v_elem,
+                               len(seqs) * qlen if variant == "multi" else None)
     return dt, nbytes
 
 
-def _cpu_inputs(name):
+def _cpu_inputs(name, variant="fp8"):
     w = workloads.WORKLOADS[name]
     lay = workloads.make_layout(w)
     k, v = workloads.make_kv(w, lay.slot_mapping.size, "cpu")
-    q = workloads.make_query(w, lay.num_seqs, "cpu")
+    q = workloads.make_query(w, lay.num_seqs * query_len(w, variant), "cpu")
     return w, lay, k, v, q
 
 
-def cpu_baseline(name: str, target_s: float = 12.0) -> dict:
+def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dict:
     """The oracle as it stands, single-threaded on the host, on a bounded sample of the same
-    workload (whole sequences: their rows written, then every head decoded)."""
-    w, lay, k, v, q = _cpu_inputs(name)
+    workload (whole sequences: their rows written, then every head attended)."""
+    w, lay, k, v, q = _cpu_inputs(name, variant)
     order = np.random.Generator(np.random.PCG64(w.seed + 5)).permutation(lay.num_seqs)
     t, nb, used = 0.0, 0, []
     for s in order:
-        dt, b = _oracle_sample(w, lay, [int(s)], k, v, q)
+        dt, b = _oracle_sample(w, lay, [int(s)], k, v, q, variant)
         t += dt
         nb += b
         used.append(int(s))
         if t >= target_s:
             break
     return {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d sequences of %s (%d tokens): oracle reshape of their rows + "
-                      "decode of all %d heads, %.1f s single-threaded"
-                      % (len(used), lay.num_seqs, name, int(lay.seq_lens[used].sum()), w.n_q, t)}
+            "sample": "%d of %d sequences of %s (%d tokens), variant %s: oracle write of their "
+                      "rows + attention for all %d heads, %.1f s single-threaded"
+                      % (len(used), lay.num_seqs, name, int(lay.seq_lens[used].sum()), variant,
+                         w.n_q, t)}
 
 
 def run_reference(args):
     """The CPU oracle timed on the host cores on this arm's workload and metric: each step
     is a bounded sample (one sequence, its rows written and all heads decoded)."""
-    w, lay, k, v, q = _cpu_inputs(args.workload)
+    w, lay, k, v, q = _cpu_inputs(args.workload, args.variant)
     order = np.random.Generator(np.random.PCG64(w.seed + 6)).permutation(lay.num_seqs)
     for i in range(args.warmup):
-        _oracle_sample(w, lay, [int(order[i % lay.num_seqs])], k, v, q)
+        _oracle_sample(w, lay, [int(order[i % lay.num_seqs])], k, v, q, args.variant)
     t, nb = 0.0, 0
     for i in range(args.steps):
-        dt, b = _oracle_sample(w, lay, [int(order[(args.warmup + i) % lay.num_seqs])], k, v, q)
+        dt, b = _oracle_sample(w, lay, [int(order[(args.warmup + i) % lay.num_seqs])], k, v, q,
+                               args.variant)
         t += dt
         nb += b
     value = nb / t / 1e9
-    sample = ("each step: 1 of %d sequences of %s, oracle reshape of its rows + decode of all "
-              "%d heads, single-threaded" % (lay.num_seqs, args.workload, w.n_q))
+    sample = ("each step: 1 of %d sequences of %s, variant %s, oracle write of its rows + "
+              "attention for all %d heads, single-threaded"
+              % (lay.num_seqs, args.workload, args.variant, w.n_q))
     return {
         "impl": "reference",
-        "metric": "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak",
+        "metric": METRIC,
         "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
         "data": "synthetic (seeded; see workloads/)",
-        "config": {"workload": args.workload, "n_q": w.n_q, "n_kv": w.n_kv,
+        "config": {"workload": args.workload, "variant": args.variant, "n_q": w.n_q, "n_kv": w.n_kv,
                    "head_dim": w.head_dim, "block_size": w.block_size},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
@@ -465,6 +611,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3_8b", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--variant", default="fp8", choices=VARIANTS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -35,26 +35,64 @@ namespace {
 
 constexpr int kWarps = 8;  // per CTA
 
+// Packed fp32 pairs: the f32x2 arithmetic of sm_100+ does two IEEE round-to-nearest
+// operations (no flush to zero) per instruction, halving the issue cost of the divide and
+// of the rope rotation.  Lane 0 of a pair is the low half.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // The reciprocal-and-corrections divide of the header note, for |s| in [2^-60, 2^60].
 struct FastDiv {
     float sa;    // |s|
     float y;     // RN(1 / |s|)
     uint32_t neg;  // 0x80808080 when s < 0 (the byte signs are flipped after packing)
+    uint64_t y2, nsa2;  // (y, y) and (-|s|, -|s|) for the packed form
     __device__ __forceinline__ explicit FastDiv(float s) {
         sa = fabsf(s);
         y = __fdiv_rn(1.0f, sa);  // correctly rounded reciprocal
         neg = signbit(s) ? 0x80808080u : 0u;
+        y2 = pack2(y, y);
+        nsa2 = pack2(-sa, -sa);
     }
-    // RN(x / |s|) with the sign of x
-    __device__ __forceinline__ float quot(float x) const {
-        const float q0 = x * y;
-        const float r0 = fmaf(-q0, sa, x);
-        const float q1 = fmaf(r0, y, q0);
-        const float r1 = fmaf(-q1, sa, x);
-        const float q2 = fmaf(r1, y, q1);
-        // the exact quotient's sign is the sign of x: restore it (a zero may have lost it)
-        return __uint_as_float((__float_as_uint(q2) & 0x7FFFFFFFu) |
-                               (__float_as_uint(x) & 0x80000000u));
+    // RN(x / |s|) with the sign of x, for a pair: q0 = x*y, then two residual steps
+    // q += fma(q, -|s|, x) * y, each operation on both lanes (fma(q, -|s|, x) equals
+    // fma(-q, |s|, x): negation is exact); the sign is restored from x (a zero may lose it)
+    __device__ __forceinline__ void quot2(float x0, float x1, float &r0, float &r1) const {
+        const uint64_t x = pack2(x0, x1);
+        const uint64_t q0 = mul2(x, y2);
+        const uint64_t e0 = fma2(q0, nsa2, x);
+        const uint64_t q1 = fma2(e0, y2, q0);
+        const uint64_t e1 = fma2(q1, nsa2, x);
+        float a, b;
+        unpack2(fma2(e1, y2, q1), a, b);
+        r0 = __uint_as_float((__float_as_uint(a) & 0x7FFFFFFFu) | (__float_as_uint(x0) & 0x80000000u));
+        r1 = __uint_as_float((__float_as_uint(b) & 0x7FFFFFFFu) | (__float_as_uint(x1) & 0x80000000u));
     }
 };
 
@@ -80,8 +118,13 @@ __device__ __noinline__ uint32_t patch_word(uint32_t w, uint32_t nanmask, float 
 template <bool kFast>
 __device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const FastDiv &fd) {
     float q[8];
+    if (kFast) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = kFast ? fd.quot(x[i]) : __fdiv_rn(x[i], s);
+        for (int i = 0; i < 8; i += 2) fd.quot2(x[i], x[i + 1], q[i], q[i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(x[i], s);
+    }
     uint32_t w0 = e4m3x2_from_f32(q[0], q[1]) | (e4m3x2_from_f32(q[2], q[3]) << 16);
     uint32_t w1 = e4m3x2_from_f32(q[4], q[5]) | (e4m3x2_from_f32(q[6], q[7]) << 16);
     if (kFast) {  // the fast quotient carries sign(x); apply sign(s)
@@ -275,54 +318,84 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const Re
 // bytes match a plain CPU evaluation.  In the NeoX layout dim i pairs with i + rot/2: a
 // lane's 8-dim group and its partner group sit rot/16 lanes apart inside the head's
 // lane block, and are exchanged with one shuffle per value.  In the GPT-J layout pairs
-// are adjacent dims inside the group.
+// are adjacent dims inside the group.  The table values a lane needs are the same for
+// every head of a row, so they are read once per row, issued with the row's data loads.
 
 __device__ __forceinline__ bool pos_ok(const ReshapeArgs &a, int64_t pos) {
     return pos >= 0 && pos < a.max_pos;
 }
 
-template <bool kF32, int U, bool kFast>
-__device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], const RowCtx &c,
-                                               const FastDiv &fd, const ReshapeArgs &a,
-                                               int64_t slot, int64_t pos, int groups, int lane) {
-    uint8_t *dst = c.cache + slot * a.row_elems;
+// The cos/sin a lane needs for one row.  A lane's 8-dim groups g = lane + 32u all start at
+// the same dim of their head, d0 = 8*lane mod head_dim (head_dim divides 256), so one set
+// of table values serves the whole row; it is fetched together with the row's data, two
+// rows ahead of its use.  NeoX: 8 cos and 8 sin of pairs ci..ci+7; GPT-J: 4 of each.
+struct RopeCS {
+    float c[8], s[8];
+};
+
+__device__ __forceinline__ void load_cs(RopeCS &t, const ReshapeArgs &a, int64_t pos, int lane) {
+    const int d0 = (lane * 8) % a.head_dim;
+    if (d0 >= a.rot) return;  // pass-through dims
     const float *cs = a.cos_sin + pos * a.rot;
     const int half = a.rot >> 1;
+    if (a.neox) {
+        const int ci = d0 < half ? d0 : d0 - half;
+        const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cs + ci));
+        const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cs + ci + 4));
+        const float4 s0 = __ldg(reinterpret_cast<const float4 *>(cs + half + ci));
+        const float4 s1 = __ldg(reinterpret_cast<const float4 *>(cs + half + ci + 4));
+        t.c[0] = c0.x; t.c[1] = c0.y; t.c[2] = c0.z; t.c[3] = c0.w;
+        t.c[4] = c1.x; t.c[5] = c1.y; t.c[6] = c1.z; t.c[7] = c1.w;
+        t.s[0] = s0.x; t.s[1] = s0.y; t.s[2] = s0.z; t.s[3] = s0.w;
+        t.s[4] = s1.x; t.s[5] = s1.y; t.s[6] = s1.z; t.s[7] = s1.w;
+    } else {
+        const float4 cv = __ldg(reinterpret_cast<const float4 *>(cs + d0 / 2));
+        const float4 sv = __ldg(reinterpret_cast<const float4 *>(cs + half + d0 / 2));
+        t.c[0] = cv.x; t.c[1] = cv.y; t.c[2] = cv.z; t.c[3] = cv.w;
+        t.s[0] = sv.x; t.s[1] = sv.y; t.s[2] = sv.z; t.s[3] = sv.w;
+    }
+}
+
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], const RopeCS &t,
+                                               const RowCtx &c, const FastDiv &fd,
+                                               const ReshapeArgs &a, int64_t slot, int groups,
+                                               int lane) {
+    uint8_t *dst = c.cache + slot * a.row_elems;
+    const int half = a.rot >> 1;
     const int partner = half >> 3;  // lanes between a group and its NeoX partner
+    const int d0 = (lane * 8) % a.head_dim;
+    const bool rotated = d0 < a.rot;
+    const bool first = d0 < half;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int g = lane + 32 * u;
         float x[8];
         buf[u].unpack(x);  // lanes past the row hold stale values; they only feed shuffles
-        const int d0 = (g * 8) % a.head_dim;
         if (a.neox) {
             float y[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(0xFFFFFFFFu, x[i], partner);
-            if (g < groups && d0 < a.rot) {
-                const bool first = d0 < half;
-                const int ci = first ? d0 : d0 - half;
-                const float4 c0 = *reinterpret_cast<const float4 *>(cs + ci);
-                const float4 c1 = *reinterpret_cast<const float4 *>(cs + ci + 4);
-                const float4 s0 = *reinterpret_cast<const float4 *>(cs + half + ci);
-                const float4 s1 = *reinterpret_cast<const float4 *>(cs + half + ci + 4);
-                const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+            if (g < groups && rotated) {
+                // first half: x*c - y*s; second half: y*s + x*c (= x*c + y*s exactly)
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    x[i] = first ? __fsub_rn(__fmul_rn(x[i], cv[i]), __fmul_rn(y[i], sv[i]))
-                                 : __fadd_rn(__fmul_rn(y[i], sv[i]), __fmul_rn(x[i], cv[i]));
+                for (int i = 0; i < 8; i += 2) {
+                    const uint64_t xc = mul2(pack2(x[i], x[i + 1]), pack2(t.c[i], t.c[i + 1]));
+                    const uint64_t ys = mul2(pack2(y[i], y[i + 1]), pack2(t.s[i], t.s[i + 1]));
+                    unpack2(first ? sub2(xc, ys) : add2(xc, ys), x[i], x[i + 1]);
+                }
             }
-        } else if (g < groups && d0 < a.rot) {
-            const float4 cv = *reinterpret_cast<const float4 *>(cs + d0 / 2);
-            const float4 sv = *reinterpret_cast<const float4 *>(cs + half + d0 / 2);
-            const float cc[4] = {cv.x, cv.y, cv.z, cv.w};
-            const float ss[4] = {sv.x, sv.y, sv.z, sv.w};
+        } else if (g < groups && rotated) {
+            // pairs (p, q) = (x[2j], x[2j+1]), two pairs per packed operation:
+            // p' = p*c - q*s, q' = p*s + q*c
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float p = x[2 * j], q = x[2 * j + 1];
-                x[2 * j] = __fsub_rn(__fmul_rn(p, cc[j]), __fmul_rn(q, ss[j]));
-                x[2 * j + 1] = __fadd_rn(__fmul_rn(p, ss[j]), __fmul_rn(q, cc[j]));
+            for (int j = 0; j < 4; j += 2) {
+                const uint64_t p = pack2(x[2 * j], x[2 * j + 2]);
+                const uint64_t q = pack2(x[2 * j + 1], x[2 * j + 3]);
+                const uint64_t c = pack2(t.c[j], t.c[j + 1]);
+                const uint64_t sn = pack2(t.s[j], t.s[j + 1]);
+                unpack2(sub2(mul2(p, c), mul2(q, sn)), x[2 * j], x[2 * j + 2]);
+                unpack2(add2(mul2(p, sn), mul2(q, c)), x[2 * j + 1], x[2 * j + 3]);
             }
         }
         if (g < groups)
@@ -331,10 +404,12 @@ __device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], cons
     }
 }
 
-template <bool kF32, int U, bool kFast>
+// K rows are rotated, V rows stored as by reshape_and_cache; the warp's rows are all K or
+// all V (is_k), and its table values travel with its row data.
+template <bool kF32, int U, bool kFast, bool kIsK>
 __device__ __forceinline__ void rope_pipelined_rows(const ReshapeArgs &a, const RowCtx &c,
-                                                    bool is_k, int64_t r, int64_t stride,
-                                                    int64_t rows, int lane) {
+                                                    int64_t r, int64_t stride, int64_t rows,
+                                                    int lane) {
     const FastDiv fd(c.s);
     const int groups = a.row_elems >> 3;
     auto pos_of = [&](int64_t row) -> int64_t {
@@ -348,28 +423,38 @@ __device__ __forceinline__ void rope_pipelined_rows(const ReshapeArgs &a, const 
         return false;
     };
     Group<kF32> A[U], B[U];
+    RopeCS ta, tb;
     int64_t s1 = slot_of(a, r, rows), p1 = pos_of(r);
     int64_t s2 = slot_of(a, r + stride, rows), p2 = pos_of(r + stride);
     bool ok1 = ok_of(r, s1, p1);
-    if (ok1) load_row<kF32, U>(A, c, r, groups, lane);
+    if (ok1) {
+        load_row<kF32, U>(A, c, r, groups, lane);
+        if (kIsK) load_cs(ta, a, p1, lane);
+    }
     while (r < rows) {
         int64_t rn = r + stride;
         bool ok2 = ok_of(rn, s2, p2);
-        if (ok2) load_row<kF32, U>(B, c, rn, groups, lane);
+        if (ok2) {
+            load_row<kF32, U>(B, c, rn, groups, lane);
+            if (kIsK) load_cs(tb, a, p2, lane);
+        }
         int64_t s3 = slot_of(a, rn + stride, rows), p3 = pos_of(rn + stride);
         if (ok1) {
-            if (is_k) store_row_rope<kF32, U, kFast>(A, c, fd, a, s1, p1, groups, lane);
+            if (kIsK) store_row_rope<kF32, U, kFast>(A, ta, c, fd, a, s1, groups, lane);
             else store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
         }
         r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
         if (r >= rows) break;
         rn = r + stride;
         ok2 = ok_of(rn, s2, p2);
-        if (ok2) load_row<kF32, U>(A, c, rn, groups, lane);
+        if (ok2) {
+            load_row<kF32, U>(A, c, rn, groups, lane);
+            if (kIsK) load_cs(ta, a, p2, lane);
+        }
         s3 = slot_of(a, rn + stride, rows);
         p3 = pos_of(rn + stride);
         if (ok1) {
-            if (is_k) store_row_rope<kF32, U, kFast>(B, c, fd, a, s1, p1, groups, lane);
+            if (kIsK) store_row_rope<kF32, U, kFast>(B, tb, c, fd, a, s1, groups, lane);
             else store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
         }
         r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
@@ -394,10 +479,14 @@ __global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const Reshape
     c.cache = is_v ? a.value_cache : a.key_cache;
     c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
     c.s = is_v ? sv : sk;
-    if (fast_range(c.s))
-        rope_pipelined_rows<kF32, U, true>(a, c, !is_v, r, stride, rows, lane);
-    else
-        rope_pipelined_rows<kF32, U, false>(a, c, !is_v, r, stride, rows, lane);
+    const bool fast = fast_range(c.s);  // uniform per warp, as is_v
+    if (is_v) {
+        if (fast) rope_pipelined_rows<kF32, U, true, false>(a, c, r, stride, rows, lane);
+        else rope_pipelined_rows<kF32, U, false, false>(a, c, r, stride, rows, lane);
+    } else {
+        if (fast) rope_pipelined_rows<kF32, U, true, true>(a, c, r, stride, rows, lane);
+        else rope_pipelined_rows<kF32, U, false, true>(a, c, r, stride, rows, lane);
+    }
 }
 
 // Any row length: one warp per row, groups streamed in rounds of 4 per lane.

@@ -87,3 +87,55 @@ def test_byte_accounting():
     lens = np.array([16, 17, 0], np.int32)
     per = bench.decode_bytes(w, lens)
     assert per == 2 * 33 * 1024 + 4 * (1 + 2 + 0) + 4 * 3 + 2 * 2 * 3 * 32 * 128
+
+
+def test_byte_accounting_of_the_variants():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["llama3_8b"]
+    slots = np.array([0, -1, 5, 7], np.int64)
+    # a bf16 side writes two bytes per element
+    assert bench.reshape_bytes(w, slots, 2, 2, 1) == 3 * 1024 * 7 + 8 * 4
+    # rope: + the 8-byte position of every row + one float32 table row per distinct position
+    pos = np.array([3, 0, 3, 9], np.int64)
+    assert bench.reshape_bytes(w, slots, 2, 1, 1, pos, 128) == \
+        3 * 1024 * 6 + 8 * 4 + 8 * 4 + 2 * 128 * 4
+    lens = np.array([16, 17, 0], np.int32)
+    assert bench.decode_bytes(w, lens, 1, 2) == \
+        3 * 33 * 1024 + 4 * (1 + 2 + 0) + 4 * 3 + 2 * 2 * 3 * 32 * 128
+    # multi-query: the query/output rows and query_start_loc
+    assert bench.decode_bytes(w, lens, query_rows=12) == \
+        2 * 33 * 1024 + 4 * (1 + 2 + 0) + 4 * 3 + 2 * 2 * 12 * 32 * 128 + 4 * 4
+    assert bench.query_len(w, "multi") == 4 and bench.query_len(w, "fp8") == 1
+
+
+def test_serving_step_rows_are_the_last_query_tokens():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["mixed_serving"]
+    lay = workloads.make_layout(w, num_seqs=5)
+    slots, pos = bench.step_rows(w, lay, 3)
+    assert slots.shape == (15,) and pos.shape == (15,)
+    for b in range(5):
+        L = int(lay.seq_lens[b])
+        assert list(pos[3 * b:3 * b + 3]) == [L - 3, L - 2, L - 1]
+        # the same slots the context layout gives those positions
+        ctx = lay.slot_mapping[(lay.row_seq == b)]
+        assert list(slots[3 * b:3 * b + 3]) == list(ctx[L - 3:L])
+
+
+def test_reference_arm_runs_each_variant():
+    for variant in ("rope", "k_bf16", "multi"):
+        r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+                   "--variant", variant)
+        assert r.returncode == 0, r.stderr
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        assert d["config"]["variant"] == variant and d["value"] > 0

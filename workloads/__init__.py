@@ -27,6 +27,10 @@ Workloads (the shapes the source pages' problem statement names):
                  log-uniform in [16, 32768]; one new token per seq is written
                  at position len-1, then decode
 Scales not named by a workload are k_scale 0.05 and v_scale 0.04.
+
+Rope tables (for the rope-fused cache write) are the model's constant input: the
+standard rotary table with base theta, cos(p * theta^(-2i/rot)) then sin(...), computed
+in float64 and rounded once to float32.
 """
 from __future__ import annotations
 
@@ -207,6 +211,13 @@ def make_new_token_kv(w: Workload, num_seqs: int, device="cpu"):
     k = _normal_bf16(shape, w.kv_std, w.seed * 16 + 4, device)
     v = _normal_bf16(shape, w.kv_std, w.seed * 16 + 5, device)
     return k, v
+
+
+def rope_table(max_pos: int, rot: int, theta: float = 500000.0) -> np.ndarray:
+    """float32 [max_pos, rot]: cos of every (position, pair) angle, then sin."""
+    inv = theta ** (-np.arange(0, rot, 2, dtype=np.float64) / rot)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
 
 
 def scale_tensor(value: float, dtype: str, device="cpu") -> torch.Tensor:
