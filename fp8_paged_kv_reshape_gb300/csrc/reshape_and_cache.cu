@@ -404,60 +404,49 @@ __device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], cons
     }
 }
 
-// K rows are rotated, V rows stored as by reshape_and_cache; the warp's rows are all K or
-// all V (is_k), and its table values travel with its row data.
-template <bool kF32, int U, bool kFast, bool kIsK>
-__device__ __forceinline__ void rope_pipelined_rows(const ReshapeArgs &a, const RowCtx &c,
-                                                    int64_t r, int64_t stride, int64_t rows,
-                                                    int lane) {
-    const FastDiv fd(c.s);
+// The tokens of one warp (every W-th token from t, W = warps in the grid): the K row of
+// each, rotated, then its V row.  One row's loads are in flight while the other row is
+// stored, so K and V work is spread evenly over the warps; the table values of the next
+// token travel with its K row's loads.
+template <bool kF32, int U, bool kFast>
+__device__ __forceinline__ void rope_token_rows(const ReshapeArgs &a, const RowCtx &ck,
+                                                const RowCtx &cv, int64_t t, int64_t W,
+                                                int lane) {
+    const FastDiv fk(ck.s), fv(cv.s);
     const int groups = a.row_elems >> 3;
-    auto pos_of = [&](int64_t row) -> int64_t {
-        return row < rows ? __ldg(a.positions + (row >> 1)) : 0;
+    const int64_t T = a.num_tokens;
+    auto slot_at = [&](int64_t tok) -> int64_t {
+        return tok < T ? __ldg(a.slot_mapping + tok) : -1;
     };
-    auto ok_of = [&](int64_t row, int64_t slot, int64_t pos) -> bool {
-        if (row >= rows) return false;
-        const bool sok = slot >= 0 && slot < a.num_slots;
-        if (sok && pos_ok(a, pos)) return true;
-        if (slot != -1 && lane == 0 && (row & 1) == 0) flag(a.status, KVFP8_DEV_BAD_SLOT);
+    auto pos_at = [&](int64_t tok) -> int64_t { return tok < T ? __ldg(a.positions + tok) : 0; };
+    auto ok_of = [&](int64_t tok, int64_t slot, int64_t pos) -> bool {
+        if (tok >= T) return false;
+        if (slot >= 0 && slot < a.num_slots && pos_ok(a, pos)) return true;
+        if (slot != -1 && lane == 0) flag(a.status, KVFP8_DEV_BAD_SLOT);
         return false;
     };
-    Group<kF32> A[U], B[U];
-    RopeCS ta, tb;
-    int64_t s1 = slot_of(a, r, rows), p1 = pos_of(r);
-    int64_t s2 = slot_of(a, r + stride, rows), p2 = pos_of(r + stride);
-    bool ok1 = ok_of(r, s1, p1);
+    Group<kF32> A[U], B[U];  // the K row and the V row
+    RopeCS tc;
+    int64_t s1 = slot_at(t), p1 = pos_at(t);
+    int64_t s2 = slot_at(t + W), p2 = pos_at(t + W);
+    bool ok1 = ok_of(t, s1, p1);
     if (ok1) {
-        load_row<kF32, U>(A, c, r, groups, lane);
-        if (kIsK) load_cs(ta, a, p1, lane);
+        load_row<kF32, U>(A, ck, 2 * t, groups, lane);
+        load_cs(tc, a, p1, lane);
+        load_row<kF32, U>(B, cv, 2 * t + 1, groups, lane);
     }
-    while (r < rows) {
-        int64_t rn = r + stride;
-        bool ok2 = ok_of(rn, s2, p2);
+    while (t < T) {
+        const int64_t tn = t + W;
+        const bool ok2 = ok_of(tn, s2, p2);
+        const int64_t s3 = slot_at(tn + W), p3 = pos_at(tn + W);
+        if (ok1) store_row_rope<kF32, U, kFast>(A, tc, ck, fk, a, s1, groups, lane);
         if (ok2) {
-            load_row<kF32, U>(B, c, rn, groups, lane);
-            if (kIsK) load_cs(tb, a, p2, lane);
+            load_row<kF32, U>(A, ck, 2 * tn, groups, lane);
+            load_cs(tc, a, p2, lane);
         }
-        int64_t s3 = slot_of(a, rn + stride, rows), p3 = pos_of(rn + stride);
-        if (ok1) {
-            if (kIsK) store_row_rope<kF32, U, kFast>(A, ta, c, fd, a, s1, groups, lane);
-            else store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
-        }
-        r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
-        if (r >= rows) break;
-        rn = r + stride;
-        ok2 = ok_of(rn, s2, p2);
-        if (ok2) {
-            load_row<kF32, U>(A, c, rn, groups, lane);
-            if (kIsK) load_cs(ta, a, p2, lane);
-        }
-        s3 = slot_of(a, rn + stride, rows);
-        p3 = pos_of(rn + stride);
-        if (ok1) {
-            if (kIsK) store_row_rope<kF32, U, kFast>(B, tb, c, fd, a, s1, groups, lane);
-            else store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
-        }
-        r = rn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
+        if (ok1) store_row<kF32, U, kFast>(B, cv, fv, s1, a.row_elems, groups, lane);
+        if (ok2) load_row<kF32, U>(B, cv, 2 * tn + 1, groups, lane);
+        t = tn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
     }
 }
 
@@ -470,23 +459,21 @@ __global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const Reshape
         return;
     }
     const int lane = threadIdx.x & 31;
-    const int64_t rows = 2 * a.num_tokens;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;  // even
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-    const bool is_v = (r & 1) != 0;
-    RowCtx c;
-    c.src = static_cast<const uint8_t *>(is_v ? a.value : a.key);
-    c.cache = is_v ? a.value_cache : a.key_cache;
-    c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
-    c.s = is_v ? sv : sk;
-    const bool fast = fast_range(c.s);  // uniform per warp, as is_v
-    if (is_v) {
-        if (fast) rope_pipelined_rows<kF32, U, true, false>(a, c, r, stride, rows, lane);
-        else rope_pipelined_rows<kF32, U, false, false>(a, c, r, stride, rows, lane);
-    } else {
-        if (fast) rope_pipelined_rows<kF32, U, true, true>(a, c, r, stride, rows, lane);
-        else rope_pipelined_rows<kF32, U, false, true>(a, c, r, stride, rows, lane);
-    }
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    RowCtx ck, cv;
+    ck.src = static_cast<const uint8_t *>(a.key);
+    ck.cache = a.key_cache;
+    ck.stride_bytes = a.key_stride * (kF32 ? 4 : 2);
+    ck.s = sk;
+    cv.src = static_cast<const uint8_t *>(a.value);
+    cv.cache = a.value_cache;
+    cv.stride_bytes = a.value_stride * (kF32 ? 4 : 2);
+    cv.s = sv;
+    if (fast_range(sk) && fast_range(sv))
+        rope_token_rows<kF32, U, true>(a, ck, cv, t, W, lane);
+    else
+        rope_token_rows<kF32, U, false>(a, ck, cv, t, W, lane);
 }
 
 // Any row length: one warp per row, groups streamed in rounds of 4 per lane.
@@ -532,8 +519,11 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
     }
 }
 
+// A grid of at most one resident wave, no more warps than units of work (rows, or tokens
+// for the rope kernel).
 template <typename K>
-cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t stream) {
+cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t stream,
+                              int64_t units) {
     int dev = 0, sms = 0, occ = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -542,8 +532,7 @@ cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t strea
     if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kWarps * 32, 0)) !=
         cudaSuccess)
         return err;
-    const int64_t rows = 2 * a.num_tokens;
-    const int64_t want = (rows + kWarps - 1) / kWarps;
+    const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = static_cast<int64_t>(sms) * std::max(occ, 1);
     const unsigned blocks = static_cast<unsigned>(std::min(want, full));
     kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
@@ -553,20 +542,20 @@ cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t strea
 template <bool kF32>
 cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
     const int per_lane = (a.row_elems / 8 + 31) / 32;  // 8-element groups per lane
-    if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<kF32, 1>, a, stream);
-    if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<kF32, 2>, a, stream);
-    if (per_lane <= 4) return launch_persistent(reshape_pipelined_kernel<kF32, 4>, a, stream);
-    if (per_lane <= 8) return launch_persistent(reshape_pipelined_kernel<kF32, 8>, a, stream);
-    return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream);
+    if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<kF32, 1>, a, stream, 2 * a.num_tokens);
+    if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<kF32, 2>, a, stream, 2 * a.num_tokens);
+    if (per_lane <= 4) return launch_persistent(reshape_pipelined_kernel<kF32, 4>, a, stream, 2 * a.num_tokens);
+    if (per_lane <= 8) return launch_persistent(reshape_pipelined_kernel<kF32, 8>, a, stream, 2 * a.num_tokens);
+    return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream, 2 * a.num_tokens);
 }
 
 template <bool kF32>
 cudaError_t dispatch_rope(const ReshapeArgs &a, cudaStream_t stream) {
     const int per_lane = (a.row_elems / 8 + 31) / 32;
-    if (per_lane <= 1) return launch_persistent(rope_reshape_kernel<kF32, 1>, a, stream);
-    if (per_lane <= 2) return launch_persistent(rope_reshape_kernel<kF32, 2>, a, stream);
-    if (per_lane <= 4) return launch_persistent(rope_reshape_kernel<kF32, 4>, a, stream);
-    if (per_lane <= 8) return launch_persistent(rope_reshape_kernel<kF32, 8>, a, stream);
+    if (per_lane <= 1) return launch_persistent(rope_reshape_kernel<kF32, 1>, a, stream, a.num_tokens);
+    if (per_lane <= 2) return launch_persistent(rope_reshape_kernel<kF32, 2>, a, stream, a.num_tokens);
+    if (per_lane <= 4) return launch_persistent(rope_reshape_kernel<kF32, 4>, a, stream, a.num_tokens);
+    if (per_lane <= 8) return launch_persistent(rope_reshape_kernel<kF32, 8>, a, stream, a.num_tokens);
     return cudaErrorNotSupported;
 }
 
