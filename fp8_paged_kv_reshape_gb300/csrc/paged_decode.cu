@@ -11,7 +11,7 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
     DecodeWorkspace w;
     w.cstart_off = 0;
     w.cta_off = up(sizeof(int32_t) * (static_cast<size_t>(num_seqs) + 1));
-    w.lse_off = w.cta_off + up(sizeof(int32_t) * kMaxDecodeCtas);
+    w.lse_off = w.cta_off + up(sizeof(CtaPlan) * kMaxDecodeCtas);
     w.o_off = w.lse_off + up(sizeof(float) * parts * n_q);
     w.total = w.o_off + up(sizeof(float) * parts * n_q * head_dim);
     return w;

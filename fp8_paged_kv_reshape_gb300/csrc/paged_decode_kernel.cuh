@@ -15,8 +15,9 @@
 //    a combine kernel merges them, one thread per four output dims.  Partial (seq, cta)
 //    pairs are stored at index seq+cta, which is unique because both grow monotonically
 //    along the chunk order.  A one-CTA plan kernel computes the chunk prefix over the
-//    sequences first.  Plan -> decode -> combine are chained as programmatic dependent
-//    launches, so each grid's launch and prologue overlap its predecessor.
+//    sequences first, and one record per CTA (its chunk range and first sequence, so a
+//    CTA starts with one load).  Plan -> decode -> combine are chained as programmatic
+//    dependent launches, so each grid's launch and prologue overlap its predecessor.
 //  * One CTA = one producer warp + one consumer warp per kv head.  A 16-token chunk of a
 //    block holds all kv heads of those tokens (16 contiguous rows of n_kv*head_dim bytes),
 //    so the producer issues TMA tensor loads of [16 rows x 128 B] boxes (one per head and
@@ -71,6 +72,13 @@ struct ChunkMeta {
 };
 enum : int32_t { kFirst = 1, kLast = 2, kDirect = 4, kDone = 8 };
 
+// The plan's record for one decode CTA: chunk range [lo, hi) (empty past the effective
+// grid), the sequence s holding chunk lo, its chunk range [cs, ce) and length L, and the
+// total chunk count T.
+struct CtaPlan {
+    int32_t lo, hi, s, cs, ce, L, T, pad;
+};
+
 struct KernelArgs {
     __nv_bfloat16 *out;
     const __nv_bfloat16 *query;
@@ -85,7 +93,7 @@ struct KernelArgs {
     const void *v_scale;
     int32_t scale_dtype;
     const int32_t *cstart;
-    const int32_t *cta_seq;  // first sequence of each CTA's chunk range
+    const CtaPlan *cta_plan;  // one record per CTA (from the plan kernel)
     float *part_lse;
     float *part_o;
     uint32_t *status;
@@ -223,6 +231,38 @@ __device__ __forceinline__ uint32_t swz(int row, int cc) {
 
 // ---------------------------------------------------------------- kernels
 
+// Running merge of split-KV partials (lse_c in log2 units, o_c normalized):
+// sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M) with M the running maximum; a part with no
+// visible token (lse = -inf) adds nothing.
+struct PartMerge {
+    float M = -INFINITY, den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    __device__ __forceinline__ void add(float l, const float4 &v) {
+        if (l == -INFINITY) return;
+        if (l > M) {  // rescale what has been summed so far
+            const float r = ex2(M - l);  // 0 while M is still -inf
+            den *= r;
+            acc.x *= r;
+            acc.y *= r;
+            acc.z *= r;
+            acc.w *= r;
+            M = l;
+        }
+        const float w = ex2(l - M);
+        den += w;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+    }
+    // four bf16 outputs: scale * acc / den (zeros when no part saw a token)
+    __device__ __forceinline__ uint2 result(float scale) const {
+        const float inv = den > 0.f ? scale / den : 0.f;
+        return make_uint2(bf16x2_from_f32(acc.x * inv, acc.y * inv),
+                          bf16x2_from_f32(acc.z * inv, acc.w * inv));
+    }
+};
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -231,14 +271,20 @@ __device__ __forceinline__ void pdl_trigger() {
 // Per-call plan, one CTA of 1024 threads:
 //  * cstart[s] = first chunk of sequence s (exclusive prefix of its 16-token chunk
 //    counts), cstart[num_seqs] = total;
-//  * the output rows of empty sequences are zeroed (no CTA visits them).
+//  * the output rows of empty sequences are zeroed (no CTA visits them);
+//  * one CtaPlan record per decode CTA (the prefix is searched in shared memory when it
+//    fits, else in the global copy).
+constexpr int kPlanSmemSeqs = 8192;
+
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t qrows,
             int32_t num_seqs, int32_t max_len, int32_t num_ctas, int32_t *cstart,
-            int32_t *cta_seq, __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
+            CtaPlan *cta_plan, __nv_bfloat16 *out, int32_t out_row_elems, uint32_t *status) {
     pdl_trigger();  // the decode grid may start its prologue; it waits for this grid's writes
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
+    __shared__ int32_t cs_smem[kPlanSmemSeqs + 1];
+    const bool in_smem = num_seqs <= kPlanSmemSeqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) carry = 0;
     __syncthreads();
@@ -289,25 +335,41 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
         }
         __syncthreads();
         const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + x - n;
-        if (i < num_seqs) cstart[i] = before;
+        if (i < num_seqs) {
+            cstart[i] = before;
+            if (in_smem) cs_smem[i] = before;
+        }
         __syncthreads();
         if (tid == 0) carry += warp_tot[31];
         __syncthreads();
     }
-    if (tid == 0) cstart[num_seqs] = carry;
+    const int32_t total = carry;
+    if (tid == 0) {
+        cstart[num_seqs] = total;
+        if (in_smem) cs_smem[num_seqs] = total;
+    }
     __syncthreads();  // cstart complete (block-visible)
-    // The first sequence of every decode CTA's chunk range: the last s with
-    // cstart[s] <= c*T/P, so a CTA starts with one load instead of a search.
-    const int64_t T = carry;
+    // Each decode CTA's record: its chunk range and the sequence holding its first chunk,
+    // the last s with cstart[s] <= lo.
+    const int32_t *cs_tab = in_smem ? cs_smem : cstart;
+    const int64_t T = total;
     const int64_t P = T < num_ctas ? T : num_ctas;
-    for (int c = tid; c < P; c += blockDim.x) {
-        const int64_t lo_chunk = static_cast<int64_t>(c) * T / P;
-        int lo = 0, hi = num_seqs;  // invariant: cstart[lo] <= lo_chunk < cstart[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (cstart[mid] <= lo_chunk) lo = mid; else hi = mid;
+    for (int c = tid; c < num_ctas; c += blockDim.x) {
+        CtaPlan r = {0, 0, 0, 0, 0, 0, total, 0};
+        if (c < P) {
+            r.lo = static_cast<int32_t>(static_cast<int64_t>(c) * T / P);
+            r.hi = static_cast<int32_t>(static_cast<int64_t>(c + 1) * T / P);
+            int lo = 0, hi = num_seqs;  // invariant: cs_tab[lo] <= r.lo < cs_tab[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cs_tab[mid] <= r.lo) lo = mid; else hi = mid;
+            }
+            r.s = lo;
+            r.cs = cs_tab[lo];
+            r.ce = cs_tab[lo + 1];
+            r.L = min(max(seq_lens[lo], 0), max_len);
         }
-        cta_seq[c] = lo;
+        cta_plan[c] = r;
     }
 }
 
@@ -348,34 +410,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
     const float *lse = a.part_lse + p0 * a.rows_per_seq + row;
     const float *o = a.part_o + (p0 * a.rows_per_seq + row) * HD + d;
     const int64_t lse_stride = a.rows_per_seq, o_stride = static_cast<int64_t>(a.rows_per_seq) * HD;
-    float M = -INFINITY, den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    PartMerge mg;
 #pragma unroll 8
-    for (int c = 0; c < k; ++c) {
-        const float l = lse[c * lse_stride];
-        const float4 v = *reinterpret_cast<const float4 *>(o + c * o_stride);
-        if (l == -INFINITY) continue;  // a part with no valid token
-        if (l > M) {                   // rescale what has been summed so far
-            const float r = ex2(M - l);  // 0 while M is still -inf
-            den *= r;
-            acc.x *= r;
-            acc.y *= r;
-            acc.z *= r;
-            acc.w *= r;
-            M = l;
-        }
-        const float w = ex2(l - M);
-        den += w;
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-    }
-    const float inv = den > 0.f ? sv / den : 0.f;
-    uint2 r;
-    r.x = bf16x2_from_f32(acc.x * inv, acc.y * inv);
-    r.y = bf16x2_from_f32(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = r;
+    for (int c = 0; c < k; ++c)
+        mg.add(lse[c * lse_stride], *reinterpret_cast<const float4 *>(o + c * o_stride));
+    *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = mg.result(sv);
 }
 
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
@@ -433,12 +472,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         return;
     }
     // Effective grid: at most one CTA per chunk, so that every active CTA's range is
-    // non-empty and the CTAs between a sequence's first and last one all hold a part of it.
-    const int64_t T = a.cstart[a.num_seqs];
-    const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);
-    if (static_cast<int64_t>(blockIdx.x) >= P) return;
-    const int64_t chunk_lo = static_cast<int64_t>(blockIdx.x) * T / P;
-    const int64_t chunk_hi = static_cast<int64_t>(blockIdx.x + 1) * T / P;
+    // non-empty and the CTAs between a sequence's first and last one all hold a part of it;
+    // the plan left CTAs past it an empty range.
+    const CtaPlan pl = a.cta_plan[blockIdx.x];
+    if (pl.lo >= pl.hi) return;
+    const int64_t chunk_lo = pl.lo, chunk_hi = pl.hi;
     __syncthreads();
 
     if (warp == a.n_kv) {
@@ -448,9 +486,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         uint32_t phase = 0;
         bool aborted = false;
         if (chunk_lo < chunk_hi) {
-            int s = a.cta_seq[blockIdx.x];  // sequence holding chunk_lo (from the plan)
-            int64_t cs = a.cstart[s], ce = a.cstart[s + 1];
-            int L = min(max(a.seq_lens[s], 0), a.max_len);
+            int s = pl.s;  // sequence holding chunk_lo, its chunks and length (from the plan)
+            int64_t cs = pl.cs, ce = pl.ce;
+            int L = pl.L;
             int wbase = -1 << 30;  // first block-table entry held in the lane window
             int32_t win = 0;
             for (int64_t x = chunk_lo; x < chunk_hi; ++x) {
@@ -1031,7 +1069,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.v_scale = d.v_scale;
     k.scale_dtype = d.scale_dtype;
     k.cstart = reinterpret_cast<const int32_t *>(w + ws.cstart_off);
-    k.cta_seq = reinterpret_cast<const int32_t *>(w + ws.cta_off);
+    k.cta_plan = reinterpret_cast<const CtaPlan *>(w + ws.cta_off);
     k.part_lse = reinterpret_cast<float *>(w + ws.lse_off);
     k.part_o = reinterpret_cast<float *>(w + ws.o_off);
     k.status = d.status;
@@ -1047,7 +1085,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
 
     plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs, k.max_len,
                                         num_ctas, reinterpret_cast<int32_t *>(w + ws.cstart_off),
-                                        reinterpret_cast<int32_t *>(w + ws.cta_off), k.out,
+                                        reinterpret_cast<CtaPlan *>(w + ws.cta_off), k.out,
                                         d.n_q * HD, d.status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
