@@ -272,9 +272,9 @@ __device__ __forceinline__ void pdl_trigger() {
 //  * cstart[s] = first chunk of sequence s (exclusive prefix of its 16-token chunk
 //    counts), cstart[num_seqs] = total;
 //  * the output rows of empty sequences are zeroed (no CTA visits them);
-//  * one CtaPlan record per decode CTA (the prefix is searched in shared memory when it
-//    fits, else in the global copy).
-constexpr int kPlanSmemSeqs = 8192;
+//  * one CtaPlan record per decode CTA (the prefix and the clamped lengths are kept in
+//    shared memory when they fit, else read back from global memory).
+constexpr int kPlanSmemSeqs = 4096;
 
 __global__ void __launch_bounds__(1024)
 plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t qrows,
@@ -284,6 +284,7 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
     __shared__ int32_t warp_tot[32];
     __shared__ int32_t carry;
     __shared__ int32_t cs_smem[kPlanSmemSeqs + 1];
+    __shared__ int32_t len_smem[kPlanSmemSeqs];
     const bool in_smem = num_seqs <= kPlanSmemSeqs;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) carry = 0;
@@ -305,6 +306,7 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
                 if (nq > L) flag(status, KVFP8_DEV_BAD_BLOCK);     // positions below zero
             }
             n = nq > 0 ? (L + kChunkTokens - 1) / kChunkTokens : 0;
+            if (in_smem) len_smem[i] = L;
         }
         unsigned empty = __ballot_sync(0xFFFFFFFFu, i < num_seqs && n == 0);
         while (empty) {  // this warp zeroes the output rows of its empty sequences
@@ -367,7 +369,7 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
             r.s = lo;
             r.cs = cs_tab[lo];
             r.ce = cs_tab[lo + 1];
-            r.L = min(max(seq_lens[lo], 0), max_len);
+            r.L = in_smem ? len_smem[lo] : min(max(seq_lens[lo], 0), max_len);
         }
         cta_plan[c] = r;
     }
@@ -410,10 +412,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
     const float *lse = a.part_lse + p0 * a.rows_per_seq + row;
     const float *o = a.part_o + (p0 * a.rows_per_seq + row) * HD + d;
     const int64_t lse_stride = a.rows_per_seq, o_stride = static_cast<int64_t>(a.rows_per_seq) * HD;
+    // eight parts per batch, every load of a batch issued before the first is used
     PartMerge mg;
-#pragma unroll 8
-    for (int c = 0; c < k; ++c)
-        mg.add(lse[c * lse_stride], *reinterpret_cast<const float4 *>(o + c * o_stride));
+    for (int c0 = 0; c0 < k; c0 += 8) {
+        float l[8];
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            l[i] = -INFINITY;
+            if (c0 + i < k) {
+                l[i] = lse[(c0 + i) * lse_stride];
+                v[i] = *reinterpret_cast<const float4 *>(o + (c0 + i) * o_stride);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mg.add(l[i], v[i]);
+    }
     *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = mg.result(sv);
 }
 

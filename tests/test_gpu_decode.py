@@ -94,6 +94,14 @@ def test_many_short_sequences():
     gpu_util.assert_attention_close(out, ref, "many_short")
 
 
+def test_more_sequences_than_the_plan_keeps_in_shared_memory():
+    # the plan kernel searches its chunk prefix in shared memory up to 4096 sequences and in
+    # global memory beyond; lengths 0..40 give empty, one-chunk and multi-chunk sequences
+    lengths = list(np.random.default_rng(16).integers(0, 41, 5000))
+    out, ref = _case(8, 2, 64, 16, lengths, seed=16)
+    gpu_util.assert_attention_close(out, ref, "5000 seqs")
+
+
 def test_scale_variants():
     lens = [300, 17, 1]
     for kwargs in (dict(sdt=torch.bfloat16), dict(null_scales=True), dict(ks=-0.07, vs=0.5),
