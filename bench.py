@@ -26,6 +26,7 @@ scaling, no collective on the data path); the time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import functools
 import hashlib
 import json
 import math
@@ -440,6 +441,8 @@ def run_ours(args, rank, world, device):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, target_s=args.cpu_seconds,
                                             variant=args.variant)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(
+            args.workload, target_s=max(2.0, args.cpu_seconds / 3), variant=args.variant)
     return line
 
 
@@ -497,9 +500,18 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     rows = np.nonzero(np.isin(lay.row_seq, seqs))[0] if lay.row_seq.size else np.zeros(0, int)
     kh = k_all[torch.from_numpy(rows)].contiguous()
     vh = v_all[torch.from_numpy(rows)].contiguous()
-    slots = lay.slot_mapping[rows]
     pos = np.maximum(lay.row_pos[rows], 0).astype(np.int64)
-    shape = (lay.num_blocks, w.block_size, w.n_kv, w.head_dim)
+    # the sampled sequences' physical blocks, relabelled 0..n-1 into a pool of their own
+    # (the store and the attention do not depend on which physical block holds a page)
+    bt_full = lay.block_tables[seqs]
+    used = np.unique(bt_full[bt_full >= 0])
+    relabel = np.full(lay.num_blocks, -1, np.int64)
+    relabel[used] = np.arange(used.size)
+    bs = w.block_size
+    slots_full = lay.slot_mapping[rows]
+    slots = np.where(slots_full >= 0, relabel[np.maximum(slots_full, 0) // bs] * bs + slots_full % bs, -1)
+    bt = np.where(bt_full >= 0, relabel[np.maximum(bt_full, 0)], -1).astype(np.int32)
+    shape = (max(1, used.size), bs, w.n_kv, w.head_dim)
     k_elem = 2 if variant == "k_bf16" else 1
     v_elem = 2 if variant == "v_bf16" else 1
     kc = np.full(shape, workloads.SENTINEL, np.uint8 if k_elem == 1 else np.uint16)
@@ -522,7 +534,6 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     else:
         oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
     if decode:
-        bt = lay.block_tables[seqs]
         if variant == "multi":
             qrows = (seq_idx[:, None] * qlen + np.arange(qlen)[None, :]).reshape(-1)
             qsl = np.arange(0, qrows.size + 1, qlen, dtype=np.int32)
@@ -543,12 +554,55 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     return dt, nbytes
 
 
+@functools.lru_cache(maxsize=2)
 def _cpu_inputs(name, variant="fp8"):
     w = workloads.WORKLOADS[name]
     lay = workloads.make_layout(w)
     k, v = workloads.make_kv(w, lay.slot_mapping.size, "cpu")
     q = workloads.make_query(w, lay.num_seqs * query_len(w, variant), "cpu")
     return w, lay, k, v, q
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_all_cores(name: str, target_s: float = 4.0, variant: str = "fp8") -> dict:
+    """The same oracle samples run side by side on every host core, one independent sample
+    per thread (the oracle's C calls release the interpreter lock), for about target_s of
+    wall time: throughput = all samples' algorithmic bytes / wall time."""
+    import concurrent.futures as cf
+    import itertools
+    import threading
+
+    w, lay, k, v, q = _cpu_inputs(name, variant)
+    order = np.random.Generator(np.random.PCG64(w.seed + 7)).permutation(lay.num_seqs)
+    cores = host_cores()
+    nxt = itertools.cycle(order.tolist())
+    lock = threading.Lock()
+    t_end = time.perf_counter() + target_s
+
+    def worker():
+        nb, n = 0, 0
+        while time.perf_counter() < t_end:
+            with lock:
+                s = next(nxt)
+            nb += _oracle_sample(w, lay, [int(s)], k, v, q, variant)[1]
+            n += 1
+        return nb, n
+
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+        res = list(ex.map(lambda _: worker(), range(cores)))
+    wall = time.perf_counter() - t0
+    nb = sum(r[0] for r in res)
+    n = sum(r[1] for r in res)
+    return {"value": nb / wall / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d whole-sequence samples of %s, variant %s, on %d threads (one sample "
+                      "per thread at a time), %.1f s wall" % (n, name, variant, cores, wall)}
 
 
 def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dict:

@@ -139,3 +139,14 @@ def test_reference_arm_runs_each_variant():
         assert r.returncode == 0, r.stderr
         d = json.loads(r.stdout.strip().splitlines()[-1])
         assert d["config"]["variant"] == variant and d["value"] > 0
+
+
+def test_cpu_baselines_report_their_threads():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    one = bench.cpu_baseline("tiny", target_s=0.2)
+    allc = bench.cpu_baseline_all_cores("tiny", target_s=0.3)
+    assert one["cores"] == 1 and one["kind"] == "oracle" and one["value"] > 0
+    assert allc["cores"] == bench.host_cores() >= 1 and allc["value"] > 0
+    assert "threads" in allc["sample"]
