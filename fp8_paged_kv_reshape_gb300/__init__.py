@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     check_scale_host,
     dequant,
     paged_attention_multi,
+    paged_attention_multi_workspace_size,
     paged_decode_attention,
     paged_decode_attention_mixed,
     paged_decode_attention_noalloc,

@@ -16,7 +16,7 @@ LIB = os.path.join(LIB_DIR, "libkvfp8.so")
 HEADER = os.path.join(ROOT, "include", "kvfp8.h")
 
 SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "paged_decode_mixed.cu",
-           "dequant.cu", "decode_noalloc.cu"]
+           "prefill_attention.cu", "dequant.cu", "decode_noalloc.cu"]
 DEPS = ["kvfp8_device.cuh", "kvfp8_internal.h", "paged_decode_kernel.cuh"]
 
 NVCC_FLAGS = [

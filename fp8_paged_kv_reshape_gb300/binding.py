@@ -34,6 +34,7 @@ ABI_FUNCTIONS = (
     "kvfp8_paged_decode_attention",
     "kvfp8_paged_decode_attention_noalloc",
     "kvfp8_paged_attention_multi",
+    "kvfp8_paged_attention_multi_workspace_size",
     "kvfp8_reshape_and_cache_mixed",
     "kvfp8_paged_decode_attention_mixed",
     "kvfp8_dequant",
@@ -76,6 +77,8 @@ def _load() -> ctypes.CDLL:
                                                 i32, i32, i32, f32, P, P, ctypes.c_int, P, sz, P,
                                                 P]
     lib.kvfp8_paged_attention_multi.restype = ctypes.c_int
+    lib.kvfp8_paged_attention_multi_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.kvfp8_paged_attention_multi_workspace_size.restype = sz
     lib.kvfp8_reshape_and_cache_mixed.argtypes = [P, P, ctypes.c_int, i64, i64, i64, P,
                                                   ctypes.c_int, P, ctypes.c_int, i32, i32, i32,
                                                   i32, P, P, P, ctypes.c_int, P, P]
@@ -249,6 +252,12 @@ def paged_decode_attention(query: torch.Tensor, key_cache: torch.Tensor, value_c
     return out
 
 
+def paged_attention_multi_workspace_size(num_seqs: int, n_q: int, n_kv: int, head_dim: int,
+                                         max_query_len: int) -> int:
+    return int(LIB.kvfp8_paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, head_dim,
+                                                              max_query_len))
+
+
 def paged_attention_multi(query: torch.Tensor, query_start_loc: torch.Tensor, max_query_len: int,
                           key_cache: torch.Tensor, value_cache: torch.Tensor,
                           block_tables: torch.Tensor, seq_lens: torch.Tensor,
@@ -271,16 +280,16 @@ def paged_attention_multi(query: torch.Tensor, query_start_loc: torch.Tensor, ma
     num_blocks, bs, n_kv, _ = key_cache.shape
     if out is None:
         out = torch.empty_like(query)
-    need = paged_decode_workspace_size(num_seqs, n_q * max_query_len, hd)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=query.device)
+    need = paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, hd, max_query_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
     sdt = _scale_args(k_scale, v_scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     rc = LIB.kvfp8_paged_attention_multi(
         _ptr(out), _ptr(query), _ptr(query_start_loc), rows, max_query_len, _ptr(key_cache),
         _ptr(value_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
         n_q, n_kv, hd, bs, num_blocks, float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt,
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
-        _stream(stream))
+        _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
     _check(rc, "kvfp8_paged_attention_multi")
     return out
 

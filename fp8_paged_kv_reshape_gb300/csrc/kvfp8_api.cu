@@ -194,6 +194,14 @@ kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const ui
     return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t kvfp8_paged_attention_multi_workspace_size(int32_t num_seqs, int32_t n_q, int32_t n_kv,
+                                                  int32_t head_dim, int32_t max_query_len) {
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || head_dim < 1 || max_query_len < 1)
+        return 0;
+    if (!kvfp8::multi_uses_decode_kernel(n_q, n_kv, head_dim, max_query_len)) return 0;
+    return kvfp8::decode_workspace_layout(num_seqs, n_q * max_query_len, head_dim).total;
+}
+
 kvfp8_status kvfp8_paged_attention_multi(
     void *out, const void *query, const int32_t *query_start_loc, int32_t num_query_rows,
     int32_t max_query_len, const uint8_t *key_cache, const uint8_t *value_cache, const int32_t *block_tables,
@@ -207,9 +215,9 @@ kvfp8_status kvfp8_paged_attention_multi(
         return KVFP8_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
     if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
-    const int64_t cols = static_cast<int64_t>(max_query_len) * (n_q / n_kv);
-    if (cols > 16 || n_kv > 8 || static_cast<int64_t>(n_kv) * head_dim > 2048 ||
-        (head_dim == 256 && cols > 8))
+    const bool split_kv = kvfp8::multi_uses_decode_kernel(n_q, n_kv, head_dim, max_query_len);
+    if (!split_kv && (n_q / n_kv > 128 ||
+                      (static_cast<int64_t>(max_query_len) * (n_q / n_kv) + 127) / 128 > 65535))
         return KVFP8_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
@@ -217,14 +225,14 @@ kvfp8_status kvfp8_paged_attention_multi(
     if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
     if (num_seqs == 0) return KVFP8_OK;
     if (!out || !query || !query_start_loc || !key_cache || !value_cache || !block_tables ||
-        !seq_lens || !workspace)
+        !seq_lens || (split_kv && !workspace))
         return KVFP8_ERR_NULL;
     if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
         !aligned16(value_cache) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
-        !aligned(query_start_loc, 4) || !aligned16(workspace))
+        !aligned(query_start_loc, 4) || (split_kv && !aligned16(workspace)))
         return KVFP8_ERR_ALIGN;
     if (workspace_bytes <
-        kvfp8_paged_decode_workspace_size(num_seqs, n_q * max_query_len, head_dim))
+        kvfp8_paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, head_dim, max_query_len))
         return KVFP8_ERR_WORKSPACE;
     kvfp8::DecodeArgs d;
     d.out = out;

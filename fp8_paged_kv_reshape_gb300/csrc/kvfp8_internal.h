@@ -87,6 +87,13 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t stream);
 // The mixed-dtype instances (exactly one of k_bf16 / v_bf16 set); called by the above.
 cudaError_t launch_paged_decode_mixed(const DecodeArgs &a, cudaStream_t stream);
 
+// Multi-query (causal) attention on the tensor cores (tcgen05): long query chunks, or kv-head
+// counts the split-KV decode kernel does not cover.  Needs no workspace.
+cudaError_t launch_prefill_attention(const DecodeArgs &a, cudaStream_t stream);
+// True when kvfp8_paged_attention_multi takes the split-KV decode kernel for this shape
+// (and so needs a workspace); false when it takes the prefill kernel.
+bool multi_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t max_query_len);
+
 cudaError_t launch_dequant(void *dst, int dst_dtype, const uint8_t *src, int64_t n,
                            const void *scale, int scale_dtype, cudaStream_t stream);
 

@@ -17,9 +17,17 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
     return w;
 }
 
+bool multi_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t max_query_len) {
+    const int64_t cols = static_cast<int64_t>(max_query_len) * (n_q / n_kv);
+    return cols <= 16 && !(head_dim == 256 && cols > 8) && n_kv <= kMaxKvHeads &&
+           static_cast<int64_t>(n_kv) * head_dim <= 2048;
+}
+
 cudaError_t launch_paged_decode(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
     if (d.k_bf16 || d.v_bf16) return launch_paged_decode_mixed(d, stream);
+    if (d.qsl != nullptr && !multi_uses_decode_kernel(d.n_q, d.n_kv, d.head_dim, d.qmax))
+        return launch_prefill_attention(d, stream);
     const DecodeWorkspace ws = decode_workspace_layout(d.num_seqs, d.qmax * d.n_q, d.head_dim);
     const int group = d.n_q / d.n_kv;
     if (d.n_kv > kMaxKvHeads) return cudaErrorNotSupported;

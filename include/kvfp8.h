@@ -246,17 +246,32 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
  *   out[row][h] = v_scale * sum_{t<=p} softmax_t(sm_scale*k_scale*q[row][h].dec(K_t)) dec(V_t)
  * n_b = 1 for every sequence is kvfp8_paged_decode_attention.
  *
+ * Two kernels serve the call.  With max_query_len * (n_q / n_kv) <= 16 score columns per
+ * kv head (<= 8 at head_dim 256), n_kv <= 8 and n_kv*head_dim <= 2048, the split-KV decode
+ * kernel runs and needs the workspace below.  Every other shape (long query chunks,
+ * prefill) runs on the tensor cores (tcgen05, accumulators in tensor memory), one CTA per
+ * 128 (query token, head) rows of a kv head, with no workspace; it needs
+ * n_q / n_kv <= 128.
+ *
  * out, query        device bf16 [num_query_rows][n_q][head_dim]
  * query_start_loc   device int32 [num_seqs + 1], non-decreasing; a sequence whose rows
  *                   fall outside [0, num_query_rows) or number more than max_query_len is
  *                   skipped and sets KVFP8_DEV_BAD_BLOCK; n_b > L also sets it (positions
  *                   below zero attend to nothing and give zero rows)
- * max_query_len     >= 1 with max_query_len * (n_q / n_kv) <= 16 (<= 8 at head_dim 256);
- *                   larger prefill chunks return KVFP8_ERR_UNSUPPORTED
- * workspace         >= kvfp8_paged_decode_workspace_size(num_seqs, n_q * max_query_len,
- *                   head_dim) bytes
+ * max_query_len     >= 1
+ * workspace         >= kvfp8_paged_attention_multi_workspace_size(...) bytes (may be NULL
+ *                   when that is 0)
  * Everything else as kvfp8_paged_decode_attention.
  */
+/*
+ * Workspace bytes kvfp8_paged_attention_multi needs for this shape: the split-KV partials
+ * (kvfp8_paged_decode_workspace_size(num_seqs, n_q * max_query_len, head_dim)) when the
+ * decode kernel serves it, 0 when the tensor-core kernel does.  Pure host arithmetic.
+ */
+KVFP8_API size_t kvfp8_paged_attention_multi_workspace_size(int32_t num_seqs, int32_t n_q,
+                                                            int32_t n_kv, int32_t head_dim,
+                                                            int32_t max_query_len);
+
 KVFP8_API kvfp8_status kvfp8_paged_attention_multi(
     void *out, const void *query, const int32_t *query_start_loc, int32_t num_query_rows,
     int32_t max_query_len, const uint8_t *key_cache, const uint8_t *value_cache,

@@ -174,3 +174,35 @@ def test_mixed_decode_host_validation():
     assert call(num_seqs=0, query=None) == binding.OK
     # both sides E4M3 is the all-FP8 call, with its own validation
     assert call(v_kind=binding.CACHE_E4M3, head_dim=96) == binding.ERR_SHAPE
+
+
+def test_multi_query_workspace_follows_the_kernel_that_serves_the_shape():
+    dec = kv.paged_decode_workspace_size
+    ws = kv.paged_attention_multi_workspace_size
+    # split-KV decode kernel: up to 16 score columns per kv head (8 at head_dim 256), n_kv <= 8
+    assert ws(4, 32, 8, 128, 4) == dec(4, 32 * 4, 128) > 0
+    assert ws(4, 4, 2, 256, 4) == dec(4, 4 * 4, 256) > 0
+    # tensor-core kernel: no workspace
+    assert ws(4, 32, 8, 128, 5) == 0          # 20 columns
+    assert ws(4, 4, 2, 256, 5) == 0           # 10 columns at head_dim 256
+    assert ws(4, 16, 16, 128, 1) == 0         # 16 kv heads
+    assert ws(-1, 32, 8, 128, 4) == 0
+
+
+def test_multi_query_host_validation_on_the_tensor_core_route():
+    def call(**over):
+        args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16), qsl=ctypes.c_void_p(16),
+                    rows=64, qmax=64, key_cache=ctypes.c_void_p(16),
+                    value_cache=ctypes.c_void_p(16), block_tables=ctypes.c_void_p(16),
+                    max_blocks_per_seq=256, seq_lens=ctypes.c_void_p(16), num_seqs=1, n_q=32,
+                    n_kv=8, head_dim=128, block_size=16, num_blocks=1024, sm_scale=0.0,
+                    k_scale=None, v_scale=None, scale_dtype=binding.F32, workspace=None,
+                    workspace_bytes=0, status=None, stream=None)
+        args.update(over)
+        return kv.LIB.kvfp8_paged_attention_multi(*args.values())
+    assert call(query=None) == binding.ERR_NULL
+    assert call(qsl=ctypes.c_void_p(18)) == binding.ERR_ALIGN
+    assert call(n_q=129 * 2, n_kv=2) == binding.ERR_UNSUPPORTED     # group of 129 heads
+    assert call(num_seqs=0, query=None) == binding.OK
+    # the split-KV route still wants its workspace
+    assert call(qmax=4, workspace=None) == binding.ERR_NULL
