@@ -19,6 +19,9 @@ Default workload: llama3_8b (32 q / 8 kv heads, head_dim 128, block 16, 64 seque
           paged_decode_attention_mixed); v_bf16 the other way round
   multi   causal multi-query attention (paged_attention_multi) with 16 // G query
           tokens per sequence (G = n_q / n_kv), after the same cache write
+  prefill chunked prefill: the context is in the cache before timing; a step writes the
+          last 512 tokens of every sequence (16 on mixed_serving) and runs causal
+          attention for them (paged_attention_multi on its tensor-core kernel)
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, weak
 scaling, no collective on the data path); the time is the max over ranks.
@@ -52,7 +55,7 @@ KERNEL_SOURCES = {
     "paged_decode_attention": ["fp8_paged_kv_reshape_gb300/csrc/paged_decode_kernel.cuh",
                                "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
 }
-VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi")
+VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi", "prefill")
 METRIC = "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak"
 
 
@@ -90,15 +93,31 @@ def decode_bytes(w: workloads.Workload, seq_lens: np.ndarray, k_elem: int = 1, v
     return kv + tables + qo + qsl
 
 
-def query_len(w: workloads.Workload, variant: str) -> int:
-    """Query tokens per sequence: 16 // G score columns' worth for the multi-query variant."""
-    return max(1, 16 // (w.n_q // w.n_kv)) if variant == "multi" else 1
+def query_len(w: workloads.Workload, variant: str, seq_lens: np.ndarray | None = None) -> int:
+    """Query tokens per sequence: 16 // G score columns' worth for the multi-query variant;
+    for prefill a 512-token chunk, or the shortest context when that is shorter (16 on the
+    serving mix)."""
+    if variant == "multi":
+        return max(1, 16 // (w.n_q // w.n_kv))
+    if variant == "prefill":
+        shortest = int(seq_lens.min()) if seq_lens is not None and seq_lens.size else 512
+        return max(1, min(512, shortest))
+    return 1
 
 
-def step_rows(w: workloads.Workload, lay: workloads.Layout, qlen: int):
+def attention_flops(w: workloads.Workload, seq_lens: np.ndarray, qlen: int) -> int:
+    """Tensor FLOPs of causal attention for qlen new tokens per sequence: every (query head,
+    visible key) pair costs 2*hd for q.k and 2*hd for p.v; token j of a sequence of length
+    L sees L - qlen + j + 1 keys."""
+    L = seq_lens.astype(np.int64)
+    pairs = int((qlen * (L - qlen) + qlen * (qlen + 1) // 2).sum())
+    return 4 * w.head_dim * w.n_q * pairs
+
+
+def step_rows(w: workloads.Workload, lay: workloads.Layout, qlen: int, serving: bool = False):
     """(slots, positions) of the rows one step writes: every context row, or for a serving
     step the last qlen tokens of every sequence (sequence-major)."""
-    if w.kind != "mixed":
+    if w.kind != "mixed" and not serving:
         return lay.slot_mapping, np.maximum(lay.row_pos, 0).astype(np.int64)
     L = lay.seq_lens.astype(np.int64)
     pos = (L[:, None] - qlen + np.arange(qlen)[None, :]).reshape(-1)
@@ -139,6 +158,18 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense f16/bf16 tensor TFLOP/s: the measured sustained cuBLAS bf16 figure (the kernel
+    runs inside a step repeated back to back; f16 and bf16 share one tensor rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops_sustained" in d:
+            return float(d["bf16_tflops_sustained"]), "measured (bf16 sustained)"
+    return 1700.0, "fallback (bf16 sustained)"
 
 
 def recorded_traffic(kernel: str, workload: str):
@@ -217,12 +248,12 @@ class Problem:
         self.kv = kv
         self.w = w = workloads.WORKLOADS[name]
         self.variant = variant
-        if variant == "multi" and w.kind == "write":
+        if variant in ("multi", "prefill") and w.kind == "write":
             raise ValueError("the %s workload has no attention step" % name)
         self.lay = lay = workloads.make_layout(w, num_seqs=num_seqs)
         self.device = device
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        self.qlen = query_len(w, variant)
+        self.qlen = query_len(w, variant, lay.seq_lens)
         self.ksc = workloads.scale_tensor(w.k_scale, w.scale_dtype, device)
         self.vsc = workloads.scale_tensor(w.v_scale, w.scale_dtype, device)
         self.k_elem = 2 if variant == "k_bf16" else 1
@@ -234,8 +265,9 @@ class Problem:
         if variant == "rope":
             max_pos = max(1, int(lay.seq_lens.max()) if lay.num_seqs else 1)
             self.table = torch.from_numpy(workloads.rope_table(max_pos, self.rot)).to(device)
-        slots, pos = step_rows(w, lay, self.qlen)
-        if w.kind == "mixed":
+        self.serving = w.kind == "mixed" or variant == "prefill"
+        slots, pos = step_rows(w, lay, self.qlen, self.serving)
+        if self.serving:
             # the cache holds the context before the timed region; a step writes the last
             # qlen tokens of every sequence and attends
             ctx_k, ctx_v = workloads.make_kv(w, lay.slot_mapping.size, device)
@@ -255,16 +287,21 @@ class Problem:
             self.bt = torch.from_numpy(lay.block_tables).to(device)
             self.sl = torch.from_numpy(lay.seq_lens).to(device)
             self.qsl = torch.arange(0, rows + 1, self.qlen, dtype=torch.int32, device=device) \
-                if variant == "multi" else None
+                if variant in ("multi", "prefill") else None
             self.out = torch.empty_like(self.q)
-            self.ws = torch.empty(kv.paged_decode_workspace_size(lay.num_seqs, w.n_q * self.qlen,
-                                                                 w.head_dim),
-                                  dtype=torch.uint8, device=device)
+            if self.qsl is not None:
+                need = kv.paged_attention_multi_workspace_size(lay.num_seqs, w.n_q, w.n_kv,
+                                                                w.head_dim, self.qlen)
+            else:
+                need = kv.paged_decode_workspace_size(lay.num_seqs, w.n_q, w.head_dim)
+            self.tensor_route = self.qsl is not None and need == 0
+            self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
         self.rs_bytes = reshape_bytes(w, slots, 2, self.k_elem, self.v_elem,
                                       pos if variant == "rope" else None, self.rot)
         self.dec_bytes = decode_bytes(w, lay.seq_lens, self.k_elem, self.v_elem,
-                                      self.lay.num_seqs * self.qlen if variant == "multi" else None) \
+                                      self.lay.num_seqs * self.qlen if self.qsl is not None else None) \
             if self.decode else 0
+        self.attn_flops = attention_flops(w, lay.seq_lens, self.qlen) if self.decode else 0
 
     def _new_cache(self, elem: int) -> torch.Tensor:
         if elem == 1:
@@ -290,7 +327,7 @@ class Problem:
 
     def attend(self):
         kv = self.kv
-        if self.variant == "multi":
+        if self.qsl is not None:
             kv.paged_attention_multi(self.q, self.qsl, self.qlen, self.kc, self.vc, self.bt,
                                      self.sl, self.ksc, self.vsc, out=self.out, workspace=self.ws,
                                      status=self.status)
@@ -315,14 +352,17 @@ class Problem:
         return ins
 
     def launches_per_step(self) -> int:
-        return 1 + (3 if self.decode else 0)  # write; plan + split-KV attention + combine
+        # write; then plan + split-KV attention + combine, or one tensor-core attention kernel
+        return 1 + ((1 if self.tensor_route else 3) if self.decode else 0)
 
     def describe(self) -> dict:
         w, lay = self.w, self.lay
         write = {"fp8": "reshape_and_cache", "multi": "reshape_and_cache",
+                 "prefill": "reshape_and_cache",
                  "rope": "rope_reshape_and_cache", "k_bf16": "reshape_and_cache_mixed",
                  "v_bf16": "reshape_and_cache_mixed"}[self.variant]
-        attn = {"multi": "paged_attention_multi", "k_bf16": "paged_decode_attention_mixed",
+        attn = {"multi": "paged_attention_multi", "prefill": "paged_attention_multi (tcgen05)",
+                "k_bf16": "paged_decode_attention_mixed",
                 "v_bf16": "paged_decode_attention_mixed"}.get(self.variant,
                                                               "paged_decode_attention")
         d = {"workload": w.name, "variant": self.variant, "n_q": w.n_q, "n_kv": w.n_kv,
@@ -416,15 +456,28 @@ def run_ours(args, rank, world, device):
     if p.decode:
         kernels["paged_decode_attention"] = {"bytes_per_launch": p.dec_bytes, "ms": dec_ms,
                                              "gbs": p.dec_bytes / (dec_ms * 1e-3) / 1e9,
-                                             "launches": 3}
+                                             "launches": 1 if p.tensor_route else 3}
     for k in kernels.values():
         k["frac"] = k["gbs"] / peak
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
-    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
-            "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
-            "traffic": recorded_traffic(dom, args.workload if args.variant == "fp8"
-                                        else "%s:%s" % (args.workload, args.variant)),
-            "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
+    traffic = recorded_traffic(dom, args.workload if args.variant == "fp8"
+                               else "%s:%s" % (args.workload, args.variant))
+    if p.decode and p.tensor_route:
+        att = kernels["paged_decode_attention"]
+        att["tflops"] = p.attn_flops / (att["ms"] * 1e-3) / 1e12
+        att["flops_per_launch"] = p.attn_flops
+    if dom == "paged_decode_attention" and p.tensor_route:
+        tpeak, tkind = measured_tensor_peak()
+        att = kernels[dom]
+        roof = {"bound": "tensor", "kernel": dom, "achieved": att["tflops"], "peak": tpeak,
+                "peak_kind": tkind, "unit": "TFLOP/s", "frac": att["tflops"] / tpeak,
+                "traffic": traffic, "algorithmic_flops_per_launch": p.attn_flops,
+                "algorithmic_bytes_per_launch": att["bytes_per_launch"]}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
     value = whole_job_gbs(per_step, args.steps, world, total_ms)
     line = {
         "metric": METRIC,
@@ -520,7 +573,7 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
              oracle.E4M3 if v_elem == 1 else oracle.CACHE_BF16)
     decode = w.kind != "write"
     sub_lens = lay.seq_lens[seqs]
-    qlen = query_len(w, variant)
+    qlen = query_len(w, variant, lay.seq_lens)
     seq_idx = np.asarray(seqs)
     table = workloads.rope_table(max(1, int(lay.seq_lens.max())), w.head_dim) \
         if variant == "rope" else None
@@ -534,7 +587,7 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     else:
         oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
     if decode:
-        if variant == "multi":
+        if variant in ("multi", "prefill"):
             qrows = (seq_idx[:, None] * qlen + np.arange(qlen)[None, :]).reshape(-1)
             qsl = np.arange(0, qrows.size + 1, qlen, dtype=np.int32)
             oracle.paged_attention_multi(q[torch.from_numpy(qrows)], qsl, kc, vc, bt, sub_lens,
@@ -550,7 +603,7 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
                            w.head_dim)
     if decode:
         nbytes += decode_bytes(w, sub_lens, k_elem, v_elem,
-                               len(seqs) * qlen if variant == "multi" else None)
+                               len(seqs) * qlen if variant in ("multi", "prefill") else None)
     return dt, nbytes
 
 
@@ -559,7 +612,7 @@ def _cpu_inputs(name, variant="fp8"):
     w = workloads.WORKLOADS[name]
     lay = workloads.make_layout(w)
     k, v = workloads.make_kv(w, lay.slot_mapping.size, "cpu")
-    q = workloads.make_query(w, lay.num_seqs * query_len(w, variant), "cpu")
+    q = workloads.make_query(w, lay.num_seqs * query_len(w, variant, lay.seq_lens), "cpu")
     return w, lay, k, v, q
 
 

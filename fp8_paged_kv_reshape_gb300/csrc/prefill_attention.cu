@@ -11,19 +11,22 @@
 //    (query token j, head g of the kv head's group) pair, row = j*G + g, so all rows of a
 //    tile share one K/V stream.  Keys are visited in tiles of 64 up to the tile's last
 //    causal position.
-//  * Warps 0-3 (one TMEM lane quarter each, one score row per thread):
-//      - convert the tile's q rows bf16 -> f16 once, and each K tile e4m3 -> f16, into the
-//        K-major 128-byte-swizzled operand layout; each V tile e4m3 -> f16 transposed
-//        (V^T: head dims as rows, keys along K), so both products take K-major operands;
-//      - thread 0 issues S = Q.K^T (tcgen05.mma kind::f16, M = 128, N = 64, fp32 in TMEM);
-//      - every thread reads its row of S from TMEM, applies the causal mask and the online
-//        softmax (log2 domain), writes P (f16) back over S in TMEM;
-//      - thread 0 issues O += P.V (A = P from TMEM, B = V^T from shared memory, M = 128,
-//        N = head_dim, fp32 in TMEM).  O is rescaled in TMEM only when a row's running
-//        maximum grows by more than 2^8 (then P <= 2^8 stays well inside fp16);
-//      - the epilogue reads O, divides by the row sum, applies v_scale and stores bf16.
-//  * Warp 4 issues the TMA loads of the FP8 K/V tiles (the per-head-segment boxes of the
-//    decode kernel's cache map) into a two-stage ring.
+//  * Warp-specialized, every stage overlapped with the others:
+//      - warp 9 issues the TMA loads of the FP8 K/V tiles (the per-head-segment boxes of
+//        the decode kernel's cache map) into a multi-stage ring;
+//      - warps 4-7 convert the tile's q rows bf16 -> f16 once, and each K tile
+//        e4m3 -> f16, into the K-major 128-byte-swizzled operand layout, and each V tile
+//        e4m3 -> f16 transposed (V^T: head dims as rows, keys along K), so both products
+//        take K-major operands; K and V^T are double-buffered;
+//      - one thread of warp 8 issues S(i) = Q.K(i)^T (tcgen05.mma kind::f16, M = 128,
+//        N = 64, fp32 in one of two TMEM buffers) and then O += P(i-1).V(i-1) (A = P from
+//        TMEM, B = V^T from shared memory, N = head_dim), so the next scores are computed
+//        while the softmax works on the current ones;
+//      - warps 0-3 (one TMEM lane quarter each, one score row per thread) read S, apply
+//        the causal mask and the online softmax (log2 domain), and write P (f16) back over
+//        S.  O is rescaled in TMEM only when a row's running maximum grows by more than
+//        2^8 (P <= 2^8 stays well inside fp16); at the end they divide by the row sum,
+//        apply v_scale and store bf16.
 //  * All waits are bounded (mbarriers with a clock64 limit); a wait that runs out sets
 //    KVFP8_DEV_TIMEOUT.  Tensor memory is always released before the CTA exits.
 #include "paged_decode_kernel.cuh"
@@ -33,7 +36,6 @@ namespace {
 
 constexpr int kPfRows = 128;   // score rows per CTA (TMEM lanes)
 constexpr int kPfKeys = 64;    // keys per tile
-constexpr int kPfThreads = 160;  // 4 compute warps + 1 producer warp
 
 // ---------------------------------------------------------------- tcgen05 wrappers
 
@@ -80,6 +82,15 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// four 8x8 b16 matrices stored transposed: lane t gives (rows 2(t%4), 2(t%4)+1; column t/4)
+// of matrix j in r[j], and the address of row t%8 of matrix t/8
+__device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                          uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // generic-proxy shared-memory writes become visible to the tensor core (async proxy)
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -133,27 +144,47 @@ struct PrefillArgs {
     int32_t box_rows;
 };
 
-// Shared-memory plan (byte offsets from a 1024-aligned base).
+// Shared-memory plan (byte offsets from a 1024-aligned base).  Q is converted once; K and
+// V^T (f16) have NB buffers, and so do the scores in tensor memory; the FP8 staging ring has
+// NS stages.  At head_dim 256 the f16 buffers fill the shared memory: NB = 2, NS = 1.
 template <int HD>
 struct PfSmem {
     static constexpr int kSeg = HD >= 128 ? 128 : 64;             // fp8 TMA box row (swizzle span)
     static constexpr int kSegs = HD / kSeg;
+    static constexpr int kNB = HD >= 256 ? 2 : 3;                  // f16 K/V^T and S buffers
+    static constexpr int kNS = HD >= 256 ? 1 : 4;                  // FP8 staging stages
     static constexpr int kQ = 0;                                   // Q f16: HD/64 blocks x 128 rows x 128 B
-    static constexpr int kK = kQ + HD * 256;                       // K f16: HD/64 blocks x 64 rows x 128 B
-    static constexpr int kV = kK + HD * 128;                       // V^T f16: HD rows x 128 B
-    static constexpr int kStage = kV + HD * 128;                   // fp8 K then V, per stage
+    static constexpr int kKBuf = HD * 128;                         // one K f16 buffer: HD/64 x 64 rows x 128 B
+    static constexpr int kVBuf = HD * 128;                         // one V^T f16 buffer: HD rows x 128 B
+    static constexpr int kK = kQ + HD * 256;
+    static constexpr int kV = kK + kNB * kKBuf;
+    static constexpr int kStage = kV + kNB * kVBuf;                // fp8 K then V, per stage
     static constexpr int kStageBytes = 2 * kPfKeys * HD;
-    static constexpr int kBars = kStage + 2 * kStageBytes;         // full[2], empty[2], s, o, wg
-    static constexpr int kMeta = kBars + 8 * 8;                    // valid-key mask per stage
-    static constexpr int kMisc = kMeta + 16;                       // tmem base, abort flag
+    static constexpr int kBars = kStage + kNS * kStageBytes;
+    // mbarriers: full[NS], empty[NS], then per buffer kv_ready, kv_free, s_ready, p_ready.
+    // kv_free[b] completes when the products of the buffer's tile are done (one commit after
+    // its O product covers its S product too); it also tells that O is up to date.
+    static constexpr int kFull = kBars, kEmpty = kFull + 8 * kNS, kKvReady = kEmpty + 8 * kNS;
+    static constexpr int kKvFree = kKvReady + 8 * kNB, kSReady = kKvFree + 8 * kNB;
+    static constexpr int kPReady = kSReady + 8 * kNB;
+    static constexpr int kMeta = kPReady + 8 * kNB;                // valid-key mask per stage
+    static constexpr int kBufMask = kMeta + 8 * kNS;               // valid-key mask per K/V buffer
+    static constexpr int kMisc = kBufMask + 8 * kNB;               // tmem base, abort flag
     static constexpr int kTotal = kMisc + 16;
-    static constexpr uint32_t kTmemCols = HD + 64 <= 128 ? 128 : (HD + 64 <= 256 ? 256 : 512);
-    static constexpr uint32_t kColS = 0;   // S (64 fp32 columns); P (f16) reuses its first 32
-    static constexpr uint32_t kColO = 64;  // O (HD fp32 columns)
+    // tensor memory: S[NB] (64 fp32 columns each; P as f16 over the first 32), then O
+    static constexpr uint32_t kColO = 64 * kNB;
+    static constexpr uint32_t kTmemCols = kColO + HD <= 256 ? 256 : 512;
 };
 
+// Warp roles (448 threads): warps 0-3 softmax + epilogue (TMEM lane quarters 0-3, one score
+// row per thread), warps 4-11 conversion, warp 12 tensor-core issue (and TMEM allocation),
+// warp 13 TMA.
+constexpr int kPfConvWarps = 8;
+constexpr int kPfMmaWarp = 4 + kPfConvWarps, kPfTmaWarp = kPfMmaWarp + 1;
+constexpr int kPfWarps = kPfTmaWarp + 1;
+
 template <int HD>
-__global__ void __launch_bounds__(kPfThreads)
+__global__ void __launch_bounds__(kPfWarps * 32, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                const PrefillArgs a) {
     using L = PfSmem<HD>;
@@ -161,11 +192,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *bp = smem_raw + (base - raw);
-    const uint32_t bar_full = base + L::kBars, bar_empty = bar_full + 16;
-    const uint32_t bar_s = bar_full + 32, bar_o = bar_full + 40, bar_wg = bar_full + 48;
     volatile uint64_t *meta = reinterpret_cast<volatile uint64_t *>(bp + L::kMeta);
+    volatile uint64_t *buf_mask = reinterpret_cast<volatile uint64_t *>(bp + L::kBufMask);
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bp + L::kMisc);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(bp + L::kMisc + 4);
+    auto bar = [&](int off, int i) { return base + static_cast<uint32_t>(off + 8 * i); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seq = blockIdx.x, tile = blockIdx.y, kvh = blockIdx.z;
@@ -179,7 +210,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     // this sequence's query rows and cached length (flagged once, by its first CTA)
     const int raw_nq = a.qsl[seq + 1] - a.qsl[seq];
     const QueryRange qr = query_range(a.qsl, seq, a.qmax, a.qrows);
-    int Lraw = a.seq_lens[seq];
+    const int Lraw = a.seq_lens[seq];
     const int Ls = min(max(Lraw, 0), a.max_len);
     if (tile == 0 && kvh == 0 && tid == 0 &&
         (qr.count != raw_nq || Lraw < 0 || Lraw > a.max_len || qr.count > Ls))
@@ -205,21 +236,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     }
 
     if (tid == 0) {
-        mbar_init(bar_full, 1);
-        mbar_init(bar_full + 8, 1);
-        mbar_init(bar_empty, 4);
-        mbar_init(bar_empty + 8, 4);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
-        mbar_init(bar_wg, 128);
+        for (int s = 0; s < L::kNS; ++s) {
+            mbar_init(bar(L::kFull, s), 1);
+            mbar_init(bar(L::kEmpty, s), kPfConvWarps);
+        }
+        for (int b = 0; b < L::kNB; ++b) {
+            mbar_init(bar(L::kKvReady, b), kPfConvWarps);
+            mbar_init(bar(L::kKvFree, b), 1);
+            mbar_init(bar(L::kSReady, b), 1);
+            mbar_init(bar(L::kPReady, b), 4);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 0) {
+    if (warp == kPfMmaWarp) {
         tmem_alloc(base + L::kMisc, L::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kPfTmaWarp && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
@@ -227,90 +261,141 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const volatile int32_t never = 0;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer warp
+    if (warp == kPfTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        // The warp holds 32 block-table entries, one per lane (refreshed as the tiles move
+        // past them); lane 0 waits for a free stage and issues the copies.
         const int32_t *bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
         const int bs = a.block_size, br = a.box_rows;
-        bool aborted = false;
+        const int nbox = kPfKeys / br;
+        int wbase = -(1 << 30);
+        int32_t win = -1;
         int issued = 0;
-        for (int i = 0; i < ntiles && !aborted; ++i) {
-            const int stage = i & 1;
-            const uint32_t full = bar_full + 8 * stage;
+        bool aborted = false;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % L::kNS;
+            const int t0 = i * kPfKeys;
+            const int e0 = t0 / bs, e1 = (min(kend, t0 + kPfKeys) - 1) / bs;
+            if (e0 < wbase || e1 >= wbase + 32) {  // next window of block-table entries
+                wbase = e0;
+                win = wbase + lane < a.max_blocks_per_seq ? bt[wbase + lane] : -1;
+            }
+            // per box: its first cache row, or -1 (past kend, or a bad block: left out)
+            uint64_t mask = 0;
+            int boxes = 0;
+            int rows[kPfKeys / 8];
+#pragma unroll
+            for (int p = 0; p < kPfKeys / 8; ++p) {
+                rows[p] = -1;
+                if (p >= nbox) continue;
+                const int t = t0 + p * br;
+                const int blk = __shfl_sync(0xFFFFFFFFu, win, (t / bs - wbase) & 31);
+                if (t >= kend) continue;
+                if (blk < 0 || blk >= a.num_blocks) {
+                    if (lane == 0) flag(a.status, KVFP8_DEV_BAD_BLOCK);
+                    continue;
+                }
+                rows[p] = blk * bs + t % bs;
+                ++boxes;
+                const int nk = min(br, kend - t);
+                mask |= (nk >= 64 ? ~0ull : ((1ull << nk) - 1)) << (p * br);
+            }
             if (lane == 0) {
-                if (!mbar_wait(bar_empty + 8 * stage, ((i >> 1) & 1) ^ 1u, abort_flag)) {
+                if (!mbar_wait(bar(L::kEmpty, st), ((i / L::kNS) & 1) ^ 1u, abort_flag)) {
                     aborted = true;
                 } else {
-                    // one box per head segment and box_rows keys; keys past kend or in a bad
-                    // block are left out of the load and of the valid mask
-                    uint64_t mask = 0;
-                    int boxes = 0;
-                    const int nbox = kPfKeys / br;
-                    int rows[kPfKeys / 8];
-                    for (int p = 0; p < nbox; ++p) {
-                        const int t = i * kPfKeys + p * br;
-                        rows[p] = -1;
-                        if (t >= kend) continue;
-                        const int e = t / bs;
-                        const int blk = e < a.max_blocks_per_seq ? bt[e] : -1;
-                        if (blk < 0 || blk >= a.num_blocks) {
-                            flag(a.status, KVFP8_DEV_BAD_BLOCK);
-                            continue;
-                        }
-                        rows[p] = blk * bs + t % bs;
-                        ++boxes;
-                        const int nk = min(br, kend - t);
-                        mask |= (nk >= 64 ? ~0ull : ((1ull << nk) - 1)) << (p * br);
-                    }
-                    meta[stage] = mask;
-                    if (boxes > 0) {
+                    meta[st] = mask;
+                    const uint32_t full = bar(L::kFull, st);
+                    if (boxes > 0)
                         mbar_arrive_tx(full, static_cast<uint32_t>(boxes * L::kSegs * 2 * br * L::kSeg));
-                        const uint32_t kst = base + L::kStage + stage * L::kStageBytes;
-                        const uint32_t vst = kst + kPfKeys * HD;
-                        for (int p = 0; p < nbox; ++p) {
-                            if (rows[p] < 0) continue;
-                            for (int sgi = 0; sgi < L::kSegs; ++sgi) {
-                                const uint32_t off = static_cast<uint32_t>(sgi * kPfKeys * L::kSeg + p * br * L::kSeg);
-                                tma_load_3d(kst + off, &tmk, 0, kvh * L::kSegs + sgi, rows[p], full);
-                                tma_load_3d(vst + off, &tmv, 0, kvh * L::kSegs + sgi, rows[p], full);
-                            }
-                        }
-                    } else {
+                    else
                         mbar_arrive(full);
-                    }
                     ++issued;
                 }
             }
             aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
+            if (aborted) break;
+            // the expected bytes are posted: lane 0 issues the K copies, lane 1 the V copies
+            if (lane < 2 && boxes > 0) {
+                const uint32_t full = bar(L::kFull, st);
+                const uint32_t dst = base + L::kStage + st * L::kStageBytes + lane * (kPfKeys * HD);
+                const CUtensorMap *map = lane == 0 ? &tmk : &tmv;
+#pragma unroll
+                for (int p = 0; p < kPfKeys / 8; ++p) {
+                    if (rows[p] < 0) continue;
+                    for (int sgi = 0; sgi < L::kSegs; ++sgi)
+                        tma_load_3d(dst + static_cast<uint32_t>(sgi * kPfKeys * L::kSeg + p * br * L::kSeg),
+                                    map, 0, kvh * L::kSegs + sgi, rows[p], full);
+                }
+            }
         }
         if (aborted && lane == 0) {
             flag(a.status, KVFP8_DEV_TIMEOUT);
             *abort_flag = 1;
             // let copies already issued land before the CTA's shared memory goes away
-            const volatile int32_t never = 0;
-            for (int k = max(0, issued - 2); k < issued; ++k)
-                mbar_wait(bar_full + 8 * (k & 1), (k >> 1) & 1, &never);
+            for (int k = max(0, issued - L::kNS); k < issued; ++k)
+                mbar_wait(bar(L::kFull, k % L::kNS), (k / L::kNS) & 1, &never);
         }
-    } else {
-        // ------------------------------------------------------------ compute warps
-        const int r = row0 + tid;                   // this thread's score row (TMEM lane tid)
-        const bool row_ok = r < nb * G;
-        const int jq = row_ok ? r / G : 0, gq = row_ok ? r % G : 0;
-        const int pos = Ls - nb + jq;               // last key position the row may see
-        const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        uint32_t wg_phase = 0;
-        bool ok = true;
-        // warp-group barrier with a bounded wait
-        auto wg_sync = [&]() {
-            mbar_arrive(bar_wg);
-            const bool done = mbar_wait(bar_wg, wg_phase, abort_flag);
-            wg_phase ^= 1u;
-            return done;
-        };
-
-        // q row -> f16, 128-byte-swizzled K-major blocks of 64 head dims
-        {
+    } else if (warp == kPfMmaWarp) {
+        // ------------------------------------------------------------ tensor-core issue
+        // S(i) is issued before O(i-1), so the tensor core computes the next scores while the
+        // softmax warps work on the current ones.
+        if (lane == 0) {
+            const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, HD);
+            int o_issued = 0;  // O products issued so far
+            bool ok = true;
+            auto issue_o = [&](int t) {  // O += P(t) . V(t), then release tile t's buffers
+                const int b = t % L::kNB;
+                if (!mbar_wait(bar(L::kPReady, b), (t / L::kNB) & 1, abort_flag)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < kPfKeys / 16; ++k)
+                    umma_ts(tmem + L::kColO, tmem + 64 * b + 8 * k,
+                            sw128_desc(base + L::kV + b * L::kVBuf + k * 32), idesc_o,
+                            (t > 0 || k > 0) ? 1u : 0u);
+                umma_commit(bar(L::kKvFree, b));
+                ++o_issued;
+                return true;
+            };
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int b = i % L::kNB;
+                ok = mbar_wait(bar(L::kKvReady, b), (i / L::kNB) & 1, abort_flag);
+                // S(i) overwrites the buffer that held P(i-NB): O(i-NB) must have read it
+                if (ok && i >= L::kNB)
+                    ok = mbar_wait(bar(L::kKvFree, b), ((i / L::kNB) & 1) ^ 1u, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < HD / 16; ++k) {
+                    const uint64_t ad = sw128_desc(base + L::kQ + (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
+                    const uint64_t bd = sw128_desc(base + L::kK + b * L::kKBuf + (k >> 2) * (kPfKeys * 128) +
+                                                   (k & 3) * 32);
+                    umma_ss(tmem + 64 * b, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                }
+                umma_commit(bar(L::kSReady, b));
+                if (i >= 1) ok = issue_o(i - 1);
+            }
+            if (ok) ok = issue_o(ntiles - 1);
+            if (!ok) {
+                flag(a.status, KVFP8_DEV_TIMEOUT);
+                *abort_flag = 1;
+                // let products already issued finish before tensor memory is released
+                if (o_issued > 0) {
+                    const int t = o_issued - 1;
+                    mbar_wait(bar(L::kKvFree, t % L::kNB), (t / L::kNB) & 1, &never);
+                }
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ conversion warps
+        const int ct = tid - 128;  // 0 .. 32*kPfConvWarps-1
+        constexpr int kCT = 32 * kPfConvWarps;
+        if (ct < kPfRows) {  // q rows -> f16, 128-byte-swizzled K-major blocks of 64 head dims; row ct
+            const int r = row0 + ct;
+            const bool row_ok = r < nb * G;
+            const int jq = row_ok ? r / G : 0, gq = row_ok ? r % G : 0;
             const __nv_bfloat16 *qrow =
                 a.query + ((static_cast<int64_t>(qr.q0) + jq) * a.n_q + kvh * G + gq) * HD;
 #pragma unroll 4
@@ -322,24 +407,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 h.y = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
                 h.z = f16x2_from_f32(bf16lo(w.z), bf16hi(w.z));
                 h.w = f16x2_from_f32(bf16lo(w.w), bf16hi(w.w));
-                *reinterpret_cast<uint4 *>(bp + L::kQ + (c >> 3) * (kPfRows * 128) + sw128(tid, c & 7)) = h;
+                *reinterpret_cast<uint4 *>(bp + L::kQ + (c >> 3) * (kPfRows * 128) + sw128(ct, c & 7)) = h;
             }
         }
-
-        float m_used = -INFINITY, lsum = 0.f;
-        int i = 0;
-        for (; i < ntiles && ok; ++i) {
-            const int stage = i & 1;
-            // the tile's FP8 bytes have landed; the previous tile's products are done (its
-            // K, V^T and P may be overwritten)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8 * stage, (i >> 1) & 1, abort_flag));
-            if (ok && i > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o, (i - 1) & 1, abort_flag));
+        bool ok = true;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int st = i % L::kNS, b = i % L::kNB;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kFull, st), (i / L::kNS) & 1, abort_flag));
+            // the buffer's previous tile (i-NB) has been through both products
+            if (ok)
+                ok = __all_sync(0xFFFFFFFFu,
+                                mbar_wait(bar(L::kKvFree, b), ((i / L::kNB) & 1) ^ 1u, abort_flag));
             if (!ok) break;
-            const uint64_t mask = meta[stage];
-            const uint8_t *kst = bp + L::kStage + stage * L::kStageBytes;
+            const uint64_t mask = meta[st];
+            const uint8_t *kst = bp + L::kStage + st * L::kStageBytes;
             const uint8_t *vst = kst + kPfKeys * HD;
+            uint8_t *kdst0 = bp + L::kK + b * L::kKBuf;
+            uint8_t *vdst = bp + L::kV + b * L::kVBuf;
             // K: 64 keys x HD/16 chunks of 16 fp8 -> f16 (invalid keys: zeros)
-            for (int task = tid; task < kPfKeys * (HD / 16); task += 128) {
+            for (int task = ct; task < kPfKeys * (HD / 16); task += kCT) {
                 const int key = task / (HD / 16), c = task % (HD / 16);  // dims 16c .. 16c+15
                 const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
                 uint4 w = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
@@ -355,72 +441,87 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 h1.z = f16x2_from_e4m3x2(w.w);
                 h1.w = f16x2_from_e4m3x2_hi(w.w);
                 const int kb = (16 * c) / 64, c8 = ((16 * c) % 64) / 8;
-                uint8_t *kdst = bp + L::kK + kb * (kPfKeys * 128);
+                uint8_t *kdst = kdst0 + kb * (kPfKeys * 128);
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
             }
-            // V^T: key pairs x HD/16 chunks; dim n of keys (2kp, 2kp+1) -> row n, K index 2kp
-            for (int task = tid; task < (kPfKeys / 2) * (HD / 16); task += 128) {
-                const int kp = task / (HD / 16), c = task % (HD / 16);
-                const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
-                const uint8_t *vseg = vst + sgi * kPfKeys * L::kSeg;
-                uint4 va = *reinterpret_cast<const uint4 *>(vseg + swz<L::kSeg>(2 * kp, within >> 4));
-                uint4 vb = *reinterpret_cast<const uint4 *>(vseg + swz<L::kSeg>(2 * kp + 1, within >> 4));
-                if (!((mask >> (2 * kp)) & 1ull)) va = make_uint4(0u, 0u, 0u, 0u);
-                if (!((mask >> (2 * kp + 1)) & 1ull)) vb = make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t aw[4] = {va.x, va.y, va.z, va.w}, bw[4] = {vb.x, vb.y, vb.z, vb.w};
+            // V^T by 8-key x 32-dim blocks: lane t converts dims (8j + 2(t%4), +1) of key t/4
+            // (one e4m3 pair -> f16x2 per matrix j) and stmatrix.trans writes each dim's 8 keys
+            // as one 16-byte row of V^T (head dims as rows, keys along K)
+            {
+                const int w4 = warp - 4;
+                const uint32_t vbase = base + L::kV + b * L::kVBuf;
+                for (int blk = w4; blk < (kPfKeys / 8) * (HD / 32); blk += kPfConvWarps) {
+                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
+                    const int key = ko * 8 + (lane >> 2);
+                    const int sgi = (32 * dg) / L::kSeg, cc = ((32 * dg) % L::kSeg) >> 4;
+                    const uint8_t *vrow = vst + sgi * kPfKeys * L::kSeg;
+                    uint4 lo = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc));
+                    uint4 hi = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc + 1));
+                    if (!((mask >> key) & 1ull)) lo = hi = make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    uint32_t r[4];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    // bytes (a_d, b_d) for dims d = 4*q4 .. 4*q4+3 of the chunk
-                    const uint32_t lo = __byte_perm(aw[q4], bw[q4], 0x5140);  // a0 b0 a1 b1
-                    const uint32_t hi = __byte_perm(aw[q4], bw[q4], 0x7362);  // a2 b2 a3 b3
-                    const uint32_t pv[4] = {f16x2_from_e4m3x2(lo), f16x2_from_e4m3x2_hi(lo),
-                                            f16x2_from_e4m3x2(hi), f16x2_from_e4m3x2_hi(hi)};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int n = 16 * c + 4 * q4 + e;   // head dim = row of V^T
-                        *reinterpret_cast<uint32_t *>(bp + L::kV + sw128(n, (2 * kp) >> 3) +
-                                                      ((2 * kp) & 7) * 2) = pv[e];
+                    for (int j = 0; j < 4; ++j) {
+                        // bytes 8j + 2(t%4), +1 of the key's 32: word 2j + (t%4)/2, half t%2
+                        const uint32_t w = (lane & 2) ? wd[2 * j + 1] : wd[2 * j];
+                        r[j] = (lane & 1) ? f16x2_from_e4m3x2_hi(w) : f16x2_from_e4m3x2(w);
                     }
+                    const int n = 32 * dg + 8 * (lane >> 3) + (lane & 7);  // V^T row this lane addresses
+                    stsm_x4_t(vbase + sw128(n, ko), r[0], r[1], r[2], r[3]);
                 }
             }
+            if (ct == 0) buf_mask[b] = mask;  // for the softmax warps, released with kv_ready
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * stage);  // the FP8 stage may be refilled
-            ok = __all_sync(0xFFFFFFFFu, wg_sync());
-            if (!ok) break;
-            if (tid == 0) {  // S = Q . K^T over HD/16 k-steps
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < HD / 16; ++k) {
-                    const uint64_t ad = sw128_desc(base + L::kQ + (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
-                    const uint64_t bd = sw128_desc(base + L::kK + (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
-                    umma_ss(tmem + L::kColS, ad, bd, f16_idesc(kPfRows, kPfKeys), k > 0 ? 1u : 0u);
-                }
-                umma_commit(bar_s);
+            if (lane == 0) {
+                mbar_arrive(bar(L::kEmpty, st));     // the FP8 stage may be refilled
+                mbar_arrive(bar(L::kKvReady, b));    // K(i), V^T(i) (and Q) are ready
             }
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s, i & 1, abort_flag));
+        }
+        if (!ok && lane == 0) {
+            flag(a.status, KVFP8_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        const int r = row0 + tid;                   // this thread's score row (TMEM lane tid)
+        const bool row_ok = r < nb * G;
+        const int jq = row_ok ? r / G : 0, gq = row_ok ? r % G : 0;
+        const int pos = Ls - nb + jq;               // last key position the row may see
+        const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        float m_used = -INFINITY, lsum = 0.f;
+        bool ok = true;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int b = i % L::kNB, ph = (i / L::kNB) & 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kSReady, b), ph, abort_flag));
+            // the tile's valid-key mask (already complete: S(i) needed the same phase)
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvReady, b), ph, abort_flag));
             if (!ok) break;
             tc_fence_after();
+            const uint64_t mask = buf_mask[b];
             uint32_t s[2][32];
-            tmem_ld32(lane_addr + L::kColS, s[0]);
-            tmem_ld32(lane_addr + L::kColS + 32, s[1]);
+            tmem_ld32(lane_addr + 64 * b, s[0]);
+            tmem_ld32(lane_addr + 64 * b + 32, s[1]);
             tmem_wait_ld();
-            // causal mask, scale, running maximum
+            // causal mask, scale, running maximum (a key past the row's position, past the
+            // sequence or in a bad block scores -inf; keys past kend are past every position)
             const int k0 = i * kPfKeys;
+            const int vis_n = row_ok ? min(kPfKeys, max(0, pos - k0 + 1)) : 0;  // keys 0..vis_n-1
+            const uint64_t vis = mask & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
             float mx = -INFINITY;
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
-                    const int key = 32 * h + c;
-                    const bool vis = row_ok && k0 + key <= pos && ((mask >> key) & 1ull);
-                    const float v = vis ? __uint_as_float(s[h][c]) * score_scale : -INFINITY;
+                    const float v = ((vis >> (32 * h + c)) & 1ull) ? __uint_as_float(s[h][c]) * score_scale
+                                                                   : -INFINITY;
                     s[h][c] = __float_as_uint(v);
                     mx = fmaxf(mx, v);
                 }
-            // rescale O only when the maximum grew by more than 2^8 (first visible keys: O
-            // is still zero for this row, nothing to rescale)
+            // rescale O only when the maximum grew by more than 2^8 (first visible keys: O is
+            // still zero for this row, nothing to rescale)
             float factor = 1.f;
             if (mx > -INFINITY) {
                 if (m_used == -INFINITY) {
@@ -431,6 +532,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 }
             }
             if (__any_sync(0xFFFFFFFFu, factor != 1.f)) {
+                // O(i-1) must be complete before O is rescaled
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvFree, (i - 1) % L::kNB),
+                                                       ((i - 1) / L::kNB) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
                 lsum *= factor;
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD; c0 += 32) {
@@ -442,7 +548,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     tmem_st32(lane_addr + L::kColO + c0, o);
                 }
             }
-            // P = 2^(s - m), f16 pairs over the first 32 columns of S
+            // P = 2^(s - m), f16 pairs over the first 32 columns of this S buffer
             uint32_t p[32];
             const float msub = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll
@@ -453,23 +559,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 lsum += p0 + p1;
                 p[c] = f16x2_from_f32(p0, p1);
             }
-            tmem_st32(lane_addr + L::kColS, p);
+            tmem_st32(lane_addr + 64 * b, p);
             tmem_wait_st();
             tc_fence_before();
-            ok = __all_sync(0xFFFFFFFFu, wg_sync());
-            if (!ok) break;
-            if (tid == 0) {  // O += P . V over 64/16 k-steps; A from TMEM, B = V^T
-                tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < kPfKeys / 16; ++k) {
-                    const uint64_t bd = sw128_desc(base + L::kV + k * 32);
-                    umma_ts(tmem + L::kColO, tmem + L::kColS + 8 * k, bd, f16_idesc(kPfRows, HD),
-                            (i > 0 || k > 0) ? 1u : 0u);
-                }
-                umma_commit(bar_o);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kPReady, b));
         }
-        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o, (ntiles - 1) & 1, abort_flag));
+        if (ok)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvFree, (ntiles - 1) % L::kNB),
+                                                   ((ntiles - 1) / L::kNB) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
             const float inv = lsum > 0.f ? sv / lsum : 0.f;
@@ -495,15 +593,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         } else if (lane == 0) {
             flag(a.status, KVFP8_DEV_TIMEOUT);
             *abort_flag = 1;
-            // let products already issued finish before tensor memory is released
-            const volatile int32_t never = 0;
-            if (i > 0) mbar_wait(bar_o, (i - 1) & 1, &never);
-            mbar_wait(bar_s, i & 1, &never);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kPfMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
@@ -513,7 +607,7 @@ template <int HD>
 cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     using L = PfSmem<HD>;
     const int row_bytes = d.n_kv * HD;
-    const int box_rows = d.block_size >= kChunkTokens ? kChunkTokens : d.block_size;
+    const int box_rows = d.block_size >= kPfKeys ? kPfKeys : d.block_size;  // whole tile when one block holds it
     const int64_t rows = static_cast<int64_t>(d.num_blocks) * d.block_size;
     CUtensorMap tmk, tmv;
     cudaError_t err;
@@ -550,7 +644,7 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     a.box_rows = box_rows;
     const int tiles = (d.qmax * a.group + kPfRows - 1) / kPfRows;
     dim3 grid(d.num_seqs, tiles, d.n_kv);
-    kern<<<grid, kPfThreads, smem, stream>>>(tmk, tmv, a);
+    kern<<<grid, kPfWarps * 32, smem, stream>>>(tmk, tmv, a);
     return cudaGetLastError();
 }
 

@@ -133,7 +133,7 @@ def test_serving_step_rows_are_the_last_query_tokens():
 
 
 def test_reference_arm_runs_each_variant():
-    for variant in ("rope", "k_bf16", "multi"):
+    for variant in ("rope", "k_bf16", "multi", "prefill"):
         r = _bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
                    "--variant", variant)
         assert r.returncode == 0, r.stderr
@@ -150,3 +150,18 @@ def test_cpu_baselines_report_their_threads():
     assert one["cores"] == 1 and one["kind"] == "oracle" and one["value"] > 0
     assert allc["cores"] == bench.host_cores() >= 1 and allc["value"] > 0
     assert "threads" in allc["sample"]
+
+
+def test_prefill_flops_count_the_causal_pairs():
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import workloads
+
+    w = workloads.WORKLOADS["llama3_8b"]
+    lens = np.array([5, 8], np.int64)
+    # 3 new tokens: sequence 0 sees 3, 4, 5 keys; sequence 1 sees 6, 7, 8
+    assert bench.attention_flops(w, lens, 3) == 4 * 128 * 32 * (3 + 4 + 5 + 6 + 7 + 8)
+    assert bench.query_len(w, "prefill", np.array([4096, 4096])) == 512
+    assert bench.query_len(w, "prefill", np.array([4096, 17])) == 17

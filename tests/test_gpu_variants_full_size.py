@@ -5,6 +5,8 @@ sequences against the oracle's matching functions:
   rope     rope on K fused into the cache write, then decode
   k_bf16   mixed cache dtypes, K bf16 / V E4M3;  v_bf16 the other way round
   multi    causal multi-query attention, 16 // G query tokens per sequence
+  prefill  chunked prefill: the last 512 tokens of each sequence (16 on the serving mix)
+           written, then causal attention for them on the tensor-core kernel
 
 For each sampled sequence the oracle writes that sequence's rows (as one step leaves them
 in the cache) into a cache of its own and attends with every head.
@@ -33,7 +35,7 @@ def _seq_rows(p, b, ctx):
     if w.kind == "write":
         rows = rows[lay.row_pos[rows] >= 0]
     idx = torch.from_numpy(rows).cuda()
-    if w.kind != "mixed":
+    if not p.serving:
         return p.k.index_select(0, idx).cpu(), p.v.index_select(0, idx).cpu()
     k = ctx[0].index_select(0, idx).clone()
     v = ctx[1].index_select(0, idx).clone()
@@ -67,7 +69,7 @@ def _oracle_seq(p, b, k, v, ks, vs):
         return (kc, vc), None
     bt = np.arange(nb, dtype=np.int32)[None, :]
     lens = np.array([L], np.int32)
-    if p.variant == "multi":
+    if p.variant in ("multi", "prefill"):
         n = p.qlen
         q = p.q[b * n:(b + 1) * n].cpu()
         out, st = oracle.paged_attention_multi(q, np.array([0, n], np.int32), kc, vc, bt, lens,
@@ -97,6 +99,7 @@ def _gpu_seq_cache(p, b, L):
 CASES = [
     ("llama3_8b", "rope", 5), ("llama3_8b", "k_bf16", 5), ("llama3_8b", "v_bf16", 5),
     ("llama3_8b", "multi", 5), ("mixed_serving", "multi", 8), ("mixed_serving", "v_bf16", 8),
+    ("llama3_8b", "prefill", 2), ("mixed_serving", "prefill", 4),
     ("prefill_write", "rope", 4), ("prefill_write", "k_bf16", 4),
 ]
 
@@ -111,7 +114,7 @@ def test_bench_variant_full_size_sampled(case):
     torch.cuda.synchronize()
     assert int(p.status.item()) == 0
     w, lay = p.w, p.lay
-    ctx = workloads.make_kv(w, lay.slot_mapping.size, "cuda") if w.kind == "mixed" else None
+    ctx = workloads.make_kv(w, lay.slot_mapping.size, "cuda") if p.serving else None
     rng = np.random.Generator(np.random.PCG64(w.seed + 91))
     seqs = list(rng.choice(lay.num_seqs, size=min(n_seq, lay.num_seqs), replace=False))
     seqs[0] = int(np.argmax(lay.seq_lens))
@@ -125,7 +128,7 @@ def test_bench_variant_full_size_sampled(case):
         assert np.array_equal(gk, kc.reshape(-1, w.n_kv, w.head_dim)[:L]), (name, variant, b, "K")
         assert np.array_equal(gv, vc.reshape(-1, w.n_kv, w.head_dim)[:L]), (name, variant, b, "V")
         if ref is not None:
-            got = p.out[b * p.qlen:(b + 1) * p.qlen] if variant == "multi" else p.out[b:b + 1]
+            got = p.out[b * p.qlen:(b + 1) * p.qlen] if p.qsl is not None else p.out[b:b + 1]
             gpu_util.assert_attention_close(got, ref, "%s %s seq %d" % (name, variant, b))
     if p.decode:
         assert torch.isfinite(p.out.float()).all()
