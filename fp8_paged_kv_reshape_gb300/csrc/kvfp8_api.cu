@@ -151,7 +151,6 @@ kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const ui
         return KVFP8_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
     if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
-    if (n_kv > 8 || static_cast<int64_t>(n_kv) * head_dim > 2048) return KVFP8_ERR_UNSUPPORTED;
     if (head_dim == 256 && n_q / n_kv > 8) return KVFP8_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
@@ -333,7 +332,7 @@ kvfp8_status kvfp8_paged_decode_attention_mixed(
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
         return KVFP8_ERR_SHAPE;
-    if (k_cache_dtype == v_cache_dtype || head_dim == 256 || n_kv > 8) return KVFP8_ERR_UNSUPPORTED;
+    if (k_cache_dtype == v_cache_dtype || head_dim == 256) return KVFP8_ERR_UNSUPPORTED;
     if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
     if (num_seqs == 0) return KVFP8_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !workspace)

@@ -19,8 +19,8 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t n_q, int32_t h
 
 bool multi_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t max_query_len) {
     const int64_t cols = static_cast<int64_t>(max_query_len) * (n_q / n_kv);
-    return cols <= 16 && !(head_dim == 256 && cols > 8) && n_kv <= kMaxKvHeads &&
-           static_cast<int64_t>(n_kv) * head_dim <= 2048;
+    (void)n_kv;
+    return cols <= 16 && !(head_dim == 256 && cols > 8);
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &d, cudaStream_t stream) {
@@ -30,7 +30,6 @@ cudaError_t launch_paged_decode(const DecodeArgs &d, cudaStream_t stream) {
         return launch_prefill_attention(d, stream);
     const DecodeWorkspace ws = decode_workspace_layout(d.num_seqs, d.qmax * d.n_q, d.head_dim);
     const int group = d.n_q / d.n_kv;
-    if (d.n_kv > kMaxKvHeads) return cudaErrorNotSupported;
     const int cols = d.qmax * group;  // score columns per kv head
     if (cols > 16) return cudaErrorNotSupported;
     const int nt = cols <= 8 ? 1 : 2;

@@ -18,8 +18,10 @@
 //    sequences first, and one record per CTA (its chunk range and first sequence, so a
 //    CTA starts with one load).  Plan -> decode -> combine are chained as programmatic
 //    dependent launches, so each grid's launch and prologue overlap its predecessor.
-//  * One CTA = one producer warp + one consumer warp per kv head.  A 16-token chunk of a
-//    block holds all kv heads of those tokens (16 contiguous rows of n_kv*head_dim bytes),
+//  * One CTA = one producer warp + one consumer warp per kv head of its head group (the
+//    kv heads split into equal groups of at most 8, a second grid dimension; one group
+//    when n_kv <= 8).  A 16-token chunk of a block holds all kv heads of those tokens (16
+//    contiguous rows of n_kv*head_dim bytes), and a CTA fetches its group's part of them,
 //    so the producer issues TMA tensor loads of [16 rows x 128 B] boxes (one per head and
 //    128-byte segment of head_dim) with 128-byte swizzle into a multi-stage ring, on an
 //    mbarrier per stage; the block-table entries come in 32 at a time, one per lane.
@@ -87,6 +89,7 @@ struct KernelArgs {
     const int32_t *seq_lens;
     int32_t num_seqs;
     int32_t n_q, n_kv, group, block_size, num_blocks;
+    int32_t hpc;  // kv heads per CTA (head group size); blockIdx.y is the head group
     int32_t max_len;  // max_blocks_per_seq * block_size
     float sm_scale;
     const void *k_scale;
@@ -456,7 +459,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     uint8_t *base_ptr = smem_raw + (base - raw);
 
     const int S = a.stages;
-    const int RK = a.n_kv * HD * KB, RV = a.n_kv * HD * VB;  // cache row bytes
+    const int hpc = a.hpc, h0 = static_cast<int>(blockIdx.y) * hpc;  // this CTA's kv heads
+    const int RK = hpc * HD * KB, RV = hpc * HD * VB;  // bytes of a cache row this CTA holds
     const uint32_t kchunk_bytes = static_cast<uint32_t>(kChunkTokens * RK);
     const uint32_t stage_bytes = kchunk_bytes + static_cast<uint32_t>(kChunkTokens * RV);
     const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;  // full[S], empty[S]
@@ -467,12 +471,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(bars + 8 * i, 1);
-            mbar_init(bars + 8 * (S + i), a.n_kv);
+            mbar_init(bars + 8 * (S + i), hpc);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == a.n_kv && lane == 0) {
+    if (warp == hpc && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
@@ -493,7 +497,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     const int64_t chunk_lo = pl.lo, chunk_hi = pl.hi;
     __syncthreads();
 
-    if (warp == a.n_kv) {
+    if (warp == hpc) {
         // ------------------------------------------------------------ producer warp
         int64_t issued = 0;
         int stage = 0;
@@ -555,20 +559,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                             mbar_arrive_tx(full, nloads * rows_bytes);
                             const uint32_t kst = base + static_cast<uint32_t>(stage) * stage_bytes;
                             const uint32_t vst = kst + kchunk_bytes;
-                            if (a.whole_box) {  // one box: every head segment, 16 rows
-                                tma_load_3d(kst, &tmk, 0, rows0[0], 0, full);
-                                tma_load_3d(vst, &tmv, 0, rows0[0], 0, full);
+                            if (a.whole_box) {  // one box: the group's head segments, 16 rows
+                                tma_load_3d(kst, &tmk, 0, rows0[0], h0 * SEGSK, full);
+                                tma_load_3d(vst, &tmv, 0, rows0[0], h0 * SEGSV, full);
                             } else {
                                 for (int p = 0; p < nloads; ++p) {
-                                    for (int g = 0; g < a.n_kv * SEGSK; ++g) {
+                                    for (int g = 0; g < hpc * SEGSK; ++g) {
                                         const uint32_t off = static_cast<uint32_t>(
                                             g * kChunkTokens * SEGK + p * a.box_rows * SEGK);
-                                        tma_load_3d(kst + off, &tmk, 0, g, rows0[p], full);
+                                        tma_load_3d(kst + off, &tmk, 0, h0 * SEGSK + g, rows0[p], full);
                                     }
-                                    for (int g = 0; g < a.n_kv * SEGSV; ++g) {
+                                    for (int g = 0; g < hpc * SEGSV; ++g) {
                                         const uint32_t off = static_cast<uint32_t>(
                                             g * kChunkTokens * SEGV + p * a.box_rows * SEGV);
-                                        tma_load_3d(vst + off, &tmv, 0, g, rows0[p], full);
+                                        tma_load_3d(vst + off, &tmv, 0, h0 * SEGSV + g, rows0[p], full);
                                     }
                                 }
                             }
@@ -608,9 +612,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                           &never);
             }
         }
-    } else if (warp < a.n_kv) {
+    } else if (warp < hpc) {
         // ------------------------------------------------------------ consumer warp
-        const int kvh = warp;
+        const int kvh = h0 + warp;  // its kv head; warp is the head's place in the group
         const int gid = lane >> 2, tig = lane & 3;
         const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
 
@@ -709,8 +713,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
             const int nvalid = mt.nvalid;
             if (nvalid > 0) {
                 const uint32_t sbase = base + static_cast<uint32_t>(stage) * stage_bytes;
-                const uint32_t kbase = sbase + kvh * (kChunkTokens * HD * KB);
-                const uint32_t vbase = sbase + kchunk_bytes + kvh * (kChunkTokens * HD * VB);
+                const uint32_t kbase = sbase + warp * (kChunkTokens * HD * KB);
+                const uint32_t vbase = sbase + kchunk_bytes + warp * (kChunkTokens * HD * VB);
 
                 // ---- scores S^T[token][head] = K . q^T
                 float sacc[NT][4];
@@ -979,21 +983,22 @@ cudaError_t encode_cache_map(CUtensorMap *map, const uint8_t *cache, int64_t row
 }
 
 // The same bytes as a 3-D tensor ordered (SEG bytes, rows, segments) -- the segment
-// stride (SEG) below the row stride -- so that one [SEG x 16 rows x all segments] box
-// fetches a whole 16-token chunk into the same [segment][row][SEG] swizzled layout that
-// the per-segment boxes produce, with one TMA instruction instead of n_kv*head_dim/SEG.
+// stride (SEG) below the row stride -- so that one [SEG x 16 rows x box_segs] box fetches
+// a head group's part of a 16-token chunk into the same [segment][row][SEG] swizzled
+// layout that the per-segment boxes produce, with one TMA instruction instead of one per
+// segment.
 cudaError_t encode_cache_map_whole(CUtensorMap *map, const uint8_t *cache, int64_t rows,
-                                   int row_bytes, int seg) {
+                                   int row_bytes, int seg, int box_segs) {
     auto enc = tensor_map_encoder();
     if (enc == nullptr) return cudaErrorNotSupported;
     const int segs = row_bytes / seg;
-    if (segs > 256) return cudaErrorNotSupported;
+    if (segs > (1 << 20) || box_segs > 256) return cudaErrorNotSupported;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(seg), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(segs)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
                                    static_cast<cuuint64_t>(seg)};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(seg), static_cast<cuuint32_t>(kChunkTokens),
-                               static_cast<cuuint32_t>(segs)};
+                               static_cast<cuuint32_t>(box_segs)};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(cache),
                            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1022,7 +1027,11 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     constexpr int KB = KT16 ? 2 : 1, VB = VT16 ? 2 : 1;
     constexpr int SEGK = HD * KB >= 128 ? 128 : 64, SEGV = HD * VB >= 128 ? 128 : 64;
     const int kbytes = d.n_kv * HD * KB, vbytes = d.n_kv * HD * VB;  // cache row bytes
-    const int stage_bytes = kChunkTokens * (kbytes + vbytes);
+    // kv heads per CTA: the largest divisor of n_kv up to 8; the groups are a grid dimension
+    int hpc = std::min(d.n_kv, kMaxKvHeads);
+    while (d.n_kv % hpc != 0) --hpc;
+    const int groups = d.n_kv / hpc;
+    const int stage_bytes = kChunkTokens * hpc * HD * (KB + VB);
     const int ctas_per_sm = std::max(
         1, std::min(min_ctas_per_sm<HD, NT, VT16>(), env_int("KVFP8_DECODE_CTAS_PER_SM", 2)));
     const int max_stages = std::max(2, std::min(8, env_int("KVFP8_DECODE_MAX_STAGES", 8)));
@@ -1040,13 +1049,14 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem))) != cudaSuccess)
         return err;
-    const int threads = 32 * (d.n_kv + 1);
+    const int threads = 32 * (hpc + 1);
     int occ = 0;
     if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem)) !=
         cudaSuccess)
         return err;
     occ = std::max(1, std::min(occ, ctas_per_sm));
-    const int num_ctas = std::min(sms * occ, kMaxDecodeCtas);
+    // about one resident wave over all head groups
+    const int num_ctas = std::max(1, std::min(sms * occ / groups, kMaxDecodeCtas));
 
     CUtensorMap tmk, tmv;
     const int box_rows = d.block_size >= kChunkTokens ? kChunkTokens : d.block_size;
@@ -1054,8 +1064,10 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     // whole-chunk boxes when a chunk never straddles blocks (and the driver accepts the
     // map); otherwise one box per head segment
     bool whole = box_rows == kChunkTokens && env_int("KVFP8_DECODE_SEGMENT_BOXES", 0) == 0 &&
-                 encode_cache_map_whole(&tmk, d.key_cache, rows, kbytes, SEGK) == cudaSuccess &&
-                 encode_cache_map_whole(&tmv, d.value_cache, rows, vbytes, SEGV) == cudaSuccess;
+                 encode_cache_map_whole(&tmk, d.key_cache, rows, kbytes, SEGK, hpc * HD * KB / SEGK) ==
+                     cudaSuccess &&
+                 encode_cache_map_whole(&tmv, d.value_cache, rows, vbytes, SEGV, hpc * HD * VB / SEGV) ==
+                     cudaSuccess;
     if (!whole) {
         if ((err = encode_cache_map(&tmk, d.key_cache, rows, kbytes, SEGK, box_rows)) != cudaSuccess)
             return err;
@@ -1075,6 +1087,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.n_q = d.n_q;
     k.n_kv = d.n_kv;
     k.group = d.n_q / d.n_kv;
+    k.hpc = hpc;
     k.block_size = d.block_size;
     k.num_blocks = d.num_blocks;
     k.max_len = d.max_blocks_per_seq * d.block_size;
@@ -1106,7 +1119,7 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     // Programmatic dependent launch: the decode grid starts its prologue while the plan
     // grid runs and waits (griddepcontrol.wait) before touching any data.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_ctas);
+    cfg.gridDim = dim3(num_ctas, groups);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

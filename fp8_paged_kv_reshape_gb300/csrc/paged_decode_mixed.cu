@@ -9,7 +9,7 @@ namespace kvfp8 {
 
 cudaError_t launch_paged_decode_mixed(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
-    if (d.qsl != nullptr || d.k_bf16 == d.v_bf16 || d.n_kv > kMaxKvHeads)
+    if (d.qsl != nullptr || d.k_bf16 == d.v_bf16)
         return cudaErrorNotSupported;
     const int group = d.n_q / d.n_kv;
     if (group > 16) return cudaErrorNotSupported;

@@ -182,9 +182,10 @@ KVFP8_API size_t kvfp8_paged_decode_workspace_size(int32_t num_seqs, int32_t n_q
  * block_tables      device int32 [num_seqs][max_blocks_per_seq]
  * seq_lens          device int32 [num_seqs]
  * num_seqs >= 0; n_q % n_kv == 0 with n_q / n_kv <= 16; head_dim in {64, 128, 256};
- * block_size in {8, 16, 32, 64, 128, 256}; num_blocks*block_size < 2^31.  This build
- * has kernels for n_kv <= 8 with n_kv*head_dim <= 2048, and n_q/n_kv <= 8 at
- * head_dim 256; other valid shapes return KVFP8_ERR_UNSUPPORTED.
+ * block_size in {8, 16, 32, 64, 128, 256}; num_blocks*block_size < 2^31.  Any n_kv: a
+ * CTA serves a group of at most 8 kv heads (the largest divisor of n_kv up to 8), the
+ * groups side by side.  This build needs n_q/n_kv <= 8 at head_dim 256; other valid
+ * shapes return KVFP8_ERR_UNSUPPORTED.
  * sm_scale          <= 0 selects 1/sqrt(head_dim)
  * k_scale, v_scale  device scalars of scale_dtype, or NULL for 1
  * workspace         device, >= kvfp8_paged_decode_workspace_size(...) bytes, contents
@@ -247,8 +248,8 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
  * n_b = 1 for every sequence is kvfp8_paged_decode_attention.
  *
  * Two kernels serve the call.  With max_query_len * (n_q / n_kv) <= 16 score columns per
- * kv head (<= 8 at head_dim 256), n_kv <= 8 and n_kv*head_dim <= 2048, the split-KV decode
- * kernel runs and needs the workspace below.  Every other shape (long query chunks,
+ * kv head (<= 8 at head_dim 256) the split-KV decode kernel runs and needs the workspace
+ * below.  Every other shape (long query chunks,
  * prefill) runs on the tensor cores (tcgen05, accumulators in tensor memory), one CTA per
  * 128 (query token, head) rows of a kv head, with no workspace; it needs
  * n_q / n_kv <= 128.
@@ -313,7 +314,7 @@ KVFP8_API kvfp8_status kvfp8_reshape_and_cache_mixed(
  * A bf16 K enters the tensor cores against bf16 q (exact products); a bf16 V against the
  * probabilities split into two bf16 parts (16 significant bits).
  * This build: exactly one side bf16 (both E4M3 is kvfp8_paged_decode_attention; both
- * bf16 returns KVFP8_ERR_UNSUPPORTED), head_dim 64 or 128, n_q/n_kv <= 16, n_kv <= 8.
+ * bf16 returns KVFP8_ERR_UNSUPPORTED), head_dim 64 or 128, n_q/n_kv <= 16.
  * Workspace: kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim).  Everything else
  * as kvfp8_paged_decode_attention.
  */

@@ -115,7 +115,6 @@ def test_decode_host_validation():
     assert _decode(n_q=8 * 17) == binding.ERR_SHAPE                  # group above 16
     assert _decode(head_dim=96) == binding.ERR_SHAPE
     assert _decode(block_size=12) == binding.ERR_SHAPE
-    assert _decode(n_kv=16, n_q=32) == binding.ERR_UNSUPPORTED
     assert _decode(head_dim=256, n_q=8 * 16) == binding.ERR_UNSUPPORTED
     assert _decode(sm_scale=float("nan")) == binding.ERR_SCALE
     assert _decode(out=ctypes.c_void_p(8)) == binding.ERR_ALIGN
@@ -185,7 +184,8 @@ def test_multi_query_workspace_follows_the_kernel_that_serves_the_shape():
     # tensor-core kernel: no workspace
     assert ws(4, 32, 8, 128, 5) == 0          # 20 columns
     assert ws(4, 4, 2, 256, 5) == 0           # 10 columns at head_dim 256
-    assert ws(4, 16, 16, 128, 1) == 0         # 16 kv heads
+    assert ws(4, 16, 16, 128, 1) == dec(4, 16, 128) > 0   # 16 kv heads: two head groups
+    assert ws(4, 16, 16, 128, 17) == 0                    # 17 columns
     assert ws(-1, 32, 8, 128, 4) == 0
 
 

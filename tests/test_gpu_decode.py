@@ -73,6 +73,11 @@ CASES = [
     ("mha_g1", 8, 8, 128, 16, [40, 129]),
     ("bs128", 32, 8, 128, 128, [300, 1000, 129]),
     ("bs256_g6", 24, 4, 128, 256, [700, 5]),
+    # more than 8 kv heads: head groups of 8 (32 = 4 x 8), 6 (12 = 2 x 6), 5 (10 = 2 x 5)
+    ("mha_32_kv_heads", 32, 32, 128, 16, [300, 1000, 17]),
+    ("g2_12_kv_heads_bs8", 24, 12, 64, 8, [129, 40]),
+    ("g4_10_kv_heads_hd256", 40, 10, 256, 32, [200, 65]),
+    ("g1_16_kv_heads_hd64", 16, 16, 64, 16, [5000, 1]),
 ]
 
 

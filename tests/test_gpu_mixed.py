@@ -172,6 +172,7 @@ DECODE_CASES = [
     ("g16_nt2", 32, 2, 128, 16, [50, 500]),
     ("g12_hd64_nt2", 24, 2, 64, 16, [77, 1234]),
     ("bs256_g6", 24, 4, 128, 256, [700, 5]),
+    ("mha16_head_groups", 16, 16, 128, 16, [400, 17]),
 ]
 
 

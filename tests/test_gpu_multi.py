@@ -55,6 +55,8 @@ CASES = [
     ("g2_hd256_q4", 4, 2, 256, 64, [129, 300], [4, 4]),
     ("g1_q16", 8, 8, 128, 8, [100, 16], [16, 16]),
     ("zero_queries", 32, 8, 128, 16, [50, 80, 0], [0, 3, 0]),
+    ("mha16_head_groups_q1", 16, 16, 128, 16, [300, 33], [1, 1]),
+    ("g2_12_kv_heads_q8", 24, 12, 64, 16, [200, 100], [8, 5]),
 ]
 
 

@@ -1,6 +1,6 @@
 """kvfp8_paged_attention_multi on its tensor-core (tcgen05) kernel: query chunks longer than
-the split-KV decode kernel's 16 score columns per kv head, and kv-head counts it does not
-take, vs the double-precision oracle.
+the split-KV decode kernel's 16 score columns per kv head (8 at head_dim 256), vs the
+double-precision oracle.
 Tolerance per element: |gpu - oracle| <= 2e-3 + 1e-2 * |oracle|."""
 import math
 
@@ -70,7 +70,7 @@ CASES = [
     ("g4_many_tiles", 32, 8, 128, 16, [2000, 150], [100, 150]),
     ("g8_q9", 64, 8, 128, 16, [333, 9, 70], [9, 9, 3]),
     ("g5_rows_straddle_tiles", 40, 8, 128, 32, [700, 100], [60, 100]),
-    ("mha_16_kv_heads", 16, 16, 128, 16, [300, 40], [3, 40]),
+    ("mha_16_kv_heads", 16, 16, 128, 16, [300, 40], [20, 40]),
     ("hd64_g2", 8, 4, 64, 16, [500, 77], [40, 77]),
     ("hd256_g2", 4, 2, 256, 64, [300, 129], [10, 129]),
     ("bs8", 16, 4, 128, 8, [250, 31], [31, 31]),
