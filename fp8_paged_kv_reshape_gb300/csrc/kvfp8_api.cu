@@ -146,12 +146,12 @@ kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const ui
                                           size_t workspace_bytes, uint32_t *status,
                                           kvfp8_stream_t stream) {
     if (!dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
-    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || n_q / n_kv > 16 ||
-        num_blocks < 1 || max_blocks_per_seq < 1)
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || num_blocks < 1 ||
+        max_blocks_per_seq < 1)
         return KVFP8_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
     if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
-    if (head_dim == 256 && n_q / n_kv > 8) return KVFP8_ERR_UNSUPPORTED;
+    if (n_q / n_kv > 128) return KVFP8_ERR_UNSUPPORTED;  // past the tensor-core kernel's rows
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
         return KVFP8_ERR_SHAPE;

@@ -26,7 +26,9 @@ bool multi_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32
 cudaError_t launch_paged_decode(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
     if (d.k_bf16 || d.v_bf16) return launch_paged_decode_mixed(d, stream);
-    if (d.qsl != nullptr && !multi_uses_decode_kernel(d.n_q, d.n_kv, d.head_dim, d.qmax))
+    // score columns past the split-KV kernel's 16 per kv head (8 at head_dim 256): long query
+    // chunks, or single-query groups of more heads, run on the tensor-core kernel
+    if (!multi_uses_decode_kernel(d.n_q, d.n_kv, d.head_dim, d.qmax))
         return launch_prefill_attention(d, stream);
     const DecodeWorkspace ws = decode_workspace_layout(d.num_seqs, d.qmax * d.n_q, d.head_dim);
     const int group = d.n_q / d.n_kv;

@@ -207,13 +207,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         if (seq == 0 && tile == 0 && kvh == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
         return;
     }
-    // this sequence's query rows and cached length (flagged once, by its first CTA)
-    const int raw_nq = a.qsl[seq + 1] - a.qsl[seq];
-    const QueryRange qr = query_range(a.qsl, seq, a.qmax, a.qrows);
+    // this sequence's query rows (qsl == nullptr: one query per sequence, row seq) and cached
+    // length (flagged once, by its first CTA)
+    const int raw_nq = a.qsl ? a.qsl[seq + 1] - a.qsl[seq] : 1;
+    const QueryRange qr = a.qsl ? query_range(a.qsl, seq, a.qmax, a.qrows) : QueryRange{seq, 1};
     const int Lraw = a.seq_lens[seq];
     const int Ls = min(max(Lraw, 0), a.max_len);
+    // (more new tokens than cached ones is an error of the multi-query form only: a decode
+    // query on an empty sequence gives a zero row)
     if (tile == 0 && kvh == 0 && tid == 0 &&
-        (qr.count != raw_nq || Lraw < 0 || Lraw > a.max_len || qr.count > Ls))
+        (qr.count != raw_nq || Lraw < 0 || Lraw > a.max_len || (a.qsl && qr.count > Ls)))
         flag(a.status, KVFP8_DEV_BAD_BLOCK);
     const int nb = qr.count, G = a.group;
     const int row0 = tile * kPfRows;                 // first score row of this tile
@@ -652,7 +655,7 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
 
 cudaError_t launch_prefill_attention(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
-    if (d.qsl == nullptr || d.k_bf16 || d.v_bf16) return cudaErrorNotSupported;
+    if (d.k_bf16 || d.v_bf16) return cudaErrorNotSupported;
     if (d.n_q / d.n_kv > kPfRows) return cudaErrorNotSupported;
     if ((d.qmax * (d.n_q / d.n_kv) + kPfRows - 1) / kPfRows > 65535) return cudaErrorNotSupported;
     switch (d.head_dim) {

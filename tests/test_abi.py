@@ -112,10 +112,9 @@ def test_decode_host_validation():
     assert _decode(query=None) == binding.ERR_NULL
     assert _decode(workspace=None) == binding.ERR_NULL
     assert _decode(n_q=30) == binding.ERR_SHAPE                      # not a multiple of n_kv
-    assert _decode(n_q=8 * 17) == binding.ERR_SHAPE                  # group above 16
+    assert _decode(n_q=8 * 129) == binding.ERR_UNSUPPORTED           # group above 128
     assert _decode(head_dim=96) == binding.ERR_SHAPE
     assert _decode(block_size=12) == binding.ERR_SHAPE
-    assert _decode(head_dim=256, n_q=8 * 16) == binding.ERR_UNSUPPORTED
     assert _decode(sm_scale=float("nan")) == binding.ERR_SCALE
     assert _decode(out=ctypes.c_void_p(8)) == binding.ERR_ALIGN
     assert _decode(workspace_bytes=100) == binding.ERR_WORKSPACE

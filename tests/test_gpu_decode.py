@@ -78,6 +78,10 @@ CASES = [
     ("g2_12_kv_heads_bs8", 24, 12, 64, 8, [129, 40]),
     ("g4_10_kv_heads_hd256", 40, 10, 256, 32, [200, 65]),
     ("g1_16_kv_heads_hd64", 16, 16, 64, 16, [5000, 1]),
+    # groups past the split-KV kernel's 16 columns (8 at head_dim 256): tensor-core kernel
+    ("g32_tensor_route", 64, 2, 128, 16, [700, 33, 0]),
+    ("g12_hd256_tensor_route", 24, 2, 256, 64, [300, 5]),
+    ("g128_tensor_route", 128, 1, 64, 16, [90, 17]),
 ]
 
 
