@@ -56,6 +56,10 @@ KERNEL_SOURCES = {
                                "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
 }
 VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi", "prefill")
+# a CPU sample of the multi-query forms attends with at most this many oracle FLOPs: the
+# last m of a sequence's new tokens (a 512-token chunk over a 128K context would otherwise
+# take the double-precision oracle most of an hour)
+SAMPLE_QUERY_FLOPS = 1 << 28
 METRIC = "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak"
 
 
@@ -541,11 +545,19 @@ def run_e2e(args, p: Problem, device):
 
 # ----------------------------------------------------------------- CPU oracle legs
 
+def sampled_queries(w: workloads.Workload, qlen: int, seq_len: int) -> int:
+    """How many of a sequence's qlen new tokens (its last ones) a CPU sample attends with."""
+    per_token = 4 * w.head_dim * w.n_q * max(1, seq_len)
+    return int(min(qlen, max(1, SAMPLE_QUERY_FLOPS // per_token)))
+
+
 def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_all, q,
                    variant: str = "fp8"):
     """Run the CPU oracle on the given sequences of the workload in the given variant: write
-    their rows into a cache, then attend with every head of them.  Returns (seconds,
-    algorithmic bytes)."""
+    their rows into a cache, then attend with every head of them.  The multi-query forms
+    attend with the last m of each sequence's qlen new tokens (sampled_queries; token j of
+    those m sees the same keys as in the full chunk) and are credited m/qlen of the
+    sequences' attention bytes.  Returns (seconds, algorithmic bytes)."""
     import oracle
 
     ks = workloads.stored_scale(w.k_scale, w.scale_dtype)
@@ -574,6 +586,7 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     decode = w.kind != "write"
     sub_lens = lay.seq_lens[seqs]
     qlen = query_len(w, variant, lay.seq_lens)
+    m = sampled_queries(w, qlen, int(sub_lens.max())) if variant in ("multi", "prefill") else qlen
     seq_idx = np.asarray(seqs)
     table = workloads.rope_table(max(1, int(lay.seq_lens.max())), w.head_dim) \
         if variant == "rope" else None
@@ -588,8 +601,8 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
         oracle.reshape_and_cache(kh, vh, kc, vc, slots, w.block_size, ks, vs)
     if decode:
         if variant in ("multi", "prefill"):
-            qrows = (seq_idx[:, None] * qlen + np.arange(qlen)[None, :]).reshape(-1)
-            qsl = np.arange(0, qrows.size + 1, qlen, dtype=np.int32)
+            qrows = (seq_idx[:, None] * qlen + (qlen - m) + np.arange(m)[None, :]).reshape(-1)
+            qsl = np.arange(0, qrows.size + 1, m, dtype=np.int32)
             oracle.paged_attention_multi(q[torch.from_numpy(qrows)], qsl, kc, vc, bt, sub_lens,
                                          ks, vs)
         elif variant in ("k_bf16", "v_bf16"):
@@ -602,9 +615,22 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     nbytes = reshape_bytes(w, slots, 2, k_elem, v_elem, pos if variant == "rope" else None,
                            w.head_dim)
     if decode:
-        nbytes += decode_bytes(w, sub_lens, k_elem, v_elem,
-                               len(seqs) * qlen if variant in ("multi", "prefill") else None)
+        if variant in ("multi", "prefill"):
+            nbytes += decode_bytes(w, sub_lens, k_elem, v_elem, len(seqs) * qlen) * m // qlen
+        else:
+            nbytes += decode_bytes(w, sub_lens, k_elem, v_elem)
     return dt, nbytes
+
+
+def _query_note(w: workloads.Workload, lay: workloads.Layout, variant: str) -> str:
+    if variant not in ("multi", "prefill"):
+        return ""
+    qlen = query_len(w, variant, lay.seq_lens)
+    lo = sampled_queries(w, qlen, int(lay.seq_lens.max()))
+    hi = sampled_queries(w, qlen, int(lay.seq_lens.min()))
+    return ("; attention for the last %s of each sampled sequence's %d new tokens (at most "
+            "2^28 oracle FLOPs), credited that fraction of its attention bytes"
+            % (str(lo) if lo == hi else "%d-%d" % (lo, hi), qlen))
 
 
 @functools.lru_cache(maxsize=2)
@@ -655,7 +681,8 @@ def cpu_baseline_all_cores(name: str, target_s: float = 4.0, variant: str = "fp8
     n = sum(r[1] for r in res)
     return {"value": nb / wall / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d whole-sequence samples of %s, variant %s, on %d threads (one sample "
-                      "per thread at a time), %.1f s wall" % (n, name, variant, cores, wall)}
+                      "per thread at a time), %.1f s wall%s"
+                      % (n, name, variant, cores, wall, _query_note(w, lay, variant))}
 
 
 def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dict:
@@ -673,9 +700,9 @@ def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dic
             break
     return {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%d of %d sequences of %s (%d tokens), variant %s: oracle write of their "
-                      "rows + attention for all %d heads, %.1f s single-threaded"
+                      "rows + attention for all %d heads, %.1f s single-threaded%s"
                       % (len(used), lay.num_seqs, name, int(lay.seq_lens[used].sum()), variant,
-                         w.n_q, t)}
+                         w.n_q, t, _query_note(w, lay, variant))}
 
 
 def run_reference(args):
@@ -693,8 +720,9 @@ def run_reference(args):
         nb += b
     value = nb / t / 1e9
     sample = ("each step: 1 of %d sequences of %s, variant %s, oracle write of its rows + "
-              "attention for all %d heads, single-threaded"
-              % (lay.num_seqs, args.workload, args.variant, w.n_q))
+              "attention for all %d heads, single-threaded%s"
+              % (lay.num_seqs, args.workload, args.variant, w.n_q,
+                 _query_note(w, lay, args.variant)))
     return {
         "impl": "reference",
         "metric": METRIC,

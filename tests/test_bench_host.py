@@ -165,3 +165,35 @@ def test_prefill_flops_count_the_causal_pairs():
     assert bench.attention_flops(w, lens, 3) == 4 * 128 * 32 * (3 + 4 + 5 + 6 + 7 + 8)
     assert bench.query_len(w, "prefill", np.array([4096, 4096])) == 512
     assert bench.query_len(w, "prefill", np.array([4096, 17])) == 17
+
+
+def test_cpu_sample_of_a_chunk_is_its_last_tokens_exactly():
+    # the CPU baseline of the multi-query forms attends with the last m of a sequence's new
+    # tokens: with the same cache and length, those rows equal the full chunk's last m rows
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import oracle
+    import workloads
+
+    w = workloads.WORKLOADS["llama3_8b"]
+    assert bench.sampled_queries(w, 512, 4096) == 4
+    assert bench.sampled_queries(w, 512, 1 << 20) == 1      # never fewer than one token
+    assert bench.sampled_queries(w, 3, 10) == 3             # never more than the chunk
+    g = torch.Generator().manual_seed(3)
+    L, n, m, bs = 40, 8, 3, 16
+    k = torch.randn(L, 2, 64, generator=g).to(torch.bfloat16)
+    v = torch.randn(L, 2, 64, generator=g).to(torch.bfloat16)
+    kc = np.zeros((3, bs, 2, 64), np.uint8)
+    vc = kc.copy()
+    assert oracle.reshape_and_cache(k, v, kc, vc, np.arange(L), bs, 0.05, 0.05) == 0
+    q = torch.randn(n, 4, 64, generator=g).to(torch.bfloat16)
+    bt = np.arange(3, dtype=np.int32)[None, :]
+    lens = np.array([L], np.int32)
+    full, st = oracle.paged_attention_multi(q, np.array([0, n], np.int32), kc, vc, bt, lens,
+                                            0.05, 0.05)
+    part, st2 = oracle.paged_attention_multi(q[n - m:], np.array([0, m], np.int32), kc, vc, bt,
+                                             lens, 0.05, 0.05)
+    assert st == st2 == 0
+    np.testing.assert_array_equal(np.asarray(part), np.asarray(full)[n - m:])
