@@ -216,7 +216,8 @@ kvfp8_status kvfp8_paged_attention_multi(
     if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
     const bool split_kv = kvfp8::multi_uses_decode_kernel(n_q, n_kv, head_dim, max_query_len);
     if (!split_kv && (n_q / n_kv > 128 ||
-                      (static_cast<int64_t>(max_query_len) * (n_q / n_kv) + 127) / 128 > 65535))
+                      (static_cast<int64_t>(max_query_len) * (n_q / n_kv) + 127) / 128 * n_kv *
+                              num_seqs > 0x7FFFFFFFLL))
         return KVFP8_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)

@@ -142,6 +142,7 @@ struct PrefillArgs {
     int32_t scale_dtype;
     uint32_t *status;
     int32_t box_rows;
+    int32_t row_tiles;  // tiles of 128 score rows per (sequence, kv head)
 };
 
 // Shared-memory plan (byte offsets from a 1024-aligned base).  Q is converted once; K and
@@ -199,7 +200,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     auto bar = [&](int off, int i) { return base + static_cast<uint32_t>(off + 8 * i); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seq = blockIdx.x, tile = blockIdx.y, kvh = blockIdx.z;
+    // kv head fastest, then row tile, then sequence: the CTAs resident at one time read every
+    // kv head's slice of the same cache rows, and a (sequence, kv head)'s row tiles run
+    // together, so its K/V tiles are fetched from HBM once and re-read from L2
+    const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.n_kv));
+    const int tile = static_cast<int>((blockIdx.x / static_cast<unsigned>(a.n_kv)) % static_cast<unsigned>(a.row_tiles));
+    const int seq = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
 
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
@@ -224,6 +230,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     const int j_last = min(nb, (row0 + kPfRows + G - 1) / G) - 1;
     const int kend = Ls - nb + j_last + 1;           // keys the tile's last row may see
     const int ntiles = kend > 0 ? (kend + kPfKeys - 1) / kPfKeys : 0;
+    // The row tiles of one (sequence, kv head) run side by side on one K/V stream; each
+    // starts its pass at its own key tile (the online softmax takes the keys in any order),
+    // so they read different lines of the stream at any one time.
+    const int rot = ntiles > 0 ? static_cast<int>((static_cast<int64_t>(tile) * ntiles) / a.row_tiles) % ntiles : 0;
+    auto key_tile = [&](int i) { const int k = i + rot; return k >= ntiles ? k - ntiles : k; };
 
     if (ntiles == 0) {  // every row of the tile sees no key: zero rows
         if (tid < kPfRows) {
@@ -269,42 +280,49 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     if (warp == kPfTmaWarp) {
         // ------------------------------------------------------------ TMA producer
         // The warp holds 32 block-table entries, one per lane (refreshed as the tiles move
-        // past them); lane 0 waits for a free stage and issues the copies.
+        // past them).  A tile is nbox boxes of K and nbox of V: lane p < nbox works out K box
+        // p and lane nbox + p V box p, side by side; lane 0 waits for a free stage and posts
+        // the expected bytes, then every lane with a box issues its own copy.  (This warp
+        // shares its scheduler with compute-heavy warps: its per-tile work is kept to a few
+        // dozen instructions, with no division.)
         const int32_t *bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
         const int bs = a.block_size, br = a.box_rows;
+        const int lbs = __ffs(bs) - 1;  // block_size is a power of two
         const int nbox = kPfKeys / br;
+        const bool k_lane = lane < nbox;
+        const int p = k_lane ? lane : lane - nbox;  // this lane's box within the tile
+        const bool box_lane = lane < 2 * nbox;
+        const CUtensorMap *map = k_lane ? &tmk : &tmv;
+        const uint32_t side = k_lane ? 0u : static_cast<uint32_t>(kPfKeys * HD);
         int wbase = -(1 << 30);
         int32_t win = -1;
         int issued = 0;
         bool aborted = false;
         for (int i = 0; i < ntiles; ++i) {
             const int st = i % L::kNS;
-            const int t0 = i * kPfKeys;
-            const int e0 = t0 / bs, e1 = (min(kend, t0 + kPfKeys) - 1) / bs;
+            const int t0 = key_tile(i) * kPfKeys;
+            const int e0 = t0 >> lbs, e1 = (min(kend, t0 + kPfKeys) - 1) >> lbs;
             if (e0 < wbase || e1 >= wbase + 32) {  // next window of block-table entries
                 wbase = e0;
                 win = wbase + lane < a.max_blocks_per_seq ? bt[wbase + lane] : -1;
             }
-            // per box: its first cache row, or -1 (past kend, or a bad block: left out)
-            uint64_t mask = 0;
-            int boxes = 0;
-            int rows[kPfKeys / 8];
-#pragma unroll
-            for (int p = 0; p < kPfKeys / 8; ++p) {
-                rows[p] = -1;
-                if (p >= nbox) continue;
-                const int t = t0 + p * br;
-                const int blk = __shfl_sync(0xFFFFFFFFu, win, (t / bs - wbase) & 31);
-                if (t >= kend) continue;
-                if (blk < 0 || blk >= a.num_blocks) {
-                    if (lane == 0) flag(a.status, KVFP8_DEV_BAD_BLOCK);
-                    continue;
-                }
-                rows[p] = blk * bs + t % bs;
-                ++boxes;
+            // this lane's box: its first key t, the block holding it, and whether it is
+            // copied (keys past kend are left out; a bad block is flagged and left out)
+            const int t = t0 + p * br;
+            const int blk = __shfl_sync(0xFFFFFFFFu, win, ((t >> lbs) - wbase) & 31);
+            const bool live = box_lane && t < kend;
+            const bool good = live && blk >= 0 && blk < a.num_blocks;
+            if (live && !good && k_lane) flag(a.status, KVFP8_DEV_BAD_BLOCK);
+            const int row = blk * bs + (t & (bs - 1));
+            uint64_t part = 0;
+            if (good && k_lane) {
                 const int nk = min(br, kend - t);
-                mask |= (nk >= 64 ? ~0ull : ((1ull << nk) - 1)) << (p * br);
+                part = (nk >= 64 ? ~0ull : ((1ull << nk) - 1)) << (p * br);
             }
+            const uint64_t mask =
+                static_cast<uint64_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(part))) |
+                static_cast<uint64_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(part >> 32))) << 32;
+            const int boxes = __popc(__ballot_sync(0xFFFFFFFFu, good && k_lane));
             if (lane == 0) {
                 if (!mbar_wait(bar(L::kEmpty, st), ((i / L::kNS) & 1) ^ 1u, abort_flag)) {
                     aborted = true;
@@ -320,18 +338,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             }
             aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
             if (aborted) break;
-            // the expected bytes are posted: lane 0 issues the K copies, lane 1 the V copies
-            if (lane < 2 && boxes > 0) {
+            // the expected bytes are posted: each lane with a box copies it
+            if (good) {
                 const uint32_t full = bar(L::kFull, st);
-                const uint32_t dst = base + L::kStage + st * L::kStageBytes + lane * (kPfKeys * HD);
-                const CUtensorMap *map = lane == 0 ? &tmk : &tmv;
+                const uint32_t dst = base + L::kStage + st * L::kStageBytes + side +
+                                     static_cast<uint32_t>(p * br * L::kSeg);
 #pragma unroll
-                for (int p = 0; p < kPfKeys / 8; ++p) {
-                    if (rows[p] < 0) continue;
-                    for (int sgi = 0; sgi < L::kSegs; ++sgi)
-                        tma_load_3d(dst + static_cast<uint32_t>(sgi * kPfKeys * L::kSeg + p * br * L::kSeg),
-                                    map, 0, kvh * L::kSegs + sgi, rows[p], full);
-                }
+                for (int sgi = 0; sgi < L::kSegs; ++sgi)
+                    tma_load_3d(dst + static_cast<uint32_t>(sgi * kPfKeys * L::kSeg), map, 0,
+                                kvh * L::kSegs + sgi, row, full);
             }
         }
         if (aborted && lane == 0) {
@@ -510,7 +525,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tmem_wait_ld();
             // causal mask, scale, running maximum (a key past the row's position, past the
             // sequence or in a bad block scores -inf; keys past kend are past every position)
-            const int k0 = i * kPfKeys;
+            const int k0 = key_tile(i) * kPfKeys;
             const int vis_n = row_ok ? min(kPfKeys, max(0, pos - k0 + 1)) : 0;  // keys 0..vis_n-1
             const uint64_t vis = mask & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
             float mx = -INFINITY;
@@ -645,9 +660,9 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     a.scale_dtype = d.scale_dtype;
     a.status = d.status;
     a.box_rows = box_rows;
-    const int tiles = (d.qmax * a.group + kPfRows - 1) / kPfRows;
-    dim3 grid(d.num_seqs, tiles, d.n_kv);
-    kern<<<grid, kPfWarps * 32, smem, stream>>>(tmk, tmv, a);
+    a.row_tiles = (d.qmax * a.group + kPfRows - 1) / kPfRows;
+    const int64_t ctas = static_cast<int64_t>(d.num_seqs) * a.row_tiles * d.n_kv;
+    kern<<<static_cast<unsigned>(ctas), kPfWarps * 32, smem, stream>>>(tmk, tmv, a);
     return cudaGetLastError();
 }
 
@@ -657,7 +672,8 @@ cudaError_t launch_prefill_attention(const DecodeArgs &d, cudaStream_t stream) {
     if (d.num_seqs == 0) return cudaSuccess;
     if (d.k_bf16 || d.v_bf16) return cudaErrorNotSupported;
     if (d.n_q / d.n_kv > kPfRows) return cudaErrorNotSupported;
-    if ((d.qmax * (d.n_q / d.n_kv) + kPfRows - 1) / kPfRows > 65535) return cudaErrorNotSupported;
+    const int64_t row_tiles = (static_cast<int64_t>(d.qmax) * (d.n_q / d.n_kv) + kPfRows - 1) / kPfRows;
+    if (row_tiles * d.n_kv * d.num_seqs > 0x7FFFFFFF) return cudaErrorNotSupported;
     switch (d.head_dim) {
         case 64: return run_prefill<64>(d, stream);
         case 128: return run_prefill<128>(d, stream);
