@@ -126,6 +126,71 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// packed fp32 pairs (sm_100+ f32x2 arithmetic: two IEEE round-to-nearest operations)
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ uint64_t pk2u(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 upk2(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+// 2^x on an f16 pair (the tensor core takes P as f16)
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+    uint32_t r;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+__device__ __forceinline__ float f16lo_f32(uint32_t h) {
+    float r;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, l;\n\t}" : "=f"(r) : "r"(h));
+    return r;
+}
+__device__ __forceinline__ float f16hi_f32(uint32_t h) {
+    float r;
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %1;\n\tcvt.f32.f16 %0, u;\n\t}" : "=f"(r) : "r"(h));
+    return r;
+}
+// the largest (kMax) or smallest of 64 scores, four independent chains of 3-input ops
+template <bool kMax>
+__device__ __forceinline__ float extreme64(const uint32_t (&s)[2][32]) {
+    auto v = [&](int c) { return __uint_as_float(s[c >> 5][c & 31]); };
+    auto op = [](float a, float b, float c) { return kMax ? max3f(a, b, c) : min3f(a, b, c); };
+    float a0 = v(0), a1 = v(1), a2 = v(2), a3 = v(3);
+#pragma unroll
+    for (int c = 4; c < 60; c += 8) {
+        a0 = op(a0, v(c), v(c + 1));
+        a1 = op(a1, v(c + 2), v(c + 3));
+        a2 = op(a2, v(c + 4), v(c + 5));
+        a3 = op(a3, v(c + 6), v(c + 7));
+    }
+    a0 = op(a0, v(60), v(61));
+    a1 = op(a1, v(62), v(63));
+    return op(a0, a1, kMax ? fmaxf(a2, a3) : fminf(a2, a3));
+}
+
 struct PrefillArgs {
     __nv_bfloat16 *out;
     const __nv_bfloat16 *query;
@@ -156,7 +221,13 @@ struct PfSmem {
     static constexpr int kNS = HD >= 256 ? 1 : 4;                  // FP8 staging stages
     static constexpr int kQ = 0;                                   // Q f16: HD/64 blocks x 128 rows x 128 B
     static constexpr int kKBuf = HD * 128;                         // one K f16 buffer: HD/64 x 64 rows x 128 B
-    static constexpr int kVBuf = HD * 128;                         // one V^T f16 buffer: HD rows x 128 B
+    // Up to head_dim 128, V^T carries 16 more rows: a row of ones then zeros, so the O
+    // product also accumulates each score row's sum of P (column HD of O) in fp32.  At 256
+    // there is no room (the product's N would pass 256 and shared memory would overflow):
+    // the softmax warps sum P themselves.
+    static constexpr bool kSumCol = HD <= 128;
+    static constexpr int kVRows = HD + (kSumCol ? 16 : 0);
+    static constexpr int kVBuf = kVRows * 128;                     // one V^T f16 buffer: rows x 128 B
     static constexpr int kK = kQ + HD * 256;
     static constexpr int kV = kK + kNB * kKBuf;
     static constexpr int kStage = kV + kNB * kVBuf;                // fp8 K then V, per stage
@@ -174,7 +245,7 @@ struct PfSmem {
     static constexpr int kTotal = kMisc + 16;
     // tensor memory: S[NB] (64 fp32 columns each; P as f16 over the first 32), then O
     static constexpr uint32_t kColO = 64 * kNB;
-    static constexpr uint32_t kTmemCols = kColO + HD <= 256 ? 256 : 512;
+    static constexpr uint32_t kTmemCols = kColO + HD + 32 <= 256 ? 256 : 512;
 };
 
 // Warp roles (448 threads): warps 0-3 softmax + epilogue (TMEM lane quarters 0-3, one score
@@ -361,7 +432,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // S(i) is issued before O(i-1), so the tensor core computes the next scores while the
         // softmax warps work on the current ones.
         if (lane == 0) {
-            const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, HD);
+            const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, L::kVRows);
             int o_issued = 0;  // O products issued so far
             bool ok = true;
             auto issue_o = [&](int t) {  // O += P(t) . V(t), then release tile t's buffers
@@ -426,6 +497,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 h.z = f16x2_from_f32(bf16lo(w.z), bf16hi(w.z));
                 h.w = f16x2_from_f32(bf16lo(w.w), bf16hi(w.w));
                 *reinterpret_cast<uint4 *>(bp + L::kQ + (c >> 3) * (kPfRows * 128) + sw128(ct, c & 7)) = h;
+            }
+        }
+        if (L::kSumCol) {  // V^T rows HD..HD+15 of every buffer: ones, then zeros
+            for (int e = ct; e < L::kNB * 128; e += kCT) {
+                const int bb = e >> 7, w = e & 127;  // 128 16-byte words per buffer
+                const uint32_t one = w < 8 ? 0x3C003C00u : 0u;
+                *reinterpret_cast<uint4 *>(bp + L::kV + bb * L::kVBuf + HD * 128 + 16 * w) =
+                    make_uint4(one, one, one, one);
             }
         }
         bool ok = true;
@@ -524,20 +603,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             tmem_ld32(lane_addr + 64 * b + 32, s[1]);
             tmem_wait_ld();
             // causal mask, scale, running maximum (a key past the row's position, past the
-            // sequence or in a bad block scores -inf; keys past kend are past every position)
+            // sequence or in a bad block scores -inf; keys past kend are past every position).
+            // A tile every row of the warp sees whole takes no mask: the maximum is taken on
+            // the raw scores (the smallest when the scale is negative) and scaled once, and
+            // the scale is applied inside the exponent's fma.
             const int k0 = key_tile(i) * kPfKeys;
             const int vis_n = row_ok ? min(kPfKeys, max(0, pos - k0 + 1)) : 0;  // keys 0..vis_n-1
             const uint64_t vis = mask & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
-            float mx = -INFINITY;
+            float mx, mult;
+            if (__all_sync(0xFFFFFFFFu, vis == ~0ull)) {
+                mx = (score_scale >= 0.f ? extreme64<true>(s) : extreme64<false>(s)) * score_scale;
+                mult = score_scale;
+            } else {
+                mx = -INFINITY;
+                mult = 1.f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float v = ((vis >> (32 * h + c)) & 1ull) ? __uint_as_float(s[h][c]) * score_scale
-                                                                   : -INFINITY;
-                    s[h][c] = __float_as_uint(v);
-                    mx = fmaxf(mx, v);
-                }
+                    for (int c = 0; c < 32; ++c) {
+                        const float v = ((vis >> (32 * h + c)) & 1ull)
+                                            ? __uint_as_float(s[h][c]) * score_scale
+                                            : -INFINITY;
+                        s[h][c] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+            }
             // rescale O only when the maximum grew by more than 2^8 (first visible keys: O is
             // still zero for this row, nothing to rescale)
             float factor = 1.f;
@@ -550,14 +640,14 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 }
             }
             if (__any_sync(0xFFFFFFFFu, factor != 1.f)) {
-                // O(i-1) must be complete before O is rescaled
+                // O(i-1) must be complete before O is rescaled (with its row-sum column)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvFree, (i - 1) % L::kNB),
                                                        ((i - 1) / L::kNB) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 lsum *= factor;
 #pragma unroll 1
-                for (int c0 = 0; c0 < HD; c0 += 32) {
+                for (int c0 = 0; c0 < (L::kSumCol ? HD + 32 : HD); c0 += 32) {
                     uint32_t o[32];
                     tmem_ld32(lane_addr + L::kColO + c0, o);
                     tmem_wait_ld();
@@ -566,16 +656,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     tmem_st32(lane_addr + L::kColO + c0, o);
                 }
             }
-            // P = 2^(s - m), f16 pairs over the first 32 columns of this S buffer
+            // P = 2^(s*mult - m) as f16 pairs over the first 32 columns of this S buffer: one
+            // packed fma, one f16 pack and one f16x2 exp2 per pair (x <= 2^3 by the rescale
+            // rule, so P <= 2^8)
             uint32_t p[32];
             const float msub = m_used == -INFINITY ? 0.f : m_used;
+            const uint64_t mul2 = pk2(mult, mult), sub2 = pk2(-msub, -msub);
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
                 const int h = c >> 4, e = (2 * c) & 31;
-                const float p0 = ex2(__uint_as_float(s[h][e]) - msub);
-                const float p1 = ex2(__uint_as_float(s[h][e + 1]) - msub);
-                lsum += p0 + p1;
-                p[c] = f16x2_from_f32(p0, p1);
+                const float2 x = upk2(fma_f32x2(pk2u(s[h][e], s[h][e + 1]), mul2, sub2));
+                p[c] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
+                if (!L::kSumCol) lsum += f16lo_f32(p[c]) + f16hi_f32(p[c]);
             }
             tmem_st32(lane_addr + 64 * b, p);
             tmem_wait_st();
@@ -588,6 +680,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                                                    ((ntiles - 1) / L::kNB) & 1, abort_flag));
         if (ok) {
             tc_fence_after();
+            if (L::kSumCol) {  // the row's sum of P, accumulated by the O product
+                uint32_t o[32];
+                tmem_ld32(lane_addr + L::kColO + HD, o);
+                tmem_wait_ld();
+                lsum = __uint_as_float(o[0]);
+            }
             const float inv = lsum > 0.f ? sv / lsum : 0.f;
             uint4 *orow = reinterpret_cast<uint4 *>(
                 a.out + ((static_cast<int64_t>(qr.q0) + jq) * a.n_q + kvh * G + gq) * HD);
