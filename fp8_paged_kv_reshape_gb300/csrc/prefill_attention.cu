@@ -521,13 +521,65 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const uint8_t *vst = kst + kPfKeys * HD;
             uint8_t *kdst0 = bp + L::kK + b * L::kKBuf;
             uint8_t *vdst = bp + L::kV + b * L::kVBuf;
-            // K: 64 keys x HD/16 chunks of 16 fp8 -> f16 (invalid keys: zeros)
-            for (int task = ct; task < kPfKeys * (HD / 16); task += kCT) {
+            // K: 64 keys x HD/16 chunks of 16 fp8 -> f16 (invalid keys: zeros).
+            // V^T by 8-key x 32-dim blocks: lane t converts dims (8j + 2(t%4), +1) of key t/4
+            // (one e4m3 pair -> f16x2 per matrix j) and stmatrix.trans writes each dim's 8 keys
+            // as one 16-byte row of V^T (head dims as rows, keys along K).
+            // Every load of a round is issued before the first conversion, so their latencies
+            // overlap (a store to shared memory would otherwise hold back the next load).
+            constexpr int kKT = kPfKeys * (HD / 16) / kCT;                   // K tasks per thread
+            constexpr int kVB = (kPfKeys / 8) * (HD / 32) / kPfConvWarps;    // V^T blocks per warp
+            constexpr int kVG = kVB < 4 ? kVB : 4;                           // V^T blocks per round
+            const int w4 = warp - 4;
+            const uint32_t vbase = base + L::kV + b * L::kVBuf;
+            uint4 kw[kKT];
+            uint4 vw[kVG][2];
+            auto v_load = [&](int g0) {
+#pragma unroll
+                for (int j = 0; j < kVG; ++j) {
+                    const int blk = w4 + (g0 + j) * kPfConvWarps;
+                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
+                    const int key = ko * 8 + (lane >> 2);
+                    const int sgi = (32 * dg) / L::kSeg, cc = ((32 * dg) % L::kSeg) >> 4;
+                    const uint8_t *vrow = vst + sgi * kPfKeys * L::kSeg;
+                    vw[j][0] = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc));
+                    vw[j][1] = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc + 1));
+                    if (!((mask >> key) & 1ull)) vw[j][0] = vw[j][1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            };
+            auto v_store = [&](int g0) {
+#pragma unroll
+                for (int j = 0; j < kVG; ++j) {
+                    const int blk = w4 + (g0 + j) * kPfConvWarps;
+                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
+                    const uint4 lo = vw[j][0], hi = vw[j][1];
+                    const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    uint32_t r[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        // bytes 8q + 2(t%4), +1 of the key's 32: word 2q + (t%4)/2, half t%2
+                        const uint32_t w = (lane & 2) ? wd[2 * q + 1] : wd[2 * q];
+                        r[q] = (lane & 1) ? f16x2_from_e4m3x2_hi(w) : f16x2_from_e4m3x2(w);
+                    }
+                    const int n = 32 * dg + 8 * (lane >> 3) + (lane & 7);  // V^T row this lane addresses
+                    stsm_x4_t(vbase + sw128(n, ko), r[0], r[1], r[2], r[3]);
+                }
+            };
+#pragma unroll
+            for (int j = 0; j < kKT; ++j) {
+                const int task = ct + j * kCT;
                 const int key = task / (HD / 16), c = task % (HD / 16);  // dims 16c .. 16c+15
                 const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
-                uint4 w = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
-                                                           swz<L::kSeg>(key, within >> 4));
-                if (!((mask >> key) & 1ull)) w = make_uint4(0u, 0u, 0u, 0u);
+                kw[j] = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
+                                                         swz<L::kSeg>(key, within >> 4));
+                if (!((mask >> key) & 1ull)) kw[j] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            v_load(0);
+#pragma unroll
+            for (int j = 0; j < kKT; ++j) {
+                const int task = ct + j * kCT;
+                const int key = task / (HD / 16), c = task % (HD / 16);
+                const uint4 w = kw[j];
                 uint4 h0, h1;
                 h0.x = f16x2_from_e4m3x2(w.x);
                 h0.y = f16x2_from_e4m3x2_hi(w.x);
@@ -542,31 +594,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
             }
-            // V^T by 8-key x 32-dim blocks: lane t converts dims (8j + 2(t%4), +1) of key t/4
-            // (one e4m3 pair -> f16x2 per matrix j) and stmatrix.trans writes each dim's 8 keys
-            // as one 16-byte row of V^T (head dims as rows, keys along K)
-            {
-                const int w4 = warp - 4;
-                const uint32_t vbase = base + L::kV + b * L::kVBuf;
-                for (int blk = w4; blk < (kPfKeys / 8) * (HD / 32); blk += kPfConvWarps) {
-                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
-                    const int key = ko * 8 + (lane >> 2);
-                    const int sgi = (32 * dg) / L::kSeg, cc = ((32 * dg) % L::kSeg) >> 4;
-                    const uint8_t *vrow = vst + sgi * kPfKeys * L::kSeg;
-                    uint4 lo = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc));
-                    uint4 hi = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc + 1));
-                    if (!((mask >> key) & 1ull)) lo = hi = make_uint4(0u, 0u, 0u, 0u);
-                    const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                    uint32_t r[4];
+            v_store(0);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        // bytes 8j + 2(t%4), +1 of the key's 32: word 2j + (t%4)/2, half t%2
-                        const uint32_t w = (lane & 2) ? wd[2 * j + 1] : wd[2 * j];
-                        r[j] = (lane & 1) ? f16x2_from_e4m3x2_hi(w) : f16x2_from_e4m3x2(w);
-                    }
-                    const int n = 32 * dg + 8 * (lane >> 3) + (lane & 7);  // V^T row this lane addresses
-                    stsm_x4_t(vbase + sw128(n, ko), r[0], r[1], r[2], r[3]);
-                }
+            for (int g0 = kVG; g0 < kVB; g0 += kVG) {
+                v_load(g0);
+                v_store(g0);
             }
             if (ct == 0) buf_mask[b] = mask;  // for the softmax warps, released with kv_ready
             fence_proxy_async();
