@@ -10,18 +10,20 @@
 //  * Work unit: one CTA per (sequence, kv head, tile of 128 score rows).  A row is a
 //    (query token j, head g of the kv head's group) pair, row = j*G + g, so all rows of a
 //    tile share one K/V stream.  Keys are visited in tiles of 64 up to the tile's last
-//    causal position.
-//  * Warp-specialized, every stage overlapped with the others:
-//      - warp 9 issues the TMA loads of the FP8 K/V tiles (the per-head-segment boxes of
-//        the decode kernel's cache map) into a multi-stage ring;
-//      - warps 4-7 convert the tile's q rows bf16 -> f16 once, and each K tile
+//    causal position, each row tile starting at its own key tile (the online softmax takes
+//    the keys in any order).  The grid runs kv head fastest, then row tile, then sequence.
+//  * Warp-specialized, every stage overlapped with the others (14 warps):
+//      - warp 13 issues the TMA loads of the FP8 K/V tiles (per-head-segment boxes of the
+//        cache map, one lane per box) into a four-stage ring;
+//      - warps 4-11 convert the tile's q rows bf16 -> f16 once, and each K tile
 //        e4m3 -> f16, into the K-major 128-byte-swizzled operand layout, and each V tile
 //        e4m3 -> f16 transposed (V^T: head dims as rows, keys along K), so both products
-//        take K-major operands; K and V^T are double-buffered;
-//      - one thread of warp 8 issues S(i) = Q.K(i)^T (tcgen05.mma kind::f16, M = 128,
-//        N = 64, fp32 in one of two TMEM buffers) and then O += P(i-1).V(i-1) (A = P from
-//        TMEM, B = V^T from shared memory, N = head_dim), so the next scores are computed
-//        while the softmax works on the current ones;
+//        take K-major operands; K, V^T and the score buffers are triple-buffered;
+//      - one thread of warp 12 issues S(i) = Q.K(i)^T (tcgen05.mma kind::f16, M = 128,
+//        N = 64, fp32 in tensor memory) and then O += P(i-1).V(i-1) (A = P from tensor
+//        memory, B = V^T from shared memory), so the next scores are computed while the
+//        softmax works on the current ones.  Up to head_dim 128 V^T carries a row of ones,
+//        so the same product also sums each row of P;
 //      - warps 0-3 (one TMEM lane quarter each, one score row per thread) read S, apply
 //        the causal mask and the online softmax (log2 domain), and write P (f16) back over
 //        S.  O is rescaled in TMEM only when a row's running maximum grows by more than
