@@ -534,6 +534,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             constexpr int kVG = kVB < 4 ? kVB : 4;                           // V^T blocks per round
             const int w4 = warp - 4;
             const uint32_t vbase = base + L::kV + b * L::kVBuf;
+            const uint32_t vsel = static_cast<uint32_t>(2 * (lane & 3)) | static_cast<uint32_t>(2 * (lane & 3) + 1) << 4;
             uint4 kw[kKT];
             uint4 vw[kVG][2];
             auto v_load = [&](int g0) {
@@ -558,11 +559,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     uint32_t r[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        // bytes 8q + 2(t%4), +1 of the key's 32: word 2q + (t%4)/2, half t%2
-                        const uint32_t w = (lane & 2) ? wd[2 * q + 1] : wd[2 * q];
-                        r[q] = (lane & 1) ? f16x2_from_e4m3x2_hi(w) : f16x2_from_e4m3x2(w);
-                    }
+                    for (int q = 0; q < 4; ++q)  // bytes 8q + 2(t%4), +1 of the key's 32
+                        r[q] = f16x2_from_e4m3x2(__byte_perm(wd[2 * q], wd[2 * q + 1], vsel));
                     const int n = 32 * dg + 8 * (lane >> 3) + (lane & 7);  // V^T row this lane addresses
                     stsm_x4_t(vbase + sw128(n, ko), r[0], r[1], r[2], r[3]);
                 }

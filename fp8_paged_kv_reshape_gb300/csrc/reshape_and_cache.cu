@@ -154,6 +154,15 @@ struct Group<false> {  // bf16: 16 bytes
         x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
         x[4] = bf16lo(v.z); x[5] = bf16hi(v.z); x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
     }
+    // the same group of lane ^ m (packed: four shuffles for eight values)
+    __device__ __forceinline__ Group xor_lane(int m) const {
+        Group g;
+        g.v.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, m);
+        g.v.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, m);
+        g.v.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, m);
+        g.v.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, m);
+        return g;
+    }
     static constexpr int kBytes = 16;
 };
 
@@ -167,6 +176,14 @@ struct Group<true> {  // fp32: 32 bytes
     __device__ __forceinline__ void unpack(float (&x)[8]) const {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    __device__ __forceinline__ Group xor_lane(int m) const {
+        Group g;
+        g.a = make_float4(__shfl_xor_sync(0xFFFFFFFFu, a.x, m), __shfl_xor_sync(0xFFFFFFFFu, a.y, m),
+                          __shfl_xor_sync(0xFFFFFFFFu, a.z, m), __shfl_xor_sync(0xFFFFFFFFu, a.w, m));
+        g.b = make_float4(__shfl_xor_sync(0xFFFFFFFFu, b.x, m), __shfl_xor_sync(0xFFFFFFFFu, b.y, m),
+                          __shfl_xor_sync(0xFFFFFFFFu, b.z, m), __shfl_xor_sync(0xFFFFFFFFu, b.w, m));
+        return g;
     }
     static constexpr int kBytes = 32;
 };
@@ -373,9 +390,8 @@ __device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], cons
         float x[8];
         buf[u].unpack(x);  // lanes past the row hold stale values; they only feed shuffles
         if (a.neox) {
-            float y[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) y[i] = __shfl_xor_sync(0xFFFFFFFFu, x[i], partner);
+            float y[8];  // the partner group's values, shuffled packed (half the shuffles for bf16)
+            buf[u].xor_lane(partner).unpack(y);
             if (g < groups && rotated) {
                 // first half: x*c - y*s; second half: y*s + x*c (= x*c + y*s exactly)
 #pragma unroll
