@@ -253,7 +253,8 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
  * below.  Every other shape (long query chunks,
  * prefill) runs on the tensor cores (tcgen05, accumulators in tensor memory), one CTA per
  * 128 (query token, head) rows of a kv head, with no workspace; it needs
- * n_q / n_kv <= 128.
+ * n_q / n_kv <= 128 and num_seqs * n_kv * ceil(max_query_len * (n_q / n_kv) / 128) < 2^31
+ * CTAs, else KVFP8_ERR_UNSUPPORTED.
  *
  * out, query        device bf16 [num_query_rows][n_q][head_dim]
  * query_start_loc   device int32 [num_seqs + 1], non-decreasing; a sequence whose rows

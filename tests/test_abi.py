@@ -202,6 +202,8 @@ def test_multi_query_host_validation_on_the_tensor_core_route():
     assert call(query=None) == binding.ERR_NULL
     assert call(qsl=ctypes.c_void_p(18)) == binding.ERR_ALIGN
     assert call(n_q=129 * 2, n_kv=2) == binding.ERR_UNSUPPORTED     # group of 129 heads
+    # 2^20 sequences x 8 kv heads x 4096 row tiles: 2^35 CTAs, past the 2^31 - 1 grid
+    assert call(num_seqs=1 << 20, n_q=128 * 8, qmax=1 << 12) == binding.ERR_UNSUPPORTED
     assert call(num_seqs=0, query=None) == binding.OK
     # the split-KV route still wants its workspace
     assert call(qmax=4, workspace=None) == binding.ERR_NULL
