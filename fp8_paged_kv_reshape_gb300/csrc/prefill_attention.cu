@@ -751,6 +751,528 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     }
 }
 
+// ---------------------------------------------------------------- two row tiles per CTA
+//
+// For head_dim 64 and 128 when a (sequence, kv head) has more than 128 score rows: one CTA
+// takes 256 rows as two row tiles that share every converted K/V tile, so the copies and
+// the conversion are paid once per two tiles of tensor work.  Each row tile has its own
+// softmax warpgroup and two score buffers in tensor memory, so S(i+1) of a row tile is
+// computed while its softmax works on S(i), and the two row tiles' products interleave on
+// the tensor core.  Tensor memory (512 columns at head_dim 128): S[r][j] at 64*(2r+j),
+// O[r] at 256 + head_dim*r.  The rows sum P themselves (fp32, in pairs).
+//
+// Warps (14): 0-3 softmax of row tile 0, 4-7 softmax of row tile 1 (warp w reads TMEM
+// lanes 32*(w%4)..+31), 8-11 conversion, 12 tensor-core issue (and TMEM allocation), 13 TMA.
+constexpr int kP2Rows = 2 * kPfRows;
+constexpr int kP2ConvWarps = 4;
+constexpr int kP2MmaWarp = 8 + kP2ConvWarps, kP2TmaWarp = kP2MmaWarp + 1;
+constexpr int kP2Warps = kP2TmaWarp + 1;
+
+template <int HD>
+struct Pf2Smem {
+    static constexpr int kSeg = HD >= 128 ? 128 : 64;
+    static constexpr int kSegs = HD / kSeg;
+    static constexpr int kNB = 3;                                  // f16 K / V^T buffers
+    static constexpr int kNS = HD >= 128 ? 3 : 4;                  // FP8 staging stages
+    static constexpr int kQTile = HD * 256;                        // one row tile of Q (f16)
+    static constexpr int kQ = 0;
+    static constexpr int kKBuf = HD * 128, kVBuf = HD * 128;
+    static constexpr int kK = kQ + 2 * kQTile;
+    static constexpr int kV = kK + kNB * kKBuf;
+    static constexpr int kStage = kV + kNB * kVBuf;
+    static constexpr int kStageBytes = 2 * kPfKeys * HD;
+    static constexpr int kBars = kStage + kNS * kStageBytes;
+    // mbarriers: full[NS], empty[NS], kv_ready[NB], kv_free[NB], then per (row tile r,
+    // score buffer j) at index 2r+j: s_ready, p_ready, o_done
+    static constexpr int kFull = kBars, kEmpty = kFull + 8 * kNS, kKvReady = kEmpty + 8 * kNS;
+    static constexpr int kKvFree = kKvReady + 8 * kNB, kSReady = kKvFree + 8 * kNB;
+    static constexpr int kPReady = kSReady + 8 * 4, kODone = kPReady + 8 * 4;
+    static constexpr int kMeta = kODone + 8 * 4;
+    static constexpr int kBufMask = kMeta + 8 * kNS;
+    static constexpr int kMisc = kBufMask + 8 * kNB;
+    static constexpr int kTotal = kMisc + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    __host__ __device__ static constexpr uint32_t col_s(int r, int j) { return static_cast<uint32_t>(64 * (2 * r + j)); }
+    __host__ __device__ static constexpr uint32_t col_o(int r) { return static_cast<uint32_t>(256 + HD * r); }
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kP2Warps * 32, 1)
+prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                const PrefillArgs a) {
+    using L = Pf2Smem<HD>;
+    static_assert(L::kTotal + 1024 <= 232448, "shared memory");
+    static_assert(L::col_o(1) + HD <= L::kTmemCols, "tensor memory");
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *bp = smem_raw + (base - raw);
+    volatile uint64_t *meta = reinterpret_cast<volatile uint64_t *>(bp + L::kMeta);
+    volatile uint64_t *buf_mask = reinterpret_cast<volatile uint64_t *>(bp + L::kBufMask);
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(bp + L::kMisc);
+    volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(bp + L::kMisc + 4);
+    auto bar = [&](int off, int i) { return base + static_cast<uint32_t>(off + 8 * i); };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.n_kv));
+    const int ctile = static_cast<int>((blockIdx.x / static_cast<unsigned>(a.n_kv)) % static_cast<unsigned>(a.row_tiles));
+    const int seq = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
+
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) {
+        if (seq == 0 && ctile == 0 && kvh == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        return;
+    }
+    const int raw_nq = a.qsl[seq + 1] - a.qsl[seq];
+    const QueryRange qr = query_range(a.qsl, seq, a.qmax, a.qrows);
+    const int Lraw = a.seq_lens[seq];
+    const int Ls = min(max(Lraw, 0), a.max_len);
+    if (ctile == 0 && kvh == 0 && tid == 0 &&
+        (qr.count != raw_nq || Lraw < 0 || Lraw > a.max_len || qr.count > Ls))
+        flag(a.status, KVFP8_DEV_BAD_BLOCK);
+    const int nb = qr.count, G = a.group;
+    const int row0 = ctile * kP2Rows;                 // first score row of this CTA
+    if (row0 >= nb * G) return;
+    const int j_last = min(nb, (row0 + kP2Rows + G - 1) / G) - 1;
+    const int kend = Ls - nb + j_last + 1;            // keys the CTA's last row may see
+    const int ntiles = kend > 0 ? (kend + kPfKeys - 1) / kPfKeys : 0;
+    const int rot = ntiles > 0 ? static_cast<int>((static_cast<int64_t>(ctile) * ntiles) / a.row_tiles) % ntiles : 0;
+    auto key_tile = [&](int i) { const int k = i + rot; return k >= ntiles ? k - ntiles : k; };
+
+    if (ntiles == 0) {  // every row of the CTA sees no key: zero rows
+        if (tid < kP2Rows) {
+            const int r = row0 + tid;
+            if (r < nb * G) {
+                const int j = r / G, g = r % G;
+                uint4 *o = reinterpret_cast<uint4 *>(
+                    a.out + ((static_cast<int64_t>(qr.q0) + j) * a.n_q + kvh * G + g) * HD);
+                for (int c = 0; c < HD / 8; ++c) o[c] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < L::kNS; ++s) {
+            mbar_init(bar(L::kFull, s), 1);
+            mbar_init(bar(L::kEmpty, s), kP2ConvWarps);
+        }
+        for (int b = 0; b < L::kNB; ++b) {
+            mbar_init(bar(L::kKvReady, b), kP2ConvWarps);
+            mbar_init(bar(L::kKvFree, b), 1);
+        }
+        for (int q = 0; q < 4; ++q) {
+            mbar_init(bar(L::kSReady, q), 1);
+            mbar_init(bar(L::kPReady, q), 4);
+            mbar_init(bar(L::kODone, q), 1);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kP2MmaWarp) {
+        tmem_alloc(base + L::kMisc, L::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kP2TmaWarp && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const volatile int32_t never = 0;
+
+    if (warp == kP2TmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        // lane p < nbox: K box p of the tile; lane nbox + p: V box p (as in prefill_kernel)
+        const int32_t *bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
+        const int bs = a.block_size, br = a.box_rows;
+        const int lbs = __ffs(bs) - 1;
+        const int nbox = kPfKeys / br;
+        const bool k_lane = lane < nbox;
+        const int p = k_lane ? lane : lane - nbox;
+        const bool box_lane = lane < 2 * nbox;
+        const CUtensorMap *map = k_lane ? &tmk : &tmv;
+        const uint32_t side = k_lane ? 0u : static_cast<uint32_t>(kPfKeys * HD);
+        int wbase = -(1 << 30);
+        int32_t win = -1;
+        int issued = 0;
+        bool aborted = false;
+        for (int i = 0; i < ntiles; ++i) {
+            const int st = i % L::kNS;
+            const int t0 = key_tile(i) * kPfKeys;
+            const int e0 = t0 >> lbs, e1 = (min(kend, t0 + kPfKeys) - 1) >> lbs;
+            if (e0 < wbase || e1 >= wbase + 32) {
+                wbase = e0;
+                win = wbase + lane < a.max_blocks_per_seq ? bt[wbase + lane] : -1;
+            }
+            const int t = t0 + p * br;
+            const int blk = __shfl_sync(0xFFFFFFFFu, win, ((t >> lbs) - wbase) & 31);
+            const bool live = box_lane && t < kend;
+            const bool good = live && blk >= 0 && blk < a.num_blocks;
+            if (live && !good && k_lane) flag(a.status, KVFP8_DEV_BAD_BLOCK);
+            const int row = blk * bs + (t & (bs - 1));
+            uint64_t part = 0;
+            if (good && k_lane) {
+                const int nk = min(br, kend - t);
+                part = (nk >= 64 ? ~0ull : ((1ull << nk) - 1)) << (p * br);
+            }
+            const uint64_t mask =
+                static_cast<uint64_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(part))) |
+                static_cast<uint64_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(part >> 32))) << 32;
+            const int boxes = __popc(__ballot_sync(0xFFFFFFFFu, good && k_lane));
+            if (lane == 0) {
+                if (!mbar_wait(bar(L::kEmpty, st), ((i / L::kNS) & 1) ^ 1u, abort_flag)) {
+                    aborted = true;
+                } else {
+                    meta[st] = mask;
+                    const uint32_t full = bar(L::kFull, st);
+                    if (boxes > 0)
+                        mbar_arrive_tx(full, static_cast<uint32_t>(boxes * L::kSegs * 2 * br * L::kSeg));
+                    else
+                        mbar_arrive(full);
+                    ++issued;
+                }
+            }
+            aborted = __shfl_sync(0xFFFFFFFFu, aborted, 0);
+            if (aborted) break;
+            if (good) {
+                const uint32_t full = bar(L::kFull, st);
+                const uint32_t dst = base + L::kStage + st * L::kStageBytes + side +
+                                     static_cast<uint32_t>(p * br * L::kSeg);
+#pragma unroll
+                for (int sgi = 0; sgi < L::kSegs; ++sgi)
+                    tma_load_3d(dst + static_cast<uint32_t>(sgi * kPfKeys * L::kSeg), map, 0,
+                                kvh * L::kSegs + sgi, row, full);
+            }
+        }
+        if (aborted && lane == 0) {
+            flag(a.status, KVFP8_DEV_TIMEOUT);
+            *abort_flag = 1;
+            for (int k = max(0, issued - L::kNS); k < issued; ++k)
+                mbar_wait(bar(L::kFull, k % L::kNS), (k / L::kNS) & 1, &never);
+        }
+    }
+    else if (warp == kP2MmaWarp) {
+        // ------------------------------------------------------------ tensor-core issue
+        // Tile i: S[r][i%2] = Q[r].K(i)^T for both row tiles, then O[r] += P[r](i-1).V(i-1).
+        // S[r][j] may be overwritten once O[r] of the tile two back (which read P from it)
+        // has completed: o_done[r][j].
+        if (lane == 0) {
+            const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, HD);
+            int o_issued = 0;
+            bool ok = true;
+            auto issue_o = [&](int t) {
+                const int b = t % L::kNB, j = t & 1;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (!mbar_wait(bar(L::kPReady, 2 * r + j), (t >> 1) & 1, abort_flag)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < kPfKeys / 16; ++k)
+                        umma_ts(tmem + L::col_o(r), tmem + L::col_s(r, j) + 8 * k,
+                                sw128_desc(base + L::kV + b * L::kVBuf + k * 32), idesc_o,
+                                (t > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(bar(L::kODone, 2 * r + j));
+                }
+                umma_commit(bar(L::kKvFree, b));
+                ++o_issued;
+                return true;
+            };
+            for (int i = 0; i < ntiles && ok; ++i) {
+                const int b = i % L::kNB, j = i & 1;
+                ok = mbar_wait(bar(L::kKvReady, b), (i / L::kNB) & 1, abort_flag);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (ok && i >= 2)
+                        ok = mbar_wait(bar(L::kODone, 2 * r + j), ((i >> 1) & 1) ^ 1u, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < HD / 16; ++k) {
+                        const uint64_t ad = sw128_desc(base + L::kQ + r * L::kQTile +
+                                                       (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
+                        const uint64_t bd = sw128_desc(base + L::kK + b * L::kKBuf +
+                                                       (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
+                        umma_ss(tmem + L::col_s(r, j), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(bar(L::kSReady, 2 * r + j));
+                }
+                if (ok && i >= 1) ok = issue_o(i - 1);
+            }
+            if (ok) ok = issue_o(ntiles - 1);
+            if (!ok) {
+                flag(a.status, KVFP8_DEV_TIMEOUT);
+                *abort_flag = 1;
+                // let products already issued finish before tensor memory is released
+                if (o_issued > 0) {
+                    const int t = o_issued - 1;
+                    mbar_wait(bar(L::kKvFree, t % L::kNB), (t / L::kNB) & 1, &never);
+                }
+            }
+        }
+    }
+    else if (warp >= 8) {
+        // ------------------------------------------------------------ conversion warps
+        const int ct = tid - 256;  // 0 .. 32*kP2ConvWarps-1
+        constexpr int kCT = 32 * kP2ConvWarps;
+        // q rows -> f16, 128-byte-swizzled K-major blocks of 64 head dims: rows ct and ct+128
+#pragma unroll 1
+        for (int rr = ct; rr < kP2Rows; rr += kCT) {
+            const int r = row0 + rr;
+            const bool row_ok = r < nb * G;
+            const int jq = row_ok ? r / G : 0, gq = row_ok ? r % G : 0;
+            const __nv_bfloat16 *qrow =
+                a.query + ((static_cast<int64_t>(qr.q0) + jq) * a.n_q + kvh * G + gq) * HD;
+            uint8_t *qt = bp + L::kQ + (rr / kPfRows) * L::kQTile;
+            const int lr = rr % kPfRows;
+#pragma unroll 4
+            for (int c = 0; c < HD / 8; ++c) {
+                uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + 8 * c);
+                uint4 h;
+                h.x = f16x2_from_f32(bf16lo(w.x), bf16hi(w.x));
+                h.y = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
+                h.z = f16x2_from_f32(bf16lo(w.z), bf16hi(w.z));
+                h.w = f16x2_from_f32(bf16lo(w.w), bf16hi(w.w));
+                *reinterpret_cast<uint4 *>(qt + (c >> 3) * (kPfRows * 128) + sw128(lr, c & 7)) = h;
+            }
+        }
+        constexpr int kKT = kPfKeys * (HD / 16) / kCT;                   // K tasks per thread
+        constexpr int kVB = (kPfKeys / 8) * (HD / 32) / kP2ConvWarps;    // V^T blocks per warp
+        constexpr int kVG = kVB < 4 ? kVB : 4;                           // V^T blocks per round
+        const int w8 = warp - 8;
+        const uint32_t vsel = static_cast<uint32_t>(2 * (lane & 3)) | static_cast<uint32_t>(2 * (lane & 3) + 1) << 4;
+        bool ok = true;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int st = i % L::kNS, b = i % L::kNB;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kFull, st), (i / L::kNS) & 1, abort_flag));
+            // the buffer's previous tile (i-NB) has been through every product
+            if (ok)
+                ok = __all_sync(0xFFFFFFFFu,
+                                mbar_wait(bar(L::kKvFree, b), ((i / L::kNB) & 1) ^ 1u, abort_flag));
+            if (!ok) break;
+            const uint64_t mask = meta[st];
+            const uint8_t *kst = bp + L::kStage + st * L::kStageBytes;
+            const uint8_t *vst = kst + kPfKeys * HD;
+            uint8_t *kdst0 = bp + L::kK + b * L::kKBuf;
+            const uint32_t vbase = base + L::kV + b * L::kVBuf;
+            // every load of a round before its conversions (as in prefill_kernel)
+            uint4 kw[kKT];
+            uint4 vw[kVG][2];
+            auto v_load = [&](int g0) {
+#pragma unroll
+                for (int q = 0; q < kVG; ++q) {
+                    const int blk = w8 + (g0 + q) * kP2ConvWarps;
+                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
+                    const int key = ko * 8 + (lane >> 2);
+                    const int sgi = (32 * dg) / L::kSeg, cc = ((32 * dg) % L::kSeg) >> 4;
+                    const uint8_t *vrow = vst + sgi * kPfKeys * L::kSeg;
+                    vw[q][0] = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc));
+                    vw[q][1] = *reinterpret_cast<const uint4 *>(vrow + swz<L::kSeg>(key, cc + 1));
+                    if (!((mask >> key) & 1ull)) vw[q][0] = vw[q][1] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            };
+            auto v_store = [&](int g0) {
+#pragma unroll
+                for (int q = 0; q < kVG; ++q) {
+                    const int blk = w8 + (g0 + q) * kP2ConvWarps;
+                    const int ko = blk % (kPfKeys / 8), dg = blk / (kPfKeys / 8);
+                    const uint4 lo = vw[q][0], hi = vw[q][1];
+                    const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    uint32_t rv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)  // bytes 8e + 2(t%4), +1 of the key's 32
+                        rv[e] = f16x2_from_e4m3x2(__byte_perm(wd[2 * e], wd[2 * e + 1], vsel));
+                    const int n = 32 * dg + 8 * (lane >> 3) + (lane & 7);
+                    stsm_x4_t(vbase + sw128(n, ko), rv[0], rv[1], rv[2], rv[3]);
+                }
+            };
+#pragma unroll
+            for (int q = 0; q < kKT; ++q) {
+                const int task = ct + q * kCT;
+                const int key = task / (HD / 16), c = task % (HD / 16);
+                const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
+                kw[q] = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
+                                                         swz<L::kSeg>(key, within >> 4));
+                if (!((mask >> key) & 1ull)) kw[q] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            v_load(0);
+#pragma unroll
+            for (int q = 0; q < kKT; ++q) {
+                const int task = ct + q * kCT;
+                const int key = task / (HD / 16), c = task % (HD / 16);
+                const uint4 w = kw[q];
+                uint4 h0, h1;
+                h0.x = f16x2_from_e4m3x2(w.x);
+                h0.y = f16x2_from_e4m3x2_hi(w.x);
+                h0.z = f16x2_from_e4m3x2(w.y);
+                h0.w = f16x2_from_e4m3x2_hi(w.y);
+                h1.x = f16x2_from_e4m3x2(w.z);
+                h1.y = f16x2_from_e4m3x2_hi(w.z);
+                h1.z = f16x2_from_e4m3x2(w.w);
+                h1.w = f16x2_from_e4m3x2_hi(w.w);
+                const int kb = (16 * c) / 64, c8 = ((16 * c) % 64) / 8;
+                uint8_t *kdst = kdst0 + kb * (kPfKeys * 128);
+                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
+                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
+            }
+            v_store(0);
+#pragma unroll
+            for (int g0 = kVG; g0 < kVB; g0 += kVG) {
+                v_load(g0);
+                v_store(g0);
+            }
+            if (ct == 0) buf_mask[b] = mask;  // for the softmax warps, released with kv_ready
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar(L::kEmpty, st));
+                mbar_arrive(bar(L::kKvReady, b));
+            }
+        }
+        if (!ok && lane == 0) {
+            flag(a.status, KVFP8_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    else {
+        // ------------------------------------------------------------ softmax warps
+        const int rt = warp >> 2;                   // row tile 0 or 1
+        const int r = row0 + tid;                   // this thread's score row
+        const bool row_ok = r < nb * G;
+        const int jq = row_ok ? r / G : 0, gq = row_ok ? r % G : 0;
+        const int pos = Ls - nb + jq;               // last key position the row may see
+        const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        float m_used = -INFINITY, la = 0.f, lb = 0.f;  // running maximum, row sum in two halves
+        bool ok = true;
+        for (int i = 0; i < ntiles && ok; ++i) {
+            const int b = i % L::kNB, j = i & 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kSReady, 2 * rt + j), (i >> 1) & 1, abort_flag));
+            // the tile's valid-key mask (already complete: S(i) needed the same phase)
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvReady, b), (i / L::kNB) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t mask = buf_mask[b];
+            const uint32_t scol = lane_addr + L::col_s(rt, j);
+            uint32_t s[2][32];
+            tmem_ld32(scol, s[0]);
+            tmem_ld32(scol + 32, s[1]);
+            tmem_wait_ld();
+            const int k0 = key_tile(i) * kPfKeys;
+            const int vis_n = row_ok ? min(kPfKeys, max(0, pos - k0 + 1)) : 0;
+            const uint64_t vis = mask & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
+            float mx, mult;
+            if (__all_sync(0xFFFFFFFFu, vis == ~0ull)) {
+                mx = (score_scale >= 0.f ? extreme64<true>(s) : extreme64<false>(s)) * score_scale;
+                mult = score_scale;
+            } else {
+                mx = -INFINITY;
+                mult = 1.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float v = ((vis >> (32 * h + c)) & 1ull)
+                                            ? __uint_as_float(s[h][c]) * score_scale
+                                            : -INFINITY;
+                        s[h][c] = __float_as_uint(v);
+                        mx = fmaxf(mx, v);
+                    }
+            }
+            float factor = 1.f;
+            if (mx > -INFINITY) {
+                if (m_used == -INFINITY) {
+                    m_used = mx;
+                } else if (mx > m_used + 8.f) {
+                    factor = ex2(m_used - mx);
+                    m_used = mx;
+                }
+            }
+            if (__any_sync(0xFFFFFFFFu, factor != 1.f)) {
+                // O[rt] of the previous tile must be complete before it is rescaled
+                const int t = i - 1;
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, 2 * rt + (t & 1)), (t >> 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                la *= factor;
+                lb *= factor;
+#pragma unroll 1
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_addr + L::col_o(rt) + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
+                    tmem_st32(lane_addr + L::col_o(rt) + c0, o);
+                }
+            }
+            uint32_t p[32];
+            const float msub = m_used == -INFINITY ? 0.f : m_used;
+            const uint64_t mul2 = pk2(mult, mult), sub2 = pk2(-msub, -msub);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const int h = c >> 4, e = (2 * c) & 31;
+                const float2 x = upk2(fma_f32x2(pk2u(s[h][e], s[h][e + 1]), mul2, sub2));
+                p[c] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
+            }
+            tmem_st32(scol, p);
+            // the row sum: pairs of P added in f16 (one rounding on values <= 2^9), then fp32
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+                uint32_t h2;
+                asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h2) : "r"(p[c]), "r"(p[c + 1]));
+                la += f16lo_f32(h2);
+                lb += f16hi_f32(h2);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::kPReady, 2 * rt + j));
+        }
+        if (ok) {
+            const int t = ntiles - 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, 2 * rt + (t & 1)), (t >> 1) & 1, abort_flag));
+        }
+        if (ok) {
+            tc_fence_after();
+            const float lsum = la + lb;
+            const float inv = lsum > 0.f ? sv / lsum : 0.f;
+            uint4 *orow = reinterpret_cast<uint4 *>(
+                a.out + ((static_cast<int64_t>(qr.q0) + jq) * a.n_q + kvh * G + gq) * HD);
+#pragma unroll 1
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + L::col_o(rt) + c0, o);
+                tmem_wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 w;
+                        w.x = bf16x2_from_f32(__uint_as_float(o[c]) * inv, __uint_as_float(o[c + 1]) * inv);
+                        w.y = bf16x2_from_f32(__uint_as_float(o[c + 2]) * inv, __uint_as_float(o[c + 3]) * inv);
+                        w.z = bf16x2_from_f32(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv);
+                        w.w = bf16x2_from_f32(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv);
+                        orow[(c0 + c) / 8] = w;
+                    }
+                }
+            }
+        } else if (lane == 0) {
+            flag(a.status, KVFP8_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kP2MmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
 template <int HD>
 cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     using L = PfSmem<HD>;
@@ -762,11 +1284,6 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     if ((err = encode_cache_map(&tmk, d.key_cache, rows, row_bytes, L::kSeg, box_rows)) != cudaSuccess)
         return err;
     if ((err = encode_cache_map(&tmv, d.value_cache, rows, row_bytes, L::kSeg, box_rows)) != cudaSuccess)
-        return err;
-    const size_t smem = L::kTotal + 1024;
-    auto kern = prefill_kernel<HD>;
-    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem))) != cudaSuccess)
         return err;
     PrefillArgs a;
     a.out = static_cast<__nv_bfloat16 *>(d.out);
@@ -790,6 +1307,25 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     a.scale_dtype = d.scale_dtype;
     a.status = d.status;
     a.box_rows = box_rows;
+    // more than one tile of 128 rows per kv head (a multi-query call): 256 rows per CTA
+    if constexpr (HD <= 128) {
+        if (d.qsl != nullptr && d.qmax * a.group > kPfRows) {
+            const size_t smem2 = Pf2Smem<HD>::kTotal + 1024;
+            auto kern2 = prefill2_kernel<HD>;
+            if ((err = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem2))) != cudaSuccess)
+                return err;
+            a.row_tiles = (d.qmax * a.group + kP2Rows - 1) / kP2Rows;
+            const int64_t ctas = static_cast<int64_t>(d.num_seqs) * a.row_tiles * d.n_kv;
+            kern2<<<static_cast<unsigned>(ctas), kP2Warps * 32, smem2, stream>>>(tmk, tmv, a);
+            return cudaGetLastError();
+        }
+    }
+    const size_t smem = L::kTotal + 1024;
+    auto kern = prefill_kernel<HD>;
+    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem))) != cudaSuccess)
+        return err;
     a.row_tiles = (d.qmax * a.group + kPfRows - 1) / kPfRows;
     const int64_t ctas = static_cast<int64_t>(d.num_seqs) * a.row_tiles * d.n_kv;
     kern<<<static_cast<unsigned>(ctas), kPfWarps * 32, smem, stream>>>(tmk, tmv, a);
