@@ -7,6 +7,10 @@
 // format).  The decode kernel covers up to 16 (query token, head) score columns per kv
 // head; past that the rows form a real M dimension and the contraction is dense, so:
 //
+// Two kernels: prefill_kernel below (one row tile of 128 per CTA), and prefill2_kernel
+// further down (two row tiles per CTA sharing each converted K/V tile), which takes the
+// long chunks at head_dim 64 and 128.
+//
 //  * Work unit: one CTA per (sequence, kv head, tile of 128 score rows).  A row is a
 //    (query token j, head g of the kv head's group) pair, row = j*G + g, so all rows of a
 //    tile share one K/V stream.  Keys are visited in tiles of 64 up to the tile's last

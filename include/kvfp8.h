@@ -252,7 +252,8 @@ KVFP8_API kvfp8_status kvfp8_paged_decode_attention_noalloc(
  * kv head (<= 8 at head_dim 256) the split-KV decode kernel runs and needs the workspace
  * below.  Every other shape (long query chunks,
  * prefill) runs on the tensor cores (tcgen05, accumulators in tensor memory), one CTA per
- * 128 (query token, head) rows of a kv head, with no workspace; it needs
+ * 128 (query token, head) rows of a kv head (256 rows, as two tiles sharing each K/V tile,
+ * when there are more than 128 rows at head_dim 64 or 128), with no workspace; it needs
  * n_q / n_kv <= 128 and num_seqs * n_kv * ceil(max_query_len * (n_q / n_kv) / 128) < 2^31
  * CTAs, else KVFP8_ERR_UNSUPPORTED.
  *
