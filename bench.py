@@ -6,8 +6,13 @@ kvfp8_paged_decode_attention of one query per sequence over that cache.  The met
 achieved HBM bandwidth: algorithmic bytes (each input byte read once, each output byte
 written once) divided by device time, in GB/s.
 
-Default workload: llama3_8b (32 q / 8 kv heads, head_dim 128, block 16, 64 sequences x
-4096 tokens; the step writes all 262144 context rows and decodes 64 queries).
+Default workload: long_context, the largest configuration (64 q / 8 kv heads, head_dim 128,
+block 16, 8 sequences of 32768-131072 tokens; the step writes all ~655k context rows and
+decodes 8 queries).  In the same run (unless --per-config off), the other timed
+configurations are measured the same way and reported under "per_config":
+  llama3_8b      write 262144 context rows, then decode 64 queries
+  prefill_write  write 32768 rows (padding rows skipped)
+  mixed_serving  write 1 new token per sequence, then decode 256 queries
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                   [--variant fp8|rope|k_bf16|v_bf16|multi]
@@ -25,6 +30,12 @@ Default workload: llama3_8b (32 q / 8 kv heads, head_dim 128, block 16, 64 seque
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas, weak
 scaling, no collective on the data path); the time is the max over ranks.
+
+Timing: W warm-up steps, a short untimed soak, then K steps bracketed by events on the
+launching stream.  Just before the first timed step a GPU-side wait of a few milliseconds
+is enqueued (outside the timed region), so the host has queued every timed launch before
+the GPU reaches them: the steps run back to back and no host enqueue gap falls inside an
+event interval.
 """
 from __future__ import annotations
 
@@ -60,6 +71,9 @@ VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi", "prefill")
 # last m of a sequence's new tokens (a 512-token chunk over a 128K context would otherwise
 # take the double-precision oracle most of an hour)
 SAMPLE_QUERY_FLOPS = 1 << 28
+# a CPU sample takes at most this many tokens of a sequence (its first ones), so that one
+# sample of a 128K-token context stays near a second of oracle time
+SAMPLE_MAX_TOKENS = 8192
 METRIC = "FP8 paged decode attn KV-read GB/s & cache-write GB/s, % of GB300 HBM peak"
 
 
@@ -355,9 +369,12 @@ class Problem:
                 ins.append(self.qsl)
         return ins
 
+    def attention_launches(self) -> int:
+        # plan + split-KV attention + combine, or one tensor-core attention kernel
+        return (1 if self.tensor_route else 3) if self.decode else 0
+
     def launches_per_step(self) -> int:
-        # write; then plan + split-KV attention + combine, or one tensor-core attention kernel
-        return 1 + ((1 if self.tensor_route else 3) if self.decode else 0)
+        return 1 + self.attention_launches()
 
     def describe(self) -> dict:
         w, lay = self.w, self.lay
@@ -394,10 +411,15 @@ class Problem:
 
 # ----------------------------------------------------------------- timed runs
 
-def run_ours(args, rank, world, device):
-    import fp8_paged_kv_reshape_gb300 as kv  # noqa: F401  (fails loudly without the library)
+NOMINAL_HBM_GBS = 8000.0  # the GB300's ~8 TB/s HBM3e figure, for context beside the measured peak
+PER_CONFIG = ("llama3_8b", "prefill_write", "mixed_serving")
+CLOCK_HZ = 2.07e9  # the GB300's maximum SM clock, for sizing the pre-timing GPU wait
 
-    p = Problem(args.workload, device, args.num_seqs, args.variant)
+
+def time_problem(p: "Problem", args, world, device) -> dict:
+    """Time K steps of one problem (after W warm-up steps and a short soak) with CUDA events
+    on the launching stream: the whole timed region, and each kernel group inside every step.
+    Returns the slowest rank's total and this rank's per-kernel means."""
     per_step = p.rs_bytes + p.dec_bytes
     flush = None if per_step > L2_BYTES else torch.empty(2 * L2_BYTES, dtype=torch.uint8,
                                                          device=device)
@@ -422,17 +444,26 @@ def run_ours(args, rank, world, device):
     assert int(p.status.item()) == 0, "device status set during warm-up"
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
-    # keep the GPU busy for ~0.5 s before timing so the sampler sees it under load
+    # keep the GPU busy for ~0.5 s before timing so the sampler sees it under load; measure
+    # the host's cost of enqueueing one step on the way
+    host = []
     t_end = time.time() + 0.5
     while time.time() < t_end:
+        h0 = time.perf_counter()
         step()
+        host.append(time.perf_counter() - h0)
         torch.cuda.synchronize(device)
+    host_s = statistics.median(host) if host else 1e-4
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
+    # a GPU-side wait, outside the timed region, long enough for the host to queue every
+    # timed launch first: the timed steps then run back to back on the device
+    wait_s = min(0.25, 2.0 * args.steps * (host_s + 20e-6) + 1e-3)
+    torch.cuda._sleep(int(wait_s * CLOCK_HZ))
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
@@ -445,27 +476,26 @@ def run_ours(args, rank, world, device):
     rs_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps if p.decode else 0.0
     assert int(p.status.item()) == 0, "device status set during the timed steps"
-
     total_ms = max_over_ranks(total_ms, world, device)
-    e2e = run_e2e(args, p, device) if not args.no_e2e else None
-    if e2e is not None:
-        e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, device)
-        e2e["value"] = whole_job_gbs(per_step, 1, world, e2e["ms_per_step"])
+    return {"total_ms": total_ms, "rs_ms": rs_ms, "dec_ms": dec_ms,
+            "host_enqueue_ms_per_step": host_s * 1e3, "clocks": sampler.summary()}
 
-    if rank != 0:
-        return None
+
+def kernel_report(p: "Problem", t: dict, workload: str, variant: str):
+    """Per-kernel-group bytes, event-timed ms, GB/s and fractions (of the measured HBM peak
+    and of the nominal 8 TB/s), and the dominant kernel's roofline object."""
     peak, peak_kind = measured_peaks()
-    kernels = {"reshape_and_cache": {"bytes_per_launch": p.rs_bytes, "ms": rs_ms,
-                                     "gbs": p.rs_bytes / (rs_ms * 1e-3) / 1e9}}
+    kernels = {"reshape_and_cache": {"bytes_per_launch": p.rs_bytes, "ms": t["rs_ms"],
+                                     "gbs": p.rs_bytes / (t["rs_ms"] * 1e-3) / 1e9}}
     if p.decode:
-        kernels["paged_decode_attention"] = {"bytes_per_launch": p.dec_bytes, "ms": dec_ms,
-                                             "gbs": p.dec_bytes / (dec_ms * 1e-3) / 1e9,
-                                             "launches": 1 if p.tensor_route else 3}
+        kernels["paged_decode_attention"] = {"bytes_per_launch": p.dec_bytes, "ms": t["dec_ms"],
+                                             "gbs": p.dec_bytes / (t["dec_ms"] * 1e-3) / 1e9,
+                                             "launches": p.attention_launches()}
     for k in kernels.values():
         k["frac"] = k["gbs"] / peak
+        k["frac_of_nominal_8tbs"] = k["gbs"] / NOMINAL_HBM_GBS
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
-    traffic = recorded_traffic(dom, args.workload if args.variant == "fp8"
-                               else "%s:%s" % (args.workload, args.variant))
+    traffic = recorded_traffic(dom, workload if variant == "fp8" else "%s:%s" % (workload, variant))
     if p.decode and p.tensor_route:
         att = kernels["paged_decode_attention"]
         att["tflops"] = p.attn_flops / (att["ms"] * 1e-3) / 1e12
@@ -480,8 +510,59 @@ def run_ours(args, rank, world, device):
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": kernels[dom]["gbs"] / peak,
+                "frac_of_nominal_8tbs": kernels[dom]["gbs"] / NOMINAL_HBM_GBS,
                 "traffic": traffic,
                 "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
+    return kernels, roof
+
+
+def run_per_config(args, world, device) -> dict:
+    """The other timed configurations, each measured exactly as the main one (own warm-up,
+    soak, clock samples and event timing); one problem on the device at a time."""
+    res = {}
+    for name in PER_CONFIG:
+        if name == args.workload:
+            continue
+        p = Problem(name, device, None, "fp8")
+        t = time_problem(p, args, world, device)
+        kernels, roof = kernel_report(p, t, name, "fp8")
+        per_step = p.rs_bytes + p.dec_bytes
+        res[name] = {"value": whole_job_gbs(per_step, args.steps, world, t["total_ms"]),
+                     "unit": "GB/s", "ms_per_step": t["total_ms"] / args.steps,
+                     "config": p.describe(), "kernels": kernels, "roofline": roof,
+                     "gpu_launches": p.launches_per_step() * args.steps,
+                     "host_enqueue_ms_per_step": t["host_enqueue_ms_per_step"],
+                     "clocks": t["clocks"]}
+        del p
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, device):
+    import fp8_paged_kv_reshape_gb300 as kv  # noqa: F401  (fails loudly without the library)
+
+    p = Problem(args.workload, device, args.num_seqs, args.variant)
+    per_step = p.rs_bytes + p.dec_bytes
+    t = time_problem(p, args, world, device)
+    total_ms = t["total_ms"]
+    e2e = run_e2e(args, p, device) if not args.no_e2e else None
+    if e2e is not None:
+        e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, device)
+        e2e["value"] = whole_job_gbs(per_step, 1, world, e2e["ms_per_step"])
+    kernels, roof = kernel_report(p, t, args.workload, args.variant)
+    describe = p.describe()
+    launches = p.launches_per_step() * args.steps
+    del p
+    torch.cuda.empty_cache()
+    per_config = None
+    want_per_config = args.per_config == "on" or (
+        args.per_config == "auto" and args.workload == "long_context" and args.variant == "fp8"
+        and args.num_seqs is None)
+    if want_per_config:
+        per_config = run_per_config(args, world, device)
+
+    if rank != 0:
+        return None
     value = whole_job_gbs(per_step, args.steps, world, total_ms)
     line = {
         "metric": METRIC,
@@ -491,10 +572,13 @@ def run_ours(args, rank, world, device):
         "compute": "f32 divide + E4M3 encode; fp16 (bf16 for a bf16 cache side) mma.sync "
                    "with f32 accumulate",
         "data": "synthetic (seeded; see workloads/)",
-        "config": p.describe(), "roofline": roof, "kernels": kernels,
-        "gpu_launches": p.launches_per_step() * args.steps,
-        "clocks": sampler.summary(), "e2e": e2e,
+        "config": describe, "roofline": roof, "kernels": kernels,
+        "gpu_launches": launches,
+        "host_enqueue_ms_per_step": t["host_enqueue_ms_per_step"],
+        "clocks": t["clocks"], "e2e": e2e,
     }
+    if per_config is not None:
+        line["per_config"] = per_config
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, target_s=args.cpu_seconds,
                                             variant=args.variant)
@@ -552,23 +636,29 @@ def sampled_queries(w: workloads.Workload, qlen: int, seq_len: int) -> int:
 
 
 def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_all, q,
-                   variant: str = "fp8"):
+                   variant: str = "fp8", max_tokens: int | None = SAMPLE_MAX_TOKENS):
     """Run the CPU oracle on the given sequences of the workload in the given variant: write
-    their rows into a cache, then attend with every head of them.  The multi-query forms
-    attend with the last m of each sequence's qlen new tokens (sampled_queries; token j of
-    those m sees the same keys as in the full chunk) and are credited m/qlen of the
-    sequences' attention bytes.  Returns (seconds, algorithmic bytes)."""
+    their rows into a cache, then attend with every head of them.  A sequence longer than
+    max_tokens is sampled as its first max_tokens tokens (a shorter sequence of the same
+    workload: written, then attended over whole).  The multi-query forms attend with the
+    last m of each sequence's qlen new tokens (sampled_queries; token j of those m sees the
+    same keys as in the full chunk) and are credited m/qlen of the sequences' attention
+    bytes.  Returns (seconds, algorithmic bytes)."""
     import oracle
 
     ks = workloads.stored_scale(w.k_scale, w.scale_dtype)
     vs = workloads.stored_scale(w.v_scale, w.scale_dtype)
     rows = np.nonzero(np.isin(lay.row_seq, seqs))[0] if lay.row_seq.size else np.zeros(0, int)
+    if max_tokens is not None:
+        rows = rows[lay.row_pos[rows] < max_tokens]
     kh = k_all[torch.from_numpy(rows)].contiguous()
     vh = v_all[torch.from_numpy(rows)].contiguous()
     pos = np.maximum(lay.row_pos[rows], 0).astype(np.int64)
     # the sampled sequences' physical blocks, relabelled 0..n-1 into a pool of their own
     # (the store and the attention do not depend on which physical block holds a page)
     bt_full = lay.block_tables[seqs]
+    if max_tokens is not None:
+        bt_full = bt_full[:, :-(-max_tokens // w.block_size)]
     used = np.unique(bt_full[bt_full >= 0])
     relabel = np.full(lay.num_blocks, -1, np.int64)
     relabel[used] = np.arange(used.size)
@@ -585,6 +675,8 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
              oracle.E4M3 if v_elem == 1 else oracle.CACHE_BF16)
     decode = w.kind != "write"
     sub_lens = lay.seq_lens[seqs]
+    if max_tokens is not None:
+        sub_lens = np.minimum(sub_lens, max_tokens).astype(np.int32)
     qlen = query_len(w, variant, lay.seq_lens)
     m = sampled_queries(w, qlen, int(sub_lens.max())) if variant in ("multi", "prefill") else qlen
     seq_idx = np.asarray(seqs)
@@ -622,15 +714,22 @@ def _oracle_sample(w: workloads.Workload, lay: workloads.Layout, seqs, k_all, v_
     return dt, nbytes
 
 
+def _cap_note(lay: workloads.Layout) -> str:
+    if int(lay.seq_lens.max()) <= SAMPLE_MAX_TOKENS:
+        return ""
+    return "; a sequence longer than %d tokens is sampled as its first %d" % (
+        SAMPLE_MAX_TOKENS, SAMPLE_MAX_TOKENS)
+
+
 def _query_note(w: workloads.Workload, lay: workloads.Layout, variant: str) -> str:
     if variant not in ("multi", "prefill"):
-        return ""
+        return _cap_note(lay)
     qlen = query_len(w, variant, lay.seq_lens)
-    lo = sampled_queries(w, qlen, int(lay.seq_lens.max()))
-    hi = sampled_queries(w, qlen, int(lay.seq_lens.min()))
+    lo = sampled_queries(w, qlen, min(int(lay.seq_lens.max()), SAMPLE_MAX_TOKENS))
+    hi = sampled_queries(w, qlen, min(int(lay.seq_lens.min()), SAMPLE_MAX_TOKENS))
     return ("; attention for the last %s of each sampled sequence's %d new tokens (at most "
-            "2^28 oracle FLOPs), credited that fraction of its attention bytes"
-            % (str(lo) if lo == hi else "%d-%d" % (lo, hi), qlen))
+            "2^28 oracle FLOPs), credited that fraction of its attention bytes%s"
+            % (str(lo) if lo == hi else "%d-%d" % (lo, hi), qlen, _cap_note(lay)))
 
 
 @functools.lru_cache(maxsize=2)
@@ -680,14 +779,15 @@ def cpu_baseline_all_cores(name: str, target_s: float = 4.0, variant: str = "fp8
     nb = sum(r[0] for r in res)
     n = sum(r[1] for r in res)
     return {"value": nb / wall / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "%d whole-sequence samples of %s, variant %s, on %d threads (one sample "
+            "sample": "%d sequence samples of %s, variant %s, on %d threads (one sample "
                       "per thread at a time), %.1f s wall%s"
                       % (n, name, variant, cores, wall, _query_note(w, lay, variant))}
 
 
 def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dict:
     """The oracle as it stands, single-threaded on the host, on a bounded sample of the same
-    workload (whole sequences: their rows written, then every head attended)."""
+    workload (sequences, at most their first SAMPLE_MAX_TOKENS tokens: their rows written,
+    then every head attended)."""
     w, lay, k, v, q = _cpu_inputs(name, variant)
     order = np.random.Generator(np.random.PCG64(w.seed + 5)).permutation(lay.num_seqs)
     t, nb, used = 0.0, 0, []
@@ -701,13 +801,15 @@ def cpu_baseline(name: str, target_s: float = 12.0, variant: str = "fp8") -> dic
     return {"value": nb / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": "%d of %d sequences of %s (%d tokens), variant %s: oracle write of their "
                       "rows + attention for all %d heads, %.1f s single-threaded%s"
-                      % (len(used), lay.num_seqs, name, int(lay.seq_lens[used].sum()), variant,
+                      % (len(used), lay.num_seqs, name,
+                         int(np.minimum(lay.seq_lens[used], SAMPLE_MAX_TOKENS).sum()), variant,
                          w.n_q, t, _query_note(w, lay, variant))}
 
 
 def run_reference(args):
     """The CPU oracle timed on the host cores on this arm's workload and metric: each step
-    is a bounded sample (one sequence, its rows written and all heads decoded)."""
+    is a bounded sample (one sequence, at most its first SAMPLE_MAX_TOKENS tokens, its rows
+    written and all heads decoded)."""
     w, lay, k, v, q = _cpu_inputs(args.workload, args.variant)
     order = np.random.Generator(np.random.PCG64(w.seed + 6)).permutation(lay.num_seqs)
     for i in range(args.warmup):
@@ -745,10 +847,13 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama3_8b", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default="long_context", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--variant", default="fp8", choices=VARIANTS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--per-config", choices=["auto", "on", "off"], default="auto",
+                    help="also time llama3_8b, prefill_write and mixed_serving (auto: with the "
+                         "default long_context workload)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="fewer sequences than the workload names (small profiling cases)")

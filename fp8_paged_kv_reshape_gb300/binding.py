@@ -216,13 +216,22 @@ def paged_decode_workspace_size(num_seqs: int, n_q: int, head_dim: int) -> int:
     return int(LIB.kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim))
 
 
-def paged_decode_attention(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
-                           block_tables: torch.Tensor, seq_lens: torch.Tensor,
-                           k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None,
-                           sm_scale: float = 0.0, out: torch.Tensor | None = None,
-                           workspace: torch.Tensor | None = None,
-                           status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """kvfp8_paged_decode_attention on torch tensors; returns out (bf16 [num_seqs, n_q, hd])."""
+def _check_tables(block_tables: torch.Tensor, seq_lens: torch.Tensor, num_seqs: int):
+    """block_tables int32 [num_seqs, max_blocks] and seq_lens int32 [num_seqs], contiguous:
+    the kernels index both for every sequence, so a short or int64 tensor would be read out
+    of bounds (or as the halves of 64-bit words)."""
+    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
+            block_tables.shape[0] != num_seqs or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks] tensor")
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != num_seqs or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be a contiguous int32 [num_seqs] tensor")
+
+
+def _check_decode_args(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                       block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                       out: torch.Tensor | None):
+    """The argument checks every single-query decode wrapper makes; returns
+    (num_seqs, n_q, head_dim, num_blocks, block_size, n_kv)."""
     if query.dtype != torch.bfloat16 or query.dim() != 3 or not query.is_contiguous():
         raise ValueError("query must be a contiguous bf16 [num_seqs, n_q, head_dim] tensor")
     num_seqs, n_q, hd = query.shape
@@ -232,11 +241,22 @@ def paged_decode_attention(query: torch.Tensor, key_cache: torch.Tensor, value_c
     if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
         raise ValueError("caches must be contiguous")
     num_blocks, bs, n_kv, _ = key_cache.shape
-    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
-            block_tables.shape[0] != num_seqs or not block_tables.is_contiguous():
-        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks] tensor")
-    if seq_lens.dtype != torch.int32 or seq_lens.numel() != num_seqs or not seq_lens.is_contiguous():
-        raise ValueError("seq_lens must be a contiguous int32 [num_seqs] tensor")
+    _check_tables(block_tables, seq_lens, num_seqs)
+    if out is not None and (out.dtype != torch.bfloat16 or out.shape != query.shape or
+                            not out.is_contiguous()):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like query")
+    return num_seqs, n_q, hd, num_blocks, bs, n_kv
+
+
+def paged_decode_attention(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                           block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                           k_scale: torch.Tensor | None = None, v_scale: torch.Tensor | None = None,
+                           sm_scale: float = 0.0, out: torch.Tensor | None = None,
+                           workspace: torch.Tensor | None = None,
+                           status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvfp8_paged_decode_attention on torch tensors; returns out (bf16 [num_seqs, n_q, hd])."""
+    num_seqs, n_q, hd, num_blocks, bs, n_kv = _check_decode_args(
+        query, key_cache, value_cache, block_tables, seq_lens, out)
     if out is None:
         out = torch.empty_like(query)
     need = paged_decode_workspace_size(num_seqs, n_q, hd)
@@ -272,12 +292,16 @@ def paged_attention_multi(query: torch.Tensor, query_start_loc: torch.Tensor, ma
         raise ValueError("query must be a contiguous bf16 [rows, n_q, head_dim] tensor")
     rows, n_q, hd = query.shape
     num_seqs = seq_lens.numel()
-    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != num_seqs + 1:
-        raise ValueError("query_start_loc must be int32 [num_seqs + 1]")
+    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != num_seqs + 1 or \
+            not query_start_loc.is_contiguous():
+        raise ValueError("query_start_loc must be a contiguous int32 [num_seqs + 1] tensor")
     if key_cache.dtype != torch.uint8 or key_cache.shape != value_cache.shape or \
             key_cache.dim() != 4 or key_cache.shape[3] != hd:
         raise ValueError("caches must be uint8 [num_blocks, block_size, n_kv, head_dim]")
+    if not (key_cache.is_contiguous() and value_cache.is_contiguous()):
+        raise ValueError("caches must be contiguous")
     num_blocks, bs, n_kv, _ = key_cache.shape
+    _check_tables(block_tables, seq_lens, num_seqs)
     if out is None:
         out = torch.empty_like(query)
     need = paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, hd, max_query_len)
@@ -303,14 +327,10 @@ def paged_decode_attention_noalloc(query: torch.Tensor, key_cache: torch.Tensor,
                                    stream=None) -> torch.Tensor:
     """kvfp8_paged_decode_attention_noalloc: the same call with the library's fixed device
     scratch instead of a workspace, for callers that cannot allocate device memory.  Pass
-    ``out`` to keep the call free of allocations on the Python side too."""
-    if query.dtype != torch.bfloat16 or query.dim() != 3 or not query.is_contiguous():
-        raise ValueError("query must be a contiguous bf16 [num_seqs, n_q, head_dim] tensor")
-    num_seqs, n_q, hd = query.shape
-    if key_cache.dtype != torch.uint8 or key_cache.shape != value_cache.shape or \
-            key_cache.dim() != 4 or key_cache.shape[3] != hd:
-        raise ValueError("caches must be uint8 [num_blocks, block_size, n_kv, head_dim]")
-    num_blocks, bs, n_kv, _ = key_cache.shape
+    ``out`` to keep the call free of allocations on the Python side too.  The arguments are
+    checked exactly as paged_decode_attention checks them."""
+    num_seqs, n_q, hd, num_blocks, bs, n_kv = _check_decode_args(
+        query, key_cache, value_cache, block_tables, seq_lens, out)
     if out is None:
         out = torch.empty_like(query)
     sdt = _scale_args(k_scale, v_scale)
@@ -384,11 +404,7 @@ def paged_decode_attention_mixed(query: torch.Tensor, key_cache: torch.Tensor,
     if key_cache.shape[3] != hd:
         raise ValueError("caches must be [num_blocks, block_size, n_kv, head_dim]")
     num_blocks, bs, n_kv, _ = key_cache.shape
-    if block_tables.dtype != torch.int32 or block_tables.dim() != 2 or \
-            block_tables.shape[0] != num_seqs or not block_tables.is_contiguous():
-        raise ValueError("block_tables must be a contiguous int32 [num_seqs, max_blocks] tensor")
-    if seq_lens.dtype != torch.int32 or seq_lens.numel() != num_seqs or not seq_lens.is_contiguous():
-        raise ValueError("seq_lens must be a contiguous int32 [num_seqs] tensor")
+    _check_tables(block_tables, seq_lens, num_seqs)
     if out is None:
         out = torch.empty_like(query)
     need = paged_decode_workspace_size(num_seqs, n_q, hd)

@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "../../include/kvfp8.h"
+#include "kvfp8_internal.h"
 
 namespace {
 
@@ -52,14 +53,20 @@ extern "C" kvfp8_status kvfp8_paged_decode_attention_noalloc(
     int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t block_size,
     int32_t num_blocks, float sm_scale, const void *k_scale, const void *v_scale,
     kvfp8_dtype scale_dtype, uint32_t *status, kvfp8_stream_t stream) {
+    // The same argument checks, in the same order, as the workspace entry point: a call it
+    // would reject is rejected here with the same code, before the scratch is looked at.
+    bool nothing_to_do = false;
+    const kvfp8_status v = kvfp8::validate_decode(
+        out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+        n_q, n_kv, head_dim, block_size, num_blocks, sm_scale, scale_dtype, &nothing_to_do);
+    if (v != KVFP8_OK || nothing_to_do) return v;
     // A batch whose scratch would not fit the fixed array is refused before anything runs.
     if (kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim) > kScratchBytes)
         return KVFP8_ERR_WORKSPACE;
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess) return KVFP8_ERR_CUDA;
-    return kvfp8_paged_decode_attention(out, query, key_cache, value_cache, block_tables,
-                                        max_blocks_per_seq, seq_lens, num_seqs, n_q, n_kv,
-                                        head_dim, block_size, num_blocks, sm_scale, k_scale,
-                                        v_scale, scale_dtype, scratch, kScratchBytes, status,
-                                        stream);
+    return kvfp8::launch_decode_validated(out, query, key_cache, value_cache, block_tables,
+                                          max_blocks_per_seq, seq_lens, num_seqs, n_q, n_kv,
+                                          head_dim, block_size, num_blocks, sm_scale, k_scale,
+                                          v_scale, scale_dtype, scratch, status, stream);
 }

@@ -83,11 +83,10 @@ dequant_kernel(void *dst, const uint8_t *src, int64_t n, const void *scale, int 
 cudaError_t launch_dequant(void *dst, int dst_dtype, const uint8_t *src, int64_t n,
                            const void *scale, int scale_dtype, cudaStream_t stream) {
     if (n == 0) return cudaSuccess;
-    int dev = 0, sms = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    DeviceFacts f;
+    cudaError_t err = device_facts(&f);
     if (err != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return err;
+    const int sms = f.sms;
     const int64_t nvec = (n >> 4) > 0 ? (n >> 4) : 1;
     const int64_t want = (nvec + 255) / 256;
     const int blocks = static_cast<int>(want < 8LL * sms ? want : 8LL * sms);

@@ -29,6 +29,76 @@ bool block_size_ok_for_decode(int32_t bs) {
 
 }  // namespace
 
+namespace kvfp8 {
+
+kvfp8_status validate_decode(const void *out, const void *query, const uint8_t *key_cache,
+                             const uint8_t *value_cache, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                             int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, float sm_scale,
+                             int scale_dtype, bool *nothing_to_do) {
+    *nothing_to_do = false;
+    if (!dtype_ok(static_cast<kvfp8_dtype>(scale_dtype))) return KVFP8_ERR_DTYPE;
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || num_blocks < 1 ||
+        max_blocks_per_seq < 1)
+        return KVFP8_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
+    if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
+    if (n_q / n_kv > 128) return KVFP8_ERR_UNSUPPORTED;  // past the tensor-core kernel's rows
+    if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
+        static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
+        return KVFP8_ERR_SHAPE;
+    if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
+    if (num_seqs == 0) {
+        *nothing_to_do = true;
+        return KVFP8_OK;
+    }
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
+        return KVFP8_ERR_NULL;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
+        !aligned16(value_cache) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return KVFP8_ERR_ALIGN;
+    return KVFP8_OK;
+}
+
+kvfp8_status launch_decode_validated(void *out, const void *query, const uint8_t *key_cache,
+                                     const uint8_t *value_cache, const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                     int32_t num_seqs, int32_t n_q, int32_t n_kv,
+                                     int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                     float sm_scale, const void *k_scale, const void *v_scale,
+                                     int scale_dtype, void *workspace, uint32_t *status,
+                                     kvfp8_stream_t stream) {
+    DecodeArgs d;
+    d.out = out;
+    d.query = query;
+    d.key_cache = key_cache;
+    d.value_cache = value_cache;
+    d.block_tables = block_tables;
+    d.max_blocks_per_seq = max_blocks_per_seq;
+    d.seq_lens = seq_lens;
+    d.num_seqs = num_seqs;
+    d.n_q = n_q;
+    d.n_kv = n_kv;
+    d.head_dim = head_dim;
+    d.block_size = block_size;
+    d.num_blocks = num_blocks;
+    d.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    d.k_scale = k_scale;
+    d.v_scale = v_scale;
+    d.scale_dtype = scale_dtype;
+    d.workspace = workspace;
+    d.status = status;
+    d.qsl = nullptr;
+    d.qmax = 1;
+    d.qrows = num_seqs;
+    d.k_bf16 = 0;
+    d.v_bf16 = 0;
+    return from_cuda(launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace kvfp8
+
 extern "C" {
 
 kvfp8_status kvfp8_reshape_and_cache(const void *key, const void *value, kvfp8_dtype src_dtype,
@@ -145,52 +215,19 @@ kvfp8_status kvfp8_paged_decode_attention(void *out, const void *query, const ui
                                           kvfp8_dtype scale_dtype, void *workspace,
                                           size_t workspace_bytes, uint32_t *status,
                                           kvfp8_stream_t stream) {
-    if (!dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
-    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || num_blocks < 1 ||
-        max_blocks_per_seq < 1)
-        return KVFP8_ERR_SHAPE;
-    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
-    if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
-    if (n_q / n_kv > 128) return KVFP8_ERR_UNSUPPORTED;  // past the tensor-core kernel's rows
-    if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
-        static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
-        return KVFP8_ERR_SHAPE;
-    if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
-    if (num_seqs == 0) return KVFP8_OK;
-    if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !workspace)
-        return KVFP8_ERR_NULL;
-    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
-        !aligned16(value_cache) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
-        !aligned16(workspace))
-        return KVFP8_ERR_ALIGN;
+    bool nothing_to_do = false;
+    const kvfp8_status v = kvfp8::validate_decode(
+        out, query, key_cache, value_cache, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+        n_q, n_kv, head_dim, block_size, num_blocks, sm_scale, scale_dtype, &nothing_to_do);
+    if (v != KVFP8_OK || nothing_to_do) return v;
+    if (!workspace) return KVFP8_ERR_NULL;
+    if (!aligned16(workspace)) return KVFP8_ERR_ALIGN;
     if (workspace_bytes < kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim))
         return KVFP8_ERR_WORKSPACE;
-    kvfp8::DecodeArgs d;
-    d.out = out;
-    d.query = query;
-    d.key_cache = key_cache;
-    d.value_cache = value_cache;
-    d.block_tables = block_tables;
-    d.max_blocks_per_seq = max_blocks_per_seq;
-    d.seq_lens = seq_lens;
-    d.num_seqs = num_seqs;
-    d.n_q = n_q;
-    d.n_kv = n_kv;
-    d.head_dim = head_dim;
-    d.block_size = block_size;
-    d.num_blocks = num_blocks;
-    d.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
-    d.k_scale = k_scale;
-    d.v_scale = v_scale;
-    d.scale_dtype = scale_dtype;
-    d.workspace = workspace;
-    d.status = status;
-    d.qsl = nullptr;
-    d.qmax = 1;
-    d.qrows = num_seqs;
-    d.k_bf16 = 0;
-    d.v_bf16 = 0;
-    return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
+    return kvfp8::launch_decode_validated(out, query, key_cache, value_cache, block_tables,
+                                          max_blocks_per_seq, seq_lens, num_seqs, n_q, n_kv,
+                                          head_dim, block_size, num_blocks, sm_scale, k_scale,
+                                          v_scale, scale_dtype, workspace, status, stream);
 }
 
 size_t kvfp8_paged_attention_multi_workspace_size(int32_t num_seqs, int32_t n_q, int32_t n_kv,

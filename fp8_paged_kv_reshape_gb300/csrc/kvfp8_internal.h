@@ -6,7 +6,82 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/kvfp8.h"
+
 namespace kvfp8 {
+
+// ---------------------------------------------------------------- launch facts
+// Device attributes and per-kernel occupancy do not change during a process, but querying
+// them costs microseconds of host time per call; they are looked up once per device (and
+// kernel, block size, shared memory) and kept.  A per-kernel dynamic shared memory limit is
+// raised once per device, when a larger size is first needed.
+
+struct DeviceFacts {
+    int sms;         // multiprocessors
+    int smem_optin;  // largest opt-in dynamic shared memory per block
+};
+
+inline cudaError_t device_facts(DeviceFacts *f) {
+    static std::mutex mu;
+    static std::map<int, DeviceFacts> cache;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(dev);
+    if (it == cache.end()) {
+        DeviceFacts d;
+        if ((err = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return err;
+        if ((err = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                          dev)) != cudaSuccess)
+            return err;
+        it = cache.emplace(dev, d).first;
+    }
+    *f = it->second;
+    return cudaSuccess;
+}
+
+// Resident blocks per SM of `kernel` at `threads` per block and `smem` dynamic bytes, after
+// making sure the kernel may use `smem` bytes of dynamic shared memory on this device.
+template <typename K>
+cudaError_t kernel_occupancy(K kernel, int threads, size_t smem, int *occ) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void *, int, int, size_t>, int> occ_cache;
+    static std::map<std::pair<const void *, int>, size_t> smem_set;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const void *fn = reinterpret_cast<const void *>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(fn, dev, threads, smem);
+    auto it = occ_cache.find(key);
+    if (it != occ_cache.end()) {
+        *occ = it->second;
+        return cudaSuccess;
+    }
+    if (smem > 48 * 1024) {
+        size_t &cur = smem_set[std::make_pair(fn, dev)];
+        if (smem > cur) {
+            if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem))) != cudaSuccess)
+                return err;
+            cur = smem;
+        }
+    }
+    int o = 0;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, threads, smem)) !=
+        cudaSuccess)
+        return err;
+    occ_cache.emplace(key, o);
+    *occ = o;
+    return cudaSuccess;
+}
 
 struct ReshapeArgs {
     const void *key;
@@ -93,6 +168,26 @@ cudaError_t launch_prefill_attention(const DecodeArgs &a, cudaStream_t stream);
 // True when kvfp8_paged_attention_multi takes the split-KV decode kernel for this shape
 // (and so needs a workspace); false when it takes the prefill kernel.
 bool multi_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t max_query_len);
+
+// Host validation of kvfp8_paged_decode_attention's arguments other than the workspace,
+// in the order that call checks them; *nothing_to_do is set (with KVFP8_OK) for an empty
+// batch.  Shared with the no-allocation entry point so both report the same errors.
+kvfp8_status validate_decode(const void *out, const void *query, const uint8_t *key_cache,
+                             const uint8_t *value_cache, const int32_t *block_tables,
+                             int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                             int32_t num_seqs, int32_t n_q, int32_t n_kv, int32_t head_dim,
+                             int32_t block_size, int32_t num_blocks, float sm_scale,
+                             int scale_dtype, bool *nothing_to_do);
+// The decode launch for arguments validate_decode accepted, with a workspace of at least
+// kvfp8_paged_decode_workspace_size bytes (16-byte aligned).
+kvfp8_status launch_decode_validated(void *out, const void *query, const uint8_t *key_cache,
+                                     const uint8_t *value_cache, const int32_t *block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t *seq_lens,
+                                     int32_t num_seqs, int32_t n_q, int32_t n_kv,
+                                     int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                     float sm_scale, const void *k_scale, const void *v_scale,
+                                     int scale_dtype, void *workspace, uint32_t *status,
+                                     kvfp8_stream_t stream);
 
 cudaError_t launch_dequant(void *dst, int dst_dtype, const uint8_t *src, int64_t n,
                            const void *scale, int scale_dtype, cudaStream_t stream);

@@ -1014,15 +1014,10 @@ int env_int(const char *name, int dflt) {
 
 template <int HD, int NT, bool kMulti, bool KT16, bool VT16>
 cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t stream) {
-    int dev = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    DeviceFacts facts;
+    cudaError_t err = device_facts(&facts);
     if (err != cudaSuccess) return err;
-    int sms = 0, smem_optin = 0;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return err;
-    if ((err = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
-        cudaSuccess)
-        return err;
+    const int sms = facts.sms, smem_optin = facts.smem_optin;
 
     constexpr int KB = KT16 ? 2 : 1, VB = VT16 ? 2 : 1;
     constexpr int SEGK = HD * KB >= 128 ? 128 : 64, SEGV = HD * VB >= 128 ? 128 : 64;
@@ -1046,14 +1041,9 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     if (smem > static_cast<size_t>(smem_optin)) return cudaErrorNotSupported;
 
     auto kern = decode_kernel<HD, NT, kMulti, KT16, VT16>;
-    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem))) != cudaSuccess)
-        return err;
     const int threads = 32 * (hpc + 1);
     int occ = 0;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem)) !=
-        cudaSuccess)
-        return err;
+    if ((err = kernel_occupancy(kern, threads, smem, &occ)) != cudaSuccess) return err;
     occ = std::max(1, std::min(occ, ctas_per_sm));
     // about one resident wave over all head groups
     const int num_ctas = std::max(1, std::min(sms * occ / groups, kMaxDecodeCtas));

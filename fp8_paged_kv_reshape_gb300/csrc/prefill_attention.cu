@@ -1316,8 +1316,8 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
         if (d.qsl != nullptr && d.qmax * a.group > kPfRows) {
             const size_t smem2 = Pf2Smem<HD>::kTotal + 1024;
             auto kern2 = prefill2_kernel<HD>;
-            if ((err = cudaFuncSetAttribute(kern2, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            static_cast<int>(smem2))) != cudaSuccess)
+            int occ2 = 0;  // also raises the kernel's shared memory limit, once per device
+            if ((err = kernel_occupancy(kern2, kP2Warps * 32, smem2, &occ2)) != cudaSuccess)
                 return err;
             a.row_tiles = (d.qmax * a.group + kP2Rows - 1) / kP2Rows;
             const int64_t ctas = static_cast<int64_t>(d.num_seqs) * a.row_tiles * d.n_kv;
@@ -1327,9 +1327,8 @@ cudaError_t run_prefill(const DecodeArgs &d, cudaStream_t stream) {
     }
     const size_t smem = L::kTotal + 1024;
     auto kern = prefill_kernel<HD>;
-    if ((err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(smem))) != cudaSuccess)
-        return err;
+    int occ = 0;  // also raises the kernel's shared memory limit, once per device
+    if ((err = kernel_occupancy(kern, kPfWarps * 32, smem, &occ)) != cudaSuccess) return err;
     a.row_tiles = (d.qmax * a.group + kPfRows - 1) / kPfRows;
     const int64_t ctas = static_cast<int64_t>(d.num_seqs) * a.row_tiles * d.n_kv;
     kern<<<static_cast<unsigned>(ctas), kPfWarps * 32, smem, stream>>>(tmk, tmv, a);

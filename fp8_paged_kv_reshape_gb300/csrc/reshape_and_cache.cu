@@ -540,16 +540,13 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
 template <typename K>
 cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t stream,
                               int64_t units) {
-    int dev = 0, sms = 0, occ = 0;
-    cudaError_t err = cudaGetDevice(&dev);
+    DeviceFacts f;
+    int occ = 0;
+    cudaError_t err = device_facts(&f);
     if (err != cudaSuccess) return err;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return err;
-    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kWarps * 32, 0)) !=
-        cudaSuccess)
-        return err;
+    if ((err = kernel_occupancy(kernel, kWarps * 32, 0, &occ)) != cudaSuccess) return err;
     const int64_t want = (units + kWarps - 1) / kWarps;
-    const int64_t full = static_cast<int64_t>(sms) * std::max(occ, 1);
+    const int64_t full = static_cast<int64_t>(f.sms) * std::max(occ, 1);
     const unsigned blocks = static_cast<unsigned>(std::min(want, full));
     kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
     return cudaGetLastError();

@@ -207,3 +207,44 @@ def test_multi_query_host_validation_on_the_tensor_core_route():
     assert call(num_seqs=0, query=None) == binding.OK
     # the split-KV route still wants its workspace
     assert call(qmax=4, workspace=None) == binding.ERR_NULL
+
+
+def _noalloc(**over):
+    args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16), key_cache=ctypes.c_void_p(16),
+                value_cache=ctypes.c_void_p(16), block_tables=ctypes.c_void_p(16),
+                max_blocks_per_seq=256, seq_lens=ctypes.c_void_p(16), num_seqs=4, n_q=32, n_kv=8,
+                head_dim=128, block_size=16, num_blocks=1024, sm_scale=0.0, k_scale=None,
+                v_scale=None, scale_dtype=binding.F32, status=None, stream=None)
+    args.update(over)
+    return kv.LIB.kvfp8_paged_decode_attention_noalloc(*args.values())
+
+
+def test_noalloc_host_validation_matches_the_workspace_entry_point():
+    # every argument error comes back with the workspace entry point's code, before the
+    # library's scratch array is looked up (so no device is needed to see them)
+    for over in (dict(query=None), dict(seq_lens=None), dict(scale_dtype=4), dict(n_q=30),
+                 dict(n_q=8 * 129), dict(head_dim=96), dict(block_size=12),
+                 dict(num_blocks=0), dict(sm_scale=float("inf")), dict(out=ctypes.c_void_p(8)),
+                 dict(block_tables=ctypes.c_void_p(18)), dict(num_seqs=-1),
+                 dict(num_seqs=0, query=None)):
+        assert _noalloc(**over) == _decode(**over), over
+    assert _noalloc(num_seqs=0, query=None) == binding.OK
+    # past the fixed scratch: refused without touching a device
+    assert kv.paged_decode_workspace_size(40000, 32, 128) > (32 << 20)
+    assert _noalloc(num_seqs=40000) == binding.ERR_WORKSPACE
+
+
+def test_noalloc_binding_checks_tables_like_the_workspace_binding():
+    import torch
+
+    q = torch.zeros(4, 32, 128, dtype=torch.bfloat16)
+    kc = torch.zeros(8, 16, 8, 128, dtype=torch.uint8)
+    bt = torch.zeros(4, 2, dtype=torch.int32)
+    sl = torch.ones(4, dtype=torch.int32)
+    bad = [(bt.long(), sl), (bt[:3], sl), (bt, sl.long()), (bt, sl[:3]), (bt.t(), sl)]
+    for fn in (kv.paged_decode_attention, kv.paged_decode_attention_noalloc):
+        for b, s in bad:
+            with pytest.raises(ValueError):
+                fn(q, kc, kc, b, s)
+        with pytest.raises(ValueError):  # out shaped unlike query
+            fn(q, kc, kc, bt, sl, out=torch.zeros(4, 32, 64, dtype=torch.bfloat16))

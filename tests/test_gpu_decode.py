@@ -180,41 +180,37 @@ def test_bad_device_scale_writes_nothing():
         assert bool((out == 7.0).all())
 
 
-def _full_size(name, n_pairs):
-    w = workloads.WORKLOADS[name]
-    lay = workloads.make_layout(w)
-    k, v = workloads.make_kv(w, lay.slot_mapping.size, "cuda")
+def _full_size(name, n_random_pairs):
+    # The bench step at full size: the whole context written (and, for the serving mix, one
+    # new token per sequence), then decode.  The oracle attends over its own cache (built
+    # from the same host inputs, never from GPU output) for every head of four sequences --
+    # the longest, the shortest and two seeded others -- and for seeded random pairs.
+    case = gpu_util.full_size_workload(name)
+    w, lay = case["w"], case["lay"]
     q = workloads.make_query(w, lay.num_seqs, "cuda")
-    ksc, vsc = gpu_util.scale_pair(w)
-    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
-    vc = kc.clone()
-    kv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(lay.slot_mapping).cuda(), ksc, vsc)
-    if w.kind == "mixed":  # the serving step: one new token per sequence at len-1, then decode
-        kn, vn = workloads.make_new_token_kv(w, lay.num_seqs, "cuda")
-        last = lay.seq_lens - 1
-        new_slots = lay.block_tables[np.arange(lay.num_seqs), last // w.block_size].astype(np.int64) \
-            * w.block_size + last % w.block_size
-        kv.reshape_and_cache(kn, vn, kc, vc, torch.from_numpy(new_slots).cuda(), ksc, vsc)
-        # the oracle sees the same rows: replace the context row at len-1 by the new token
-        rows = np.nonzero(lay.row_pos == (lay.seq_lens[lay.row_seq] - 1))[0]
-        k = k.clone()
-        v = v.clone()
-        k[torch.from_numpy(rows).cuda()] = kn[torch.from_numpy(lay.row_seq[rows]).cuda().long()]
-        v[torch.from_numpy(rows).cuda()] = vn[torch.from_numpy(lay.row_seq[rows]).cuda().long()]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = kv.paged_decode_attention(q, kc, vc, torch.from_numpy(lay.block_tables).cuda(),
-                                    torch.from_numpy(lay.seq_lens).cuda(), ksc, vsc, status=status)
+    out = kv.paged_decode_attention(q, case["kc"], case["vc"],
+                                    torch.from_numpy(lay.block_tables).cuda(),
+                                    torch.from_numpy(lay.seq_lens).cuda(), case["ksc"],
+                                    case["vsc"], status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    assert torch.isfinite(out.float()).all()
+    ko, vo = gpu_util.oracle_full_cache(case)
     rng = np.random.Generator(np.random.PCG64(w.seed + 77))
-    seqs = rng.integers(0, lay.num_seqs, n_pairs)
-    seqs[0], seqs[-1] = int(np.argmax(lay.seq_lens)), int(np.argmin(lay.seq_lens))
-    pairs = [(int(b), int(h)) for b, h in zip(seqs, rng.integers(0, w.n_q, n_pairs))]
+    whole = [int(np.argmax(lay.seq_lens)), int(np.argmin(lay.seq_lens))]
+    for s in rng.permutation(lay.num_seqs):
+        if len(whole) == min(4, lay.num_seqs):
+            break
+        if int(s) not in whole:
+            whole.append(int(s))
+    pairs = [(b, h) for b in whole for h in range(w.n_q)]
+    pairs += [(int(b), int(h)) for b, h in zip(rng.integers(0, lay.num_seqs, n_random_pairs),
+                                                rng.integers(0, w.n_q, n_random_pairs))]
     ks, vs = gpu_util.stored_scales(w)
-    ref = gpu_util.oracle_pairs(pairs, k, v, q, lay, w, ks, vs)
+    ref = gpu_util.oracle_pairs_threaded(pairs, q, ko, vo, lay.block_tables, lay.seq_lens, ks, vs)
     got = torch.stack([out[b, h] for b, h in pairs])
     gpu_util.assert_attention_close(got, ref, name)
-    assert torch.isfinite(out.float()).all()
 
 
 def test_full_size_llama3_8b_sampled():
@@ -222,7 +218,7 @@ def test_full_size_llama3_8b_sampled():
 
 
 def test_full_size_long_context_sampled():
-    _full_size("long_context", 12)
+    _full_size("long_context", 16)
 
 
 def test_full_size_mixed_serving_sampled():

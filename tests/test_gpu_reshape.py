@@ -99,53 +99,37 @@ def _workload_inputs(name, **over):
     return w, lay, k, v
 
 
-@pytest.mark.parametrize("name", ["tiny", "prefill_write"])
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "long_context", "prefill_write",
+                                  "mixed_serving"])
 def test_workload_full_cache_bit_exact(name):
-    w, lay, k, v = _workload_inputs(name)
-    ks, vs = gpu_util.stored_scales(w)
-    ksc, vsc = gpu_util.scale_pair(w)
-    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
-    vc = kc.clone()
-    kv.reshape_and_cache(k, v, kc, vc, torch.from_numpy(lay.slot_mapping).cuda(), ksc, vsc)
-    torch.cuda.synchronize()
-    ko = workloads.new_cache(lay.num_blocks, w).numpy()
-    vo = ko.copy()
-    assert oracle.reshape_and_cache(gpu_util.to_u16(k), gpu_util.to_u16(v), ko, vo,
-                                    lay.slot_mapping, w.block_size, ks, vs) == 0
-    assert np.array_equal(kc.cpu().numpy(), ko)
-    assert np.array_equal(vc.cpu().numpy(), vo)
+    # Every configuration at full size, written as a bench step writes it (all context rows;
+    # the serving mix then writes one new token per sequence over its last row), and the
+    # whole K and V caches compared byte for byte with the oracle's, sentinels included.
+    case = gpu_util.full_size_workload(name)
+    ko, vo = gpu_util.oracle_full_cache(case)
+    kc = case["kc"].cpu().numpy()
+    bad = np.nonzero(kc.ravel() != ko.ravel())[0]
+    assert bad.size == 0, (name, bad.size, bad[:8])
+    del kc
+    vc = case["vc"].cpu().numpy()
+    bad = np.nonzero(vc.ravel() != vo.ravel())[0]
+    assert bad.size == 0, (name, bad.size, bad[:8])
+    lay = case["lay"]
     if name == "prefill_write":
         assert (lay.slot_mapping == -1).sum() > 0  # padding rows were present and skipped
-
-
-@pytest.mark.parametrize("name", ["llama3_8b", "long_context", "mixed_serving"])
-def test_workload_full_size_sampled_rows(name):
-    # Full-size prefill of the whole context; the oracle recomputes a seeded sample of rows.
-    w, lay, k, v = _workload_inputs(name)
-    ks, vs = gpu_util.stored_scales(w)
-    ksc, vsc = gpu_util.scale_pair(w)
-    kc = workloads.new_cache(lay.num_blocks, w, "cuda")
-    vc = kc.clone()
-    slots = torch.from_numpy(lay.slot_mapping).cuda()
-    kv.reshape_and_cache(k, v, kc, vc, slots, ksc, vsc)
-    torch.cuda.synchronize()
-    rng = np.random.Generator(np.random.PCG64(w.seed))
-    rows = np.sort(rng.choice(lay.slot_mapping.size, size=4096, replace=False))
-    rows = np.unique(np.concatenate([rows, [0, lay.slot_mapping.size - 1]]))
-    ridx = torch.from_numpy(rows).cuda()
-    n = rows.size
-    ko = np.full((n, 1, w.n_kv, w.head_dim), 0, np.uint8)
-    vo = ko.copy()
-    assert oracle.reshape_and_cache(gpu_util.to_u16(k.index_select(0, ridx)),
-                                    gpu_util.to_u16(v.index_select(0, ridx)), ko, vo,
-                                    np.arange(n, dtype=np.int64), 1, ks, vs) == 0
-    flat_k = kc.view(-1, w.n_kv, w.head_dim)
-    flat_v = vc.view(-1, w.n_kv, w.head_dim)
-    sl = slots.index_select(0, ridx)
-    np.testing.assert_array_equal(flat_k.index_select(0, sl).cpu().numpy(), ko[:, 0])
-    np.testing.assert_array_equal(flat_v.index_select(0, sl).cpu().numpy(), vo[:, 0])
+        assert (ko == workloads.SENTINEL).all(axis=(1, 2, 3)).any()  # untouched pool blocks
     if name == "llama3_8b":  # the 0.1% outliers x20 reach the saturation code
-        assert (np.abs(ko.astype(np.int16) & 0x7F) == 0x7E).any()
+        assert ((ko & 0x7F) == 0x7E).any()
+    if name == "mixed_serving":  # the last row of every sequence holds its new token
+        w = case["w"]
+        kn, vn, new_slots = case["new"]
+        ks, vs = gpu_util.stored_scales(w)
+        kt = np.zeros((lay.num_seqs, 1, w.n_kv, w.head_dim), np.uint8)
+        vt = kt.copy()
+        assert oracle.reshape_and_cache(kn, vn, kt, vt, np.arange(lay.num_seqs), 1, ks, vs) == 0
+        row = w.n_kv * w.head_dim
+        np.testing.assert_array_equal(ko.reshape(-1, row)[new_slots], kt.reshape(-1, row))
+        np.testing.assert_array_equal(vo.reshape(-1, row)[new_slots], vt.reshape(-1, row))
 
 
 def test_strided_rows_from_a_fused_projection():

@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tests import gpu_util
 
 pytestmark = pytest.mark.gpu
@@ -50,7 +51,19 @@ def _noalloc_via_c_abi(q, kc, vc, bt, sl, ks, vs, out, status):
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
+def _oracle(q, kc, vc, bt, sl, ks, vs):
+    ref, st = oracle.paged_decode_attention(q.cpu(), kc.cpu().numpy(), vc.cpu().numpy(),
+                                            bt.cpu().numpy(), sl.cpu().numpy(), float(ks.item()),
+                                            float(vs.item()))
+    assert st == 0
+    return ref
+
+
 def test_no_alloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
+    # Two different batches back to back through the raw C ABI: each output must equal the
+    # workspace entry point's bit for bit (same kernels, same inputs), and both must match the
+    # double-precision oracle within the attention tolerance.  The second call reuses the
+    # scratch the first one left behind.
     cases = [(1, [1000, 17, 4096, 0, 300, 1]), (2, [30000, 33, 5, 2048])]
     for seed, lengths in cases:
         q, kc, vc, bt, sl, ks, vs = _inputs(seed, lengths)
@@ -61,8 +74,29 @@ def test_no_alloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
         torch.cuda.synchronize()
         assert rc == binding.OK, kv.status_string(rc)
         assert int(status.item()) == 0
-        ref64 = ref.float().cpu().numpy().astype(np.float64)
-        gpu_util.assert_attention_close(out, ref64, f"noalloc call {seed}")
+        assert torch.equal(out, ref), f"call {seed}: differs from the workspace entry point"
+        gpu_util.assert_attention_close(out, _oracle(q, kc, vc, bt, sl, ks, vs),
+                                        f"noalloc call {seed} vs oracle")
+
+
+def test_no_alloc_through_the_binding_allocates_no_device_memory():
+    q, kc, vc, bt, sl, ks, vs = _inputs(3, [5000, 1, 777, 64, 2])
+    ref = kv.paged_decode_attention(q, kc, vc, bt, sl, ks, vs)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = [torch.full_like(q, float("nan")) for _ in range(3)]
+    kv.paged_decode_attention_noalloc(q, kc, vc, bt, sl, ks, vs, out=out, status=status)
+    torch.cuda.synchronize()  # the first call has loaded its kernels
+    free0 = torch.cuda.mem_get_info()[0]
+    for o in outs:
+        kv.paged_decode_attention_noalloc(q, kc, vc, bt, sl, ks, vs, out=o, status=status)
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 == free0, "device memory changed across no-alloc calls"
+    assert int(status.item()) == 0
+    for o in [out] + outs:
+        assert torch.equal(o, ref)
+    gpu_util.assert_attention_close(out, _oracle(q, kc, vc, bt, sl, ks, vs), "noalloc binding")
 
 
 def test_no_alloc_refuses_a_batch_larger_than_its_scratch():
