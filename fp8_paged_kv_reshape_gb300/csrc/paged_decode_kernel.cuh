@@ -378,6 +378,113 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
     }
 }
 
+// Chunks of sequence i (and its clamped length): 16-token chunks of its L cached tokens, or
+// none when it has no query rows.  The same rule the plan kernel applies.
+__device__ __forceinline__ int seq_chunks(const KernelArgs &a, int i, int &L) {
+    L = min(max(a.seq_lens[i], 0), a.max_len);
+    const int nq = a.qsl ? query_range(a.qsl, i, a.rows_per_seq / a.n_q, a.qrows).count : 1;
+    return nq > 0 ? (L + kChunkTokens - 1) / kChunkTokens : 0;
+}
+
+// Sequences one thread holds in registers while a CTA plans its own range.
+constexpr int kPlanPerThread = 16;
+
+// The plan of one decode CTA worked out by the CTA itself, for batches of at most
+// blockDim.x * kPlanPerThread sequences (the launcher runs the plan kernel otherwise).
+// Every thread takes a contiguous run of up to kPlanPerThread sequences, loads their lengths
+// (independent loads, all in flight together), and a block-wide scan of the per-thread chunk
+// sums gives every sequence's first chunk and the total T.  The thread whose run holds chunk
+// lo = c*T/P writes the record.  CTA (0, 0) also writes the chunk prefix for the combine
+// kernel and raises the status bits for bad lengths or query ranges; the output rows of
+// empty sequences are zeroed by CTA (i mod gridDim.x, 0).  All threads must call it.
+__device__ __forceinline__ CtaPlan plan_in_cta(const KernelArgs &a, int32_t *cstart_out,
+                                            __nv_bfloat16 *out, int out_row_elems) {
+    __shared__ int32_t warp_sum[32];
+    __shared__ CtaPlan rec;
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+    const int nw = (nt + 31) >> 5;
+    const int k = (a.num_seqs + nt - 1) / nt;  // sequences per thread (<= kPlanPerThread)
+    const int s0 = tid * k;
+    const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
+    int n[kPlanPerThread], len[kPlanPerThread];
+    int sum = 0;
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) {
+        n[j] = 0;
+        len[j] = 0;
+        const int i = s0 + j;
+        if (j < k && i < a.num_seqs) {
+            const int raw = a.seq_lens[i];
+            n[j] = seq_chunks(a, i, len[j]);
+            if (lead) {
+                if (raw < 0 || raw > a.max_len) flag(a.status, KVFP8_DEV_BAD_BLOCK);
+                if (a.qsl) {
+                    const int nq = query_range(a.qsl, i, a.rows_per_seq / a.n_q, a.qrows).count;
+                    if (nq != a.qsl[i + 1] - a.qsl[i] || nq > len[j])
+                        flag(a.status, KVFP8_DEV_BAD_BLOCK);
+                }
+            }
+            if (n[j] == 0 && blockIdx.y == 0 && i % gridDim.x == blockIdx.x) {
+                // an empty sequence: no CTA visits it, so its output rows are zeroed here
+                const QueryRange qr = a.qsl ? query_range(a.qsl, i, a.rows_per_seq / a.n_q, a.qrows)
+                                            : QueryRange{i, 1};
+                uint4 *rows = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(qr.q0) * out_row_elems);
+                for (int64_t e = 0; e < static_cast<int64_t>(qr.count) * out_row_elems / 8; ++e)
+                    rows[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            sum += n[j];
+        }
+    }
+    // exclusive scan of the per-thread sums over the block
+    int x = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nw ? warp_sum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sum[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? warp_sum[warp - 1] : 0) + x - sum;
+    const int64_t T = warp_sum[nw - 1];
+    const int64_t P = T < a.num_ctas ? T : a.num_ctas;
+    const int c = blockIdx.x;
+    CtaPlan r = {0, 0, 0, 0, 0, 0, static_cast<int32_t>(T), 0};
+    if (tid == 0) rec = r;
+    __syncthreads();
+    const int64_t lo = c < P ? static_cast<int64_t>(c) * T / P : -1;
+    int run = before;
+#pragma unroll
+    for (int j = 0; j < kPlanPerThread; ++j) {
+        const int i = s0 + j;
+        if (j < k && i < a.num_seqs) {
+            if (lead) cstart_out[i] = run;
+            if (n[j] > 0 && run <= lo && lo < run + n[j]) {
+                r.lo = static_cast<int32_t>(lo);
+                r.hi = static_cast<int32_t>(static_cast<int64_t>(c + 1) * T / P);
+                r.s = i;
+                r.cs = run;
+                r.ce = run + n[j];
+                r.L = len[j];
+                rec = r;  // exactly one thread's run holds chunk lo
+            }
+            run += n[j];
+        }
+    }
+    if (lead && tid == 0) cstart_out[a.num_seqs] = static_cast<int32_t>(T);
+    __syncthreads();
+    return rec;
+}
+
 // The CTA whose chunk range contains chunk x (ranges are [c*T/P, (c+1)*T/P), P <= T).
 __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t P) {
     return static_cast<int>(((x + 1) * P - 1) / T);
@@ -480,7 +587,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
-    pdl_wait();     // the plan grid's cstart and zeroed rows are visible from here on
+    pdl_wait();     // the previous grid's writes (plan, cache, last call's combine) are visible
     pdl_trigger();  // let the combine grid get launched; it waits for this grid to finish
 
     const float sk = KT16 ? 1.f : load_scale(a.k_scale, a.scale_dtype);
@@ -491,8 +598,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     }
     // Effective grid: at most one CTA per chunk, so that every active CTA's range is
     // non-empty and the CTAs between a sequence's first and last one all hold a part of it;
-    // the plan left CTAs past it an empty range.
-    const CtaPlan pl = a.cta_plan[blockIdx.x];
+    // the plan leaves CTAs past it an empty range.
+    const CtaPlan pl = a.cta_plan != nullptr
+                           ? a.cta_plan[blockIdx.x]
+                           : plan_in_cta(a, const_cast<int32_t *>(a.cstart), a.out, a.n_q * HD);
     if (pl.lo >= pl.hi) return;
     const int64_t chunk_lo = pl.lo, chunk_hi = pl.hi;
     __syncthreads();
@@ -513,8 +622,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                 while (x >= ce) {
                     ++s;
                     cs = ce;
-                    ce = a.cstart[s + 1];
-                    L = min(max(a.seq_lens[s], 0), a.max_len);
+                    ce = cs + seq_chunks(a, s, L);
                     wbase = -1 << 30;
                 }
                 const int j = static_cast<int>(x - cs);
@@ -1100,14 +1208,24 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.k_bf16 = KT16 ? 1 : 0;
     k.v_bf16 = VT16 ? 1 : 0;
 
-    plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs, k.max_len,
-                                        num_ctas, reinterpret_cast<int32_t *>(w + ws.cstart_off),
-                                        reinterpret_cast<CtaPlan *>(w + ws.cta_off), k.out,
-                                        d.n_q * HD, d.status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    // Batches a CTA can plan from registers are planned inside the decode grid (no plan
+    // launch); larger ones get the one-CTA plan kernel first.
+    const bool plan_inside = d.num_seqs <= threads * kPlanPerThread &&
+                             env_int("KVFP8_DECODE_PLAN_KERNEL", 0) == 0;
+    if (plan_inside) {
+        k.cta_plan = nullptr;
+    } else {
+        plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs,
+                                            k.max_len, num_ctas,
+                                            reinterpret_cast<int32_t *>(w + ws.cstart_off),
+                                            reinterpret_cast<CtaPlan *>(w + ws.cta_off), k.out,
+                                            d.n_q * HD, d.status);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
 
-    // Programmatic dependent launch: the decode grid starts its prologue while the plan
-    // grid runs and waits (griddepcontrol.wait) before touching any data.
+    // Programmatic dependent launch: the decode grid starts its prologue while the previous
+    // grid in the stream (the plan kernel, or the caller's last kernel) finishes, and waits
+    // (griddepcontrol.wait) before it reads or writes any memory.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas, groups);
     cfg.blockDim = dim3(threads);

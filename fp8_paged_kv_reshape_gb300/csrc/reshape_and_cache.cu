@@ -163,6 +163,11 @@ struct Group<false> {  // bf16: 16 bytes
         g.v.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, m);
         return g;
     }
+    // the elements as bf16 pairs (a bf16 source is copied unchanged)
+    __device__ __forceinline__ void bf16_words(uint32_t (&o)[4]) const {
+        o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    }
+    static constexpr int kElems = 8;
     static constexpr int kBytes = 16;
 };
 
@@ -185,7 +190,66 @@ struct Group<true> {  // fp32: 32 bytes
                           __shfl_xor_sync(0xFFFFFFFFu, b.z, m), __shfl_xor_sync(0xFFFFFFFFu, b.w, m));
         return g;
     }
+    // the elements rounded to bf16 pairs (nearest even)
+    __device__ __forceinline__ void bf16_words(uint32_t (&o)[4]) const {
+        o[0] = bf16x2_from_f32(a.x, a.y); o[1] = bf16x2_from_f32(a.z, a.w);
+        o[2] = bf16x2_from_f32(b.x, b.y); o[3] = bf16x2_from_f32(b.z, b.w);
+    }
+    static constexpr int kElems = 8;
     static constexpr int kBytes = 32;
+};
+
+// 32-byte streaming load (sm_100+): eight words in one instruction; p 32-byte aligned.
+__device__ __forceinline__ void ld_cs_v8(const uint8_t *p, uint32_t *w) {
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
+// Sixteen consecutive elements of a source row for the wide path: one 32-byte load (bf16)
+// or two (fp32) per lane, and 16 output bytes per lane, stored with one 16-byte store.
+// Rows and their start must be 32-byte aligned.
+template <bool kF32>
+struct Wide;
+
+template <>
+struct Wide<false> {  // bf16: 32 bytes
+    uint32_t w[8];
+    __device__ __forceinline__ void load(const uint8_t *p) { ld_cs_v8(p, w); }
+    __device__ __forceinline__ void unpack(float (&x)[16]) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            x[2 * i] = bf16lo(w[i]);
+            x[2 * i + 1] = bf16hi(w[i]);
+        }
+    }
+    __device__ __forceinline__ void bf16_words(uint32_t (&o)[8]) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = w[i];
+    }
+    static constexpr int kElems = 16;
+    static constexpr int kBytes = 32;
+};
+
+template <>
+struct Wide<true> {  // fp32: 64 bytes
+    uint32_t w[16];
+    __device__ __forceinline__ void load(const uint8_t *p) {
+        ld_cs_v8(p, w);
+        ld_cs_v8(p + 32, w + 8);
+    }
+    __device__ __forceinline__ void unpack(float (&x)[16]) const {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = __uint_as_float(w[i]);
+    }
+    __device__ __forceinline__ void bf16_words(uint32_t (&o)[8]) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            o[i] = bf16x2_from_f32(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+    }
+    static constexpr int kElems = 16;
+    static constexpr int kBytes = 64;
 };
 
 struct RowCtx {
@@ -207,54 +271,58 @@ __device__ __forceinline__ bool row_ok(const ReshapeArgs &a, int64_t row, int64_
     return false;
 }
 
-template <bool kF32, int U>
-__device__ __forceinline__ void load_row(Group<kF32> (&buf)[U], const RowCtx &c, int64_t row,
-                                         int groups, int lane) {
+template <typename G, int U>
+__device__ __forceinline__ void load_row(G (&buf)[U], const RowCtx &c, int64_t row, int units,
+                                         int lane) {
     const uint8_t *p = c.src + (row >> 1) * c.stride_bytes;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int g = lane + 32 * u;
-        if (g < groups) buf[u].load(p + static_cast<int64_t>(g) * Group<kF32>::kBytes);
+        if (g < units) buf[u].load(p + static_cast<int64_t>(g) * G::kBytes);
     }
 }
 
 // A side whose cache is bf16 (mixed cache dtypes): the row is stored at 16 bits, rounded to
 // bf16 (a bf16 source is copied unchanged), with no scale.
-template <bool kF32, int U>
-__device__ __forceinline__ void store_row_bf16(const Group<kF32> (&buf)[U], const RowCtx &c,
-                                               int64_t slot, int row_elems, int groups, int lane) {
+template <typename G, int U>
+__device__ __forceinline__ void store_row_bf16(const G (&buf)[U], const RowCtx &c, int64_t slot,
+                                               int row_elems, int units, int lane) {
     uint8_t *dst = c.cache + slot * row_elems * 2;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int g = lane + 32 * u;
-        if (g < groups) {
-            uint4 w;
-            if constexpr (kF32) {
-                float x[8];
-                buf[u].unpack(x);
-                w = make_uint4(bf16x2_from_f32(x[0], x[1]), bf16x2_from_f32(x[2], x[3]),
-                               bf16x2_from_f32(x[4], x[5]), bf16x2_from_f32(x[6], x[7]));
-            } else {
-                w = buf[u].v;
-            }
-            *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * 16) = w;
+        if (g < units) {
+            uint32_t o[G::kElems / 2];
+            buf[u].bf16_words(o);
+            uint4 *q = reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * G::kElems * 2);
+#pragma unroll
+            for (int i = 0; i < G::kElems / 8; ++i)
+                q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
     }
 }
 
-template <bool kF32, int U, bool kFast>
-__device__ __forceinline__ void store_row(const Group<kF32> (&buf)[U], const RowCtx &c,
-                                          const FastDiv &fd, int64_t slot, int row_elems,
-                                          int groups, int lane) {
+// E4M3 codes of a row: 8 bytes per lane and unit (8-element groups) or 16 (wide units).
+template <typename G, int U, bool kFast>
+__device__ __forceinline__ void store_row(const G (&buf)[U], const RowCtx &c, const FastDiv &fd,
+                                          int64_t slot, int row_elems, int units, int lane) {
     uint8_t *dst = c.cache + slot * row_elems;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         const int g = lane + 32 * u;
-        if (g < groups) {
-            float x[8];
+        if (g < units) {
+            float x[G::kElems];
             buf[u].unpack(x);
-            *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
-                quantize8<kFast>(x, c.s, fd);
+            if constexpr (G::kElems == 8) {
+                *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
+                    quantize8<kFast>(x, c.s, fd);
+            } else {
+                const uint2 lo = quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x), c.s, fd);
+                const uint2 hi =
+                    quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x + 8), c.s, fd);
+                *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * 16) =
+                    make_uint4(lo.x, lo.y, hi.x, hi.y);
+            }
         }
     }
 }
@@ -266,43 +334,44 @@ __device__ __forceinline__ bool fast_range(float s) {
 
 // The rows of one warp (every stride-th row from r), two in flight.  kMode: 0 = E4M3 with
 // the fast divide, 1 = E4M3 with __fdiv_rn, 2 = bf16 cache (mixed cache dtypes).
-template <bool kF32, int U, int kMode>
+template <typename G, int U, int kMode>
 __device__ __forceinline__ void pipelined_rows(const ReshapeArgs &a, const RowCtx &c, int64_t r,
                                                int64_t stride, int64_t rows, int lane) {
     constexpr bool kFast = kMode == 0;
     const FastDiv fd(c.s);
-    const int groups = a.row_elems >> 3;
-    Group<kF32> A[U], B[U];
+    const int units = a.row_elems / G::kElems;
+    G A[U], B[U];
     int64_t s1 = slot_of(a, r, rows);
     int64_t s2 = slot_of(a, r + stride, rows);
     bool ok1 = r < rows && row_ok(a, r, s1, lane);
-    if (ok1) load_row<kF32, U>(A, c, r, groups, lane);
+    if (ok1) load_row(A, c, r, units, lane);
     while (r < rows) {
         int64_t rn = r + stride;
         bool ok2 = rn < rows && row_ok(a, rn, s2, lane);
-        if (ok2) load_row<kF32, U>(B, c, rn, groups, lane);
+        if (ok2) load_row(B, c, rn, units, lane);
         int64_t s3 = slot_of(a, rn + stride, rows);
         if (ok1) {
-            if (kMode == 2) store_row_bf16<kF32, U>(A, c, s1, a.row_elems, groups, lane);
-            else store_row<kF32, U, kFast>(A, c, fd, s1, a.row_elems, groups, lane);
+            if (kMode == 2) store_row_bf16(A, c, s1, a.row_elems, units, lane);
+            else store_row<G, U, kFast>(A, c, fd, s1, a.row_elems, units, lane);
         }
         r = rn; s1 = s2; s2 = s3; ok1 = ok2;
         if (r >= rows) break;
         rn = r + stride;
         ok2 = rn < rows && row_ok(a, rn, s2, lane);
-        if (ok2) load_row<kF32, U>(A, c, rn, groups, lane);
+        if (ok2) load_row(A, c, rn, units, lane);
         s3 = slot_of(a, rn + stride, rows);
         if (ok1) {
-            if (kMode == 2) store_row_bf16<kF32, U>(B, c, s1, a.row_elems, groups, lane);
-            else store_row<kF32, U, kFast>(B, c, fd, s1, a.row_elems, groups, lane);
+            if (kMode == 2) store_row_bf16(B, c, s1, a.row_elems, units, lane);
+            else store_row<G, U, kFast>(B, c, fd, s1, a.row_elems, units, lane);
         }
         r = rn; s1 = s2; s2 = s3; ok1 = ok2;
     }
 }
 
-// Rows of up to 256*U elements.
-template <bool kF32, int U>
+// Rows of up to 32*U units of G::kElems elements.
+template <typename G, int U>
 __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const ReshapeArgs a) {
+    constexpr bool kF32 = G::kBytes == 4 * G::kElems;
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
     if ((!a.k_bf16 && !scale_ok(sk)) || (!a.v_bf16 && !scale_ok(sv))) {
@@ -320,11 +389,11 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const Re
     c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
     c.s = is_v ? sv : sk;
     if (is_v ? a.v_bf16 : a.k_bf16)  // uniform per warp
-        pipelined_rows<kF32, U, 2>(a, c, r, stride, rows, lane);
+        pipelined_rows<G, U, 2>(a, c, r, stride, rows, lane);
     else if (fast_range(c.s))
-        pipelined_rows<kF32, U, 0>(a, c, r, stride, rows, lane);
+        pipelined_rows<G, U, 0>(a, c, r, stride, rows, lane);
     else
-        pipelined_rows<kF32, U, 1>(a, c, r, stride, rows, lane);
+        pipelined_rows<G, U, 1>(a, c, r, stride, rows, lane);
 }
 
 // ---------------------------------------------------------------- rope + cache write
@@ -447,9 +516,9 @@ __device__ __forceinline__ void rope_token_rows(const ReshapeArgs &a, const RowC
     int64_t s2 = slot_at(t + W), p2 = pos_at(t + W);
     bool ok1 = ok_of(t, s1, p1);
     if (ok1) {
-        load_row<kF32, U>(A, ck, 2 * t, groups, lane);
+        load_row(A, ck, 2 * t, groups, lane);
         load_cs(tc, a, p1, lane);
-        load_row<kF32, U>(B, cv, 2 * t + 1, groups, lane);
+        load_row(B, cv, 2 * t + 1, groups, lane);
     }
     while (t < T) {
         const int64_t tn = t + W;
@@ -457,11 +526,11 @@ __device__ __forceinline__ void rope_token_rows(const ReshapeArgs &a, const RowC
         const int64_t s3 = slot_at(tn + W), p3 = pos_at(tn + W);
         if (ok1) store_row_rope<kF32, U, kFast>(A, tc, ck, fk, a, s1, groups, lane);
         if (ok2) {
-            load_row<kF32, U>(A, ck, 2 * tn, groups, lane);
+            load_row(A, ck, 2 * tn, groups, lane);
             load_cs(tc, a, p2, lane);
         }
-        if (ok1) store_row<kF32, U, kFast>(B, cv, fv, s1, a.row_elems, groups, lane);
-        if (ok2) load_row<kF32, U>(B, cv, 2 * tn + 1, groups, lane);
+        if (ok1) store_row<Group<kF32>, U, kFast>(B, cv, fv, s1, a.row_elems, groups, lane);
+        if (ok2) load_row(B, cv, 2 * tn + 1, groups, lane);
         t = tn; s1 = s2; s2 = s3; p1 = p2; p2 = p3; ok1 = ok2;
     }
 }
@@ -552,14 +621,30 @@ cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t strea
     return cudaGetLastError();
 }
 
+// The wide path (16 elements and one 16-byte store of codes per lane and unit) needs rows of
+// at least 512 elements, a multiple of 16, and 32-byte aligned source rows.
+bool wide_ok(const ReshapeArgs &a) {
+    const int64_t esz = a.src_dtype == KVFP8_F32 ? 4 : 2;
+    const uintptr_t bases = reinterpret_cast<uintptr_t>(a.key) | reinterpret_cast<uintptr_t>(a.value);
+    return a.row_elems % 16 == 0 && a.row_elems >= 512 && a.row_elems <= 2048 &&
+           (bases & 31u) == 0 && (a.key_stride * esz) % 32 == 0 && (a.value_stride * esz) % 32 == 0;
+}
+
 template <bool kF32>
 cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
+    const int64_t rows = 2 * a.num_tokens;
+    if (wide_ok(a)) {
+        const int per_lane = (a.row_elems / 16 + 31) / 32;  // 16-element units per lane
+        if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<Wide<kF32>, 1>, a, stream, rows);
+        if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<Wide<kF32>, 2>, a, stream, rows);
+        return launch_persistent(reshape_pipelined_kernel<Wide<kF32>, 4>, a, stream, rows);
+    }
     const int per_lane = (a.row_elems / 8 + 31) / 32;  // 8-element groups per lane
-    if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<kF32, 1>, a, stream, 2 * a.num_tokens);
-    if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<kF32, 2>, a, stream, 2 * a.num_tokens);
-    if (per_lane <= 4) return launch_persistent(reshape_pipelined_kernel<kF32, 4>, a, stream, 2 * a.num_tokens);
-    if (per_lane <= 8) return launch_persistent(reshape_pipelined_kernel<kF32, 8>, a, stream, 2 * a.num_tokens);
-    return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream, 2 * a.num_tokens);
+    if (per_lane <= 1) return launch_persistent(reshape_pipelined_kernel<Group<kF32>, 1>, a, stream, rows);
+    if (per_lane <= 2) return launch_persistent(reshape_pipelined_kernel<Group<kF32>, 2>, a, stream, rows);
+    if (per_lane <= 4) return launch_persistent(reshape_pipelined_kernel<Group<kF32>, 4>, a, stream, rows);
+    if (per_lane <= 8) return launch_persistent(reshape_pipelined_kernel<Group<kF32>, 8>, a, stream, rows);
+    return launch_persistent(reshape_rowloop_kernel<kF32>, a, stream, rows);
 }
 
 template <bool kF32>

@@ -39,24 +39,32 @@ def _oracle(key_host, value_host, slots_np, nb, bs, n_kv, hd, ks, vs, src=oracle
     return kc, vc
 
 
-def test_every_bf16_value_at_many_scales():
+# Row layouts (n_kv, head_dim): 8-element rows take the 8-wide kernel; 512- and 1024-element
+# rows with 32-byte aligned sources take the wide kernel (16 elements per lane, one unit or two)
+ROW_LAYOUTS = [(1, 8), (4, 128), (8, 128)]
+
+
+@pytest.mark.parametrize("n_kv,hd", ROW_LAYOUTS)
+def test_every_bf16_value_at_many_scales(n_kv, hd):
     bits = np.arange(1 << 16, dtype=np.uint16)
-    k = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(8192, 1, 8)
-    v = torch.from_numpy(bits[::-1].view(np.int16).copy()).view(torch.bfloat16).reshape(8192, 1, 8)
-    slots = torch.arange(8192, dtype=torch.int64)
+    n = bits.size // (n_kv * hd)
+    k = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).reshape(n, n_kv, hd)
+    v = torch.from_numpy(bits[::-1].view(np.int16).copy()).view(torch.bfloat16).reshape(n, n_kv, hd)
+    slots = torch.arange(n, dtype=torch.int64)
     kd, vd, sd = k.cuda(), v.cuda(), slots.cuda()
     for s in SCALES:
         s32 = float(np.float32(s))
-        kc, vc = _run(kd, vd, sd, 8192, 1, s32, -s32)
-        ko, vo = _oracle(gpu_util.to_u16(k), gpu_util.to_u16(v), slots.numpy(), 8192, 1, 1, 8, s32,
-                         -s32)
+        kc, vc = _run(kd, vd, sd, n, 1, s32, -s32)
+        ko, vo = _oracle(gpu_util.to_u16(k), gpu_util.to_u16(v), slots.numpy(), n, 1, n_kv, hd,
+                         s32, -s32)
         bad = np.nonzero(kc.ravel() != ko.ravel())[0]
         assert bad.size == 0, (s, [(hex(int(bits[i])), hex(kc.ravel()[i]), hex(ko.ravel()[i]))
                                    for i in bad[:8]])
         np.testing.assert_array_equal(vc, vo)
 
 
-def test_float32_source_bit_patterns():
+@pytest.mark.parametrize("n_kv,hd", ROW_LAYOUTS)
+def test_float32_source_bit_patterns(n_kv, hd):
     rng = np.random.Generator(np.random.PCG64(21))
     x = rng.integers(0, 1 << 32, size=1 << 21, dtype=np.uint64).astype(np.uint32).view(np.float32)
     y = (rng.standard_normal(1 << 21) * np.exp2(rng.uniform(-14, 12, 1 << 21))).astype(np.float32)
@@ -64,18 +72,37 @@ def test_float32_source_bit_patterns():
                         -1e-45, 2.0 ** -10, 3 * 2.0 ** -10, 432.0, 3.4e38, -3.4e38], np.float32)
     neg_nan = np.array([0xFFC00000, 0xFF800001, 0x7F800001], np.uint32).view(np.float32)
     data = np.concatenate([x, y, special, neg_nan])
-    data = np.concatenate([data, np.zeros((-data.size) % 8, np.float32)])
-    n = data.size // 8
-    key = torch.from_numpy(data.reshape(n, 1, 8).copy())
+    row = n_kv * hd
+    data = np.concatenate([data, np.zeros((-data.size) % row, np.float32)])
+    n = data.size // row
+    key = torch.from_numpy(data.reshape(n, n_kv, hd).copy())
     slots = torch.arange(n, dtype=torch.int64)
     for s in (0.05, 0.03, 1.0, -0.125, 2.0 ** -60, -2.0 ** 60, 1e-25, 3.7e22):
         s32 = float(np.float32(s))
         kc, vc = _run(key.cuda(), key.cuda(), slots.cuda(), n, 1, s32, s32)
-        ko, _ = _oracle(key.numpy(), key.numpy(), slots.numpy(), n, 1, 1, 8, s32, s32, src=oracle.F32)
+        ko, _ = _oracle(key.numpy(), key.numpy(), slots.numpy(), n, 1, n_kv, hd, s32, s32,
+                        src=oracle.F32)
         bad = np.nonzero(kc.ravel() != ko.ravel())[0]
         assert bad.size == 0, (s, [(hex(int(data.view(np.uint32)[i])), hex(kc.ravel()[i]),
                                     hex(ko.ravel()[i])) for i in bad[:8]])
         np.testing.assert_array_equal(vc, kc)
+
+
+def test_rows_16_but_not_32_byte_aligned_take_the_8_wide_kernel():
+    # a source starting 16 bytes into an allocation: the wide kernel's 32-byte loads would be
+    # misaligned, so the call must fall back to 16-byte loads and give the same bytes
+    torch.manual_seed(6)
+    n, n_kv, hd = 257, 8, 128
+    buf = (torch.randn(n * n_kv * hd + 8, device="cuda") * 20).to(torch.bfloat16)
+    key = buf[8:].view(n, n_kv, hd)
+    assert key.data_ptr() % 32 == 16
+    val = torch.flip(key, dims=[0]).contiguous()
+    slots = torch.randperm(40 * 16, device="cuda")[:n].to(torch.int64)
+    kc, vc = _run(key, val, slots, 40, 16, 0.05, -0.04)
+    ko, vo = _oracle(gpu_util.to_u16(key), gpu_util.to_u16(val), slots.cpu().numpy(), 40, 16,
+                     n_kv, hd, 0.05, -0.04)
+    np.testing.assert_array_equal(kc, ko)
+    np.testing.assert_array_equal(vc, vo)
 
 
 def test_special_values_follow_the_page_encoder():
