@@ -75,6 +75,10 @@ def _load():
                                                          i32, P, i32, i32, i32, i32, i32, i32, f64,
                                                          f32, f32]
         lib.kvo_paged_decode_attention_mixed.restype = u32
+        lib.kvo_paged_attention_multi_mixed.argtypes = [P, P, P, P, ctypes.c_int, P, ctypes.c_int,
+                                                        P, i32, P, i32, i32, i32, i32, i32, i32,
+                                                        f64, f32, f32]
+        lib.kvo_paged_attention_multi_mixed.restype = u32
         lib.kvo_paged_decode_attention_pairs.argtypes = [P, P, i32, P, P, P, P, i32, P, i32, i32,
                                                          i32, i32, i32, f64, f32, f32]
         lib.kvo_paged_decode_attention_pairs.restype = u32
@@ -295,6 +299,32 @@ def paged_decode_attention_mixed(query, key_cache: np.ndarray, k_kind: int,
         _ptr(out), _ptr(q), _ptr(np.ascontiguousarray(key_cache)), k_kind,
         _ptr(np.ascontiguousarray(value_cache)), v_kind, _ptr(bt), bt.shape[1], _ptr(sl),
         num_seqs, n_q, n_kv, hd, bs, num_blocks, float(sm_scale), float(np.float32(k_scale)),
+        float(np.float32(v_scale)))
+    return out, int(st)
+
+
+def paged_attention_multi_mixed(query, query_start_loc: np.ndarray, key_cache: np.ndarray,
+                                k_kind: int, value_cache: np.ndarray, v_kind: int,
+                                block_tables: np.ndarray, seq_lens: np.ndarray, k_scale: float,
+                                v_scale: float, sm_scale: float = 0.0):
+    """Causal multi-query attention with a per-side cache kind (E4M3 or CACHE_BF16), in
+    double; query [total_q, n_q, hd] (bf16) with sequence b's rows at query_start_loc[b];
+    returns (out float64 like query, status)."""
+    q = _as_u16(query)
+    total_q, n_q, hd = q.shape
+    num_blocks, bs, n_kv, hd2 = key_cache.shape
+    assert hd2 == hd and n_q % n_kv == 0
+    for c, kind in ((key_cache, k_kind), (value_cache, v_kind)):
+        assert c.dtype == (np.uint8 if kind == E4M3 else np.uint16)
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    assert qsl.size == sl.size + 1 and qsl[-1] == total_q
+    out = np.zeros((total_q, n_q, hd), dtype=np.float64)
+    st = _load().kvo_paged_attention_multi_mixed(
+        _ptr(out), _ptr(q), _ptr(qsl), _ptr(np.ascontiguousarray(key_cache)), k_kind,
+        _ptr(np.ascontiguousarray(value_cache)), v_kind, _ptr(bt), bt.shape[1], _ptr(sl), sl.size,
+        n_q, n_kv, hd, bs, num_blocks, float(sm_scale), float(np.float32(k_scale)),
         float(np.float32(v_scale)))
     return out, int(st)
 

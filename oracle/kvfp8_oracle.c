@@ -586,6 +586,48 @@ uint32_t kvo_paged_attention_multi(double *out, const uint16_t *query,
     return status;
 }
 
+/* Multi-query (causal) attention with a per-side cache kind: the two forms above put
+ * together.  [P1] tests/test-fp8.cpp check_fp8_attention runs its batch of new tokens
+ * (each attending to every past token up to itself) over a cache with K only, V only or
+ * both in FP8, the other side at 16 bits and unscaled.  Sequence b's query token j sits at
+ * position p = len - n_b + j and its output is the single-query decode over the cache
+ * prefix 0..p, so each row is kvo_paged_decode_attention_mixed of that one query with
+ * sequence length p + 1 (no token past p is visible). */
+uint32_t kvo_paged_attention_multi_mixed(double *out, const uint16_t *query,
+                                         const int32_t *query_start_loc, const void *key_cache,
+                                         int k_kind, const void *value_cache, int v_kind,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+                                         int32_t n_kv, int32_t head_dim, int32_t block_size,
+                                         int32_t num_blocks, double sm_scale, float k_scale,
+                                         float v_scale)
+{
+    if ((k_kind == 0 && !kvo_scale_ok(k_scale)) || (v_kind == 0 && !kvo_scale_ok(v_scale)))
+        return KVO_BAD_SCALE;
+    uint32_t status = 0;
+    for (int32_t b = 0; b < num_seqs; ++b) {
+        int32_t len = seq_lens[b];
+        if (len > max_blocks_per_seq * block_size) {
+            status |= KVO_BAD_BLOCK;
+            len = max_blocks_per_seq * block_size;
+        }
+        const int32_t q0 = query_start_loc[b];
+        const int32_t nb = query_start_loc[b + 1] - q0;
+        if (nb > len)
+            status |= KVO_BAD_BLOCK;
+        for (int32_t j = 0; j < nb; ++j) {
+            const int32_t p = len - nb + j;  /* attends to tokens 0..p */
+            const int32_t visible = p + 1 > 0 ? p + 1 : 0;
+            const int64_t row = (int64_t)(q0 + j) * n_q * head_dim;
+            status |= kvo_paged_decode_attention_mixed(
+                out + row, query + row, key_cache, k_kind, value_cache, v_kind,
+                block_tables + (int64_t)b * max_blocks_per_seq, max_blocks_per_seq, &visible, 1,
+                n_q, n_kv, head_dim, block_size, num_blocks, sm_scale, k_scale, v_scale);
+        }
+    }
+    return status;
+}
+
 /* Attention for a chosen list of (sequence, q head) pairs only, for sampled
  * checks at full size: pairs holds n_pairs (seq, head) int32 pairs and out is
  * [n_pairs][head_dim]. */

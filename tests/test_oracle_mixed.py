@@ -87,3 +87,56 @@ def test_library_softmax_on_each_mix():
                 s = K[:, h // 4] @ qf[b, h] / math.sqrt(32)
                 np.testing.assert_allclose(out[b, h], scipy.special.softmax(s) @ V[:, h // 4],
                                            rtol=1e-12, atol=1e-14)
+
+
+def _multi_setup(lengths, nbs, seed):
+    k, v, _, bt, slots, nb = _setup(lengths, seed)
+    rng = np.random.default_rng(seed + 100)
+    qsl = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    q = torch.as_tensor(rng.standard_normal((int(qsl[-1]), 8, 32)).astype(np.float32)).to(torch.bfloat16)
+    return k, v, q, bt, slots, nb, qsl
+
+
+def test_multi_mixed_with_a_bf16_side_holding_fp8_values_equals_the_fp8_multi_form():
+    # E4M3 values are exact in bf16: a bf16 side holding dec(code) (scale 1) must give the
+    # all-FP8 causal multi-query result -- a check against the separately pinned FP8 form
+    lengths, nbs = [6, 17, 30], [3, 1, 5]
+    k, v, q, bt, slots, nb, qsl = _multi_setup(lengths, nbs, 5)
+    kc8, vc8 = _caches(nb, (oracle.E4M3, oracle.E4M3))
+    oracle.reshape_and_cache(k, v, kc8, vc8, slots, 4, 1.0, 0.04)
+    DEC = oracle.e4m3_decode_all()
+    as_bf16 = lambda c: (DEC[c].astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)  # noqa: E731
+    assert np.array_equal((as_bf16(kc8).astype(np.uint32) << 16).view(np.float32), DEC[kc8].astype(np.float32))
+    ref, st = oracle.paged_attention_multi(q, qsl, kc8, vc8, bt, np.array(lengths), 1.0, 0.04)
+    assert st == 0
+    got, st = oracle.paged_attention_multi_mixed(q, qsl, as_bf16(kc8), oracle.CACHE_BF16, vc8,
+                                                 oracle.E4M3, bt, np.array(lengths), 123.0, 0.04)
+    assert st == 0
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-15)
+    ref_v, _ = oracle.paged_attention_multi(q, qsl, kc8, vc8, bt, np.array(lengths), 1.0, 1.0)
+    got_v, _ = oracle.paged_attention_multi_mixed(q, qsl, kc8, oracle.E4M3, as_bf16(vc8),
+                                                  oracle.CACHE_BF16, bt, np.array(lengths), 1.0, 9.0)
+    np.testing.assert_allclose(got_v, ref_v, rtol=1e-12, atol=1e-15)
+
+
+def test_multi_mixed_is_causal_and_its_first_token_sees_one_key():
+    lengths, nbs = [12, 9], [12, 4]
+    k, v, q, bt, slots, nb, qsl = _multi_setup(lengths, nbs, 6)
+    kinds = (oracle.CACHE_BF16, oracle.E4M3)
+    kc, vc = _caches(nb, kinds)
+    oracle.reshape_and_cache_mixed(k, v, kc, kinds[0], vc, kinds[1], slots, 4, 0.05, 0.25)
+    out, st = oracle.paged_attention_multi_mixed(q, qsl, kc, kinds[0], vc, kinds[1], bt,
+                                                 np.array(lengths), 0.05, 0.25)
+    assert st == 0
+    # sequence 0's first query token sits at position 0: its output is V_0 itself
+    DEC = oracle.e4m3_decode_all()
+    v0 = 0.25 * DEC[vc.reshape(-1, 2, 32)[slots[0]]]
+    for h in range(8):
+        np.testing.assert_allclose(out[0, h], v0[h // 4], rtol=0, atol=1e-15)
+    # rows past a token's position do not change its output
+    fk = kc.reshape(-1, 2, 32)
+    fk[slots[12 + 8]] ^= 0x1234  # sequence 1's last token (position 8)
+    out2, _ = oracle.paged_attention_multi_mixed(q, qsl, kc, kinds[0], vc, kinds[1], bt,
+                                                 np.array(lengths), 0.05, 0.25)
+    np.testing.assert_array_equal(out2[:12 + 3], out[:12 + 3])  # every row before it
+    assert not np.array_equal(out2[12 + 3], out[12 + 3])      # the row at position 8 sees it
