@@ -12,12 +12,14 @@ from .binding import (  # noqa: F401
     DEV_BAD_SCALE,
     DEV_BAD_SLOT,
     DEV_TIMEOUT,
+    ERR_UNSUPPORTED,
     KvFp8Error,
     LIB,
     LIB_PATH,
     check_scale_host,
     dequant,
     paged_attention_multi,
+    paged_attention_multi_mixed,
     paged_attention_multi_workspace_size,
     paged_decode_attention,
     paged_decode_attention_mixed,

@@ -13,6 +13,9 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIB_DIR, "libkvfp8.so")
+# test-only variant for the bounded-wait timeout test (never loaded by the package)
+WITHHOLD_LIB = os.path.join(LIB_DIR, "libkvfp8_withhold.so")
+WITHHOLD_DEFINE = "-DKVFP8_TEST_WITHHOLD_FIRST_CHUNK=1"
 HEADER = os.path.join(ROOT, "include", "kvfp8.h")
 
 SOURCES = ["kvfp8_api.cu", "reshape_and_cache.cu", "paged_decode.cu", "paged_decode_mixed.cu",
@@ -42,6 +45,27 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(p) > t for p in inputs)
 
 
+def _compile(nvcc: str, src: str, obj: str, defines=(), verbose: bool = False) -> str:
+    extra = os.environ.get("KVFP8_NVCC_EXTRA", "").split()
+    cmd = [nvcc, *NVCC_FLAGS, *extra, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+    if verbose and (r.stdout or r.stderr):
+        sys.stderr.write(r.stdout + r.stderr)
+    return obj
+
+
+def _link(nvcc: str, objs, lib: str) -> str:
+    tmp = lib + f".tmp{os.getpid()}"
+    cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link the library if it is missing or older than its sources."""
     if not force and not _stale(LIB):
@@ -49,27 +73,28 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJ_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
-    extra = os.environ.get("KVFP8_NVCC_EXTRA", "").split()
-
-    def compile_one(src: str) -> str:
-        obj = os.path.join(OBJ_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
-        if verbose and (r.stdout or r.stderr):
-            sys.stderr.write(r.stdout + r.stderr)
-        return obj
-
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+        objs = list(ex.map(lambda src: _compile(nvcc, src, os.path.join(OBJ_DIR, src.replace(".cu", ".o")),
+                                                verbose=verbose), SOURCES))
+    return _link(nvcc, objs, LIB)
+
+
+def build_withhold_variant(verbose: bool = False) -> str:
+    """A test-only copy of the library whose single-query decode kernels withhold the copy
+    of every CTA's first chunk and give up any wait after about 1e5 cycles, so that the
+    bounded-wait timeout path can be driven on a GPU with no copy ever in flight.  Built
+    from the same sources (paged_decode.cu recompiled with one define, the other units
+    reused); the package never loads it."""
+    build(verbose=verbose)
+    if not _stale(WITHHOLD_LIB):
+        return WITHHOLD_LIB
+    nvcc = _nvcc()
+    wdir = os.path.join(OBJ_DIR, "withhold")
+    os.makedirs(wdir, exist_ok=True)
+    objs = [os.path.join(OBJ_DIR, src.replace(".cu", ".o")) for src in SOURCES]
+    objs[SOURCES.index("paged_decode.cu")] = _compile(
+        nvcc, "paged_decode.cu", os.path.join(wdir, "paged_decode.o"), (WITHHOLD_DEFINE,), verbose)
+    return _link(nvcc, objs, WITHHOLD_LIB)
 
 
 if __name__ == "__main__":

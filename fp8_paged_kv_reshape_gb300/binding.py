@@ -37,6 +37,7 @@ ABI_FUNCTIONS = (
     "kvfp8_paged_attention_multi_workspace_size",
     "kvfp8_reshape_and_cache_mixed",
     "kvfp8_paged_decode_attention_mixed",
+    "kvfp8_paged_attention_multi_mixed",
     "kvfp8_dequant",
     "kvfp8_check_scale_host",
     "kvfp8_status_string",
@@ -87,6 +88,11 @@ def _load() -> ctypes.CDLL:
                                                        i32, P, i32, i32, i32, i32, i32, i32, f32,
                                                        P, P, ctypes.c_int, P, sz, P, P]
     lib.kvfp8_paged_decode_attention_mixed.restype = ctypes.c_int
+    lib.kvfp8_paged_attention_multi_mixed.argtypes = [P, P, P, i32, i32, P, ctypes.c_int, P,
+                                                      ctypes.c_int, P, i32, P, i32, i32, i32,
+                                                      i32, i32, i32, f32, P, P, ctypes.c_int, P,
+                                                      sz, P, P]
+    lib.kvfp8_paged_attention_multi_mixed.restype = ctypes.c_int
     lib.kvfp8_dequant.argtypes = [P, ctypes.c_int, P, i64, P, ctypes.c_int, P]
     lib.kvfp8_dequant.restype = ctypes.c_int
     lib.kvfp8_check_scale_host.argtypes = [f32]
@@ -417,6 +423,44 @@ def paged_decode_attention_mixed(query: torch.Tensor, key_cache: torch.Tensor,
         float(sm_scale), _ptr(k_scale), _ptr(v_scale), sdt, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     _check(rc, "kvfp8_paged_decode_attention_mixed")
+    return out
+
+
+def paged_attention_multi_mixed(query: torch.Tensor, query_start_loc: torch.Tensor,
+                                max_query_len: int, key_cache: torch.Tensor,
+                                value_cache: torch.Tensor, block_tables: torch.Tensor,
+                                seq_lens: torch.Tensor, k_scale: torch.Tensor | None = None,
+                                v_scale: torch.Tensor | None = None, sm_scale: float = 0.0,
+                                out: torch.Tensor | None = None,
+                                workspace: torch.Tensor | None = None,
+                                status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvfp8_paged_attention_multi_mixed: causal multi-query attention where each cache's
+    dtype picks its side's format (uint8 = E4M3, scaled; bfloat16 = unscaled)."""
+    if query.dtype != torch.bfloat16 or query.dim() != 3 or not query.is_contiguous():
+        raise ValueError("query must be a contiguous bf16 [rows, n_q, head_dim] tensor")
+    rows, n_q, hd = query.shape
+    num_seqs = seq_lens.numel()
+    if query_start_loc.dtype != torch.int32 or query_start_loc.numel() != num_seqs + 1 or \
+            not query_start_loc.is_contiguous():
+        raise ValueError("query_start_loc must be a contiguous int32 [num_seqs + 1] tensor")
+    kk, vk = _check_mixed_caches(key_cache, value_cache)
+    if key_cache.shape[3] != hd:
+        raise ValueError("caches must be [num_blocks, block_size, n_kv, head_dim]")
+    num_blocks, bs, n_kv, _ = key_cache.shape
+    _check_tables(block_tables, seq_lens, num_seqs)
+    if out is None:
+        out = torch.empty_like(query)
+    need = paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, hd, max_query_len)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=query.device)
+    sdt = _scale_args(k_scale, v_scale)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = LIB.kvfp8_paged_attention_multi_mixed(
+        _ptr(out), _ptr(query), _ptr(query_start_loc), rows, max_query_len, _ptr(key_cache), kk,
+        _ptr(value_cache), vk, _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+        num_seqs, n_q, n_kv, hd, bs, num_blocks, float(sm_scale), _ptr(k_scale), _ptr(v_scale),
+        sdt, _ptr(workspace), ws_bytes, _ptr(status), _stream(stream))
+    _check(rc, "kvfp8_paged_attention_multi_mixed")
     return out
 
 

@@ -362,15 +362,17 @@ kvfp8_status kvfp8_paged_decode_attention_mixed(
             num_seqs, n_q, n_kv, head_dim, block_size, num_blocks, sm_scale, k_scale, v_scale,
             scale_dtype, workspace, workspace_bytes, status, stream);
     if (!dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
-    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || n_q / n_kv > 16 ||
-        num_blocks < 1 || max_blocks_per_seq < 1)
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || num_blocks < 1 ||
+        max_blocks_per_seq < 1)
         return KVFP8_ERR_SHAPE;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
     if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
     if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
         static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
         return KVFP8_ERR_SHAPE;
-    if (k_cache_dtype == v_cache_dtype || head_dim == 256) return KVFP8_ERR_UNSUPPORTED;
+    if (k_cache_dtype == v_cache_dtype ||
+        !kvfp8::mixed_uses_decode_kernel(n_q, n_kv, head_dim, 1))
+        return KVFP8_ERR_UNSUPPORTED;
     if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
     if (num_seqs == 0) return KVFP8_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !workspace)
@@ -404,6 +406,74 @@ kvfp8_status kvfp8_paged_decode_attention_mixed(
     d.qsl = nullptr;
     d.qmax = 1;
     d.qrows = num_seqs;
+    d.k_bf16 = k_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
+    d.v_bf16 = v_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
+    return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kvfp8_status kvfp8_paged_attention_multi_mixed(
+    void *out, const void *query, const int32_t *query_start_loc, int32_t num_query_rows,
+    int32_t max_query_len, const void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    const void *value_cache, kvfp8_cache_dtype v_cache_dtype, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+    int32_t n_kv, int32_t head_dim, int32_t block_size, int32_t num_blocks, float sm_scale,
+    const void *k_scale, const void *v_scale, kvfp8_dtype scale_dtype, void *workspace,
+    size_t workspace_bytes, uint32_t *status, kvfp8_stream_t stream) {
+    if (!cache_dtype_ok(k_cache_dtype) || !cache_dtype_ok(v_cache_dtype)) return KVFP8_ERR_DTYPE;
+    if (k_cache_dtype == KVFP8_CACHE_E4M3 && v_cache_dtype == KVFP8_CACHE_E4M3)
+        return kvfp8_paged_attention_multi(
+            out, query, query_start_loc, num_query_rows, max_query_len,
+            static_cast<const uint8_t *>(key_cache), static_cast<const uint8_t *>(value_cache),
+            block_tables, max_blocks_per_seq, seq_lens, num_seqs, n_q, n_kv, head_dim, block_size,
+            num_blocks, sm_scale, k_scale, v_scale, scale_dtype, workspace, workspace_bytes, status,
+            stream);
+    if (!dtype_ok(scale_dtype)) return KVFP8_ERR_DTYPE;
+    if (num_seqs < 0 || n_q < 1 || n_kv < 1 || n_q % n_kv != 0 || max_query_len < 1 ||
+        num_query_rows < 0 || num_blocks < 1 || max_blocks_per_seq < 1)
+        return KVFP8_ERR_SHAPE;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVFP8_ERR_SHAPE;
+    if (!block_size_ok_for_decode(block_size)) return KVFP8_ERR_SHAPE;
+    if (static_cast<int64_t>(num_blocks) * block_size > 0x7FFFFFFFLL ||
+        static_cast<int64_t>(max_blocks_per_seq) * block_size > 0x7FFFFFFFLL)
+        return KVFP8_ERR_SHAPE;
+    if (k_cache_dtype == v_cache_dtype ||
+        !kvfp8::mixed_uses_decode_kernel(n_q, n_kv, head_dim, max_query_len))
+        return KVFP8_ERR_UNSUPPORTED;
+    if (std::isnan(sm_scale) || std::isinf(sm_scale)) return KVFP8_ERR_SCALE;
+    if (num_seqs == 0) return KVFP8_OK;
+    if (!out || !query || !query_start_loc || !key_cache || !value_cache || !block_tables ||
+        !seq_lens || !workspace)
+        return KVFP8_ERR_NULL;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) ||
+        !aligned16(value_cache) || !aligned(block_tables, 4) || !aligned(seq_lens, 4) ||
+        !aligned(query_start_loc, 4) || !aligned16(workspace))
+        return KVFP8_ERR_ALIGN;
+    if (workspace_bytes <
+        kvfp8_paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, head_dim, max_query_len))
+        return KVFP8_ERR_WORKSPACE;
+    kvfp8::DecodeArgs d;
+    d.out = out;
+    d.query = query;
+    d.key_cache = static_cast<const uint8_t *>(key_cache);
+    d.value_cache = static_cast<const uint8_t *>(value_cache);
+    d.block_tables = block_tables;
+    d.max_blocks_per_seq = max_blocks_per_seq;
+    d.seq_lens = seq_lens;
+    d.num_seqs = num_seqs;
+    d.n_q = n_q;
+    d.n_kv = n_kv;
+    d.head_dim = head_dim;
+    d.block_size = block_size;
+    d.num_blocks = num_blocks;
+    d.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    d.k_scale = k_scale;
+    d.v_scale = v_scale;
+    d.scale_dtype = scale_dtype;
+    d.workspace = workspace;
+    d.status = status;
+    d.qsl = query_start_loc;
+    d.qmax = max_query_len;
+    d.qrows = num_query_rows;
     d.k_bf16 = k_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
     d.v_bf16 = v_cache_dtype == KVFP8_CACHE_BF16 ? 1 : 0;
     return from_cuda(kvfp8::launch_paged_decode(d, reinterpret_cast<cudaStream_t>(stream)));

@@ -161,6 +161,9 @@ DecodeWorkspace decode_workspace_layout(int32_t num_seqs, int32_t rows, int32_t 
 cudaError_t launch_paged_decode(const DecodeArgs &a, cudaStream_t stream);
 // The mixed-dtype instances (exactly one of k_bf16 / v_bf16 set); called by the above.
 cudaError_t launch_paged_decode_mixed(const DecodeArgs &a, cudaStream_t stream);
+// True when the split-KV kernel has a mixed-dtype instance for this shape (up to 16 score
+// columns per kv head, 8 at head_dim 256); the tensor-core kernel has none.
+bool mixed_uses_decode_kernel(int32_t n_q, int32_t n_kv, int32_t head_dim, int32_t max_query_len);
 
 // Multi-query (causal) attention on the tensor cores (tcgen05): long query chunks, or kv-head
 // counts the split-KV decode kernel does not cover.  Needs no workspace.

@@ -10,14 +10,15 @@
 //  * Work split: the cache is cut into 16-token chunks; the chunks of all sequences are
 //    laid end to end and each CTA of a fixed grid (one or two per SM; fewer when there
 //    are fewer chunks than CTAs) takes an equal contiguous, non-empty range, whatever
-//    the length mix.  A sequence that lies inside one CTA is
-//    finished there; otherwise each CTA writes a partial (normalized o, log2-sum-exp) and
-//    a combine kernel merges them, one thread per four output dims.  Partial (seq, cta)
-//    pairs are stored at index seq+cta, which is unique because both grow monotonically
-//    along the chunk order.  A one-CTA plan kernel computes the chunk prefix over the
-//    sequences first, and one record per CTA (its chunk range and first sequence, so a
-//    CTA starts with one load).  Plan -> decode -> combine are chained as programmatic
-//    dependent launches, so each grid's launch and prologue overlap its predecessor.
+//    the length mix.  A sequence that lies inside one CTA is finished there; otherwise
+//    each CTA writes a partial (normalized o, log2-sum-exp) and a combine kernel merges
+//    them.  Partial (seq, cta) pairs are stored at index seq+cta, which is unique because
+//    both grow monotonically along the chunk order.  A one-CTA plan kernel computes the
+//    chunk prefix over the sequences first, and one record per CTA (its chunk range and
+//    first sequence, so a CTA starts with one read).  Plan -> decode -> combine are chained
+//    as programmatic dependent launches, so each grid's launch and prologue overlap its
+//    predecessor; while a decode CTA waits for the plan it prefetches its slice of the
+//    block tables into L2, and its producer prefetches each next sequence's query rows.
 //  * One CTA = one producer warp + one consumer warp per kv head of its head group (the
 //    kv heads split into equal groups of at most 8, a second grid dimension; one group
 //    when n_kv <= 8).  A 16-token chunk of a block holds all kv heads of those tokens (16
@@ -64,7 +65,16 @@ namespace {
 
 constexpr int kMaxKvHeads = 8;                 // consumer warps per CTA
 constexpr int kThreadsMax = 32 * (kMaxKvHeads + 1);
+#ifdef KVFP8_TEST_WITHHOLD_FIRST_CHUNK
+// Test-only build (a separate library file, never the package's): every CTA's producer
+// withholds the copy of its first chunk and every wait gives up after ~1e5 cycles, so the
+// consumers' bounded waits run out while no copy is in flight, driving the timeout path.
+constexpr long long kWaitCycles = 100000LL;
+constexpr bool kWithholdFirstChunk = true;
+#else
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+constexpr bool kWithholdFirstChunk = false;
+#endif
 
 struct ChunkMeta {
     int32_t seq;
@@ -75,10 +85,9 @@ struct ChunkMeta {
 enum : int32_t { kFirst = 1, kLast = 2, kDirect = 4, kDone = 8 };
 
 // The plan's record for one decode CTA: chunk range [lo, hi) (empty past the effective
-// grid), the sequence s holding chunk lo, its chunk range [cs, ce) and length L, and the
-// total chunk count T.
+// grid), the sequence s holding chunk lo, its chunk range [cs, ce) and length L.
 struct CtaPlan {
-    int32_t lo, hi, s, cs, ce, L, T, pad;
+    int32_t lo, hi, s, cs, ce, L, pad0, pad1;
 };
 
 struct KernelArgs {
@@ -360,7 +369,7 @@ plan_kernel(const int32_t *seq_lens, const int32_t *qsl, int32_t qmax, int32_t q
     const int64_t T = total;
     const int64_t P = T < num_ctas ? T : num_ctas;
     for (int c = tid; c < num_ctas; c += blockDim.x) {
-        CtaPlan r = {0, 0, 0, 0, 0, 0, total, 0};
+        CtaPlan r = {0, 0, 0, 0, 0, 0, 0, 0};
         if (c < P) {
             r.lo = static_cast<int32_t>(static_cast<int64_t>(c) * T / P);
             r.hi = static_cast<int32_t>(static_cast<int64_t>(c + 1) * T / P);
@@ -386,103 +395,26 @@ __device__ __forceinline__ int seq_chunks(const KernelArgs &a, int i, int &L) {
     return nq > 0 ? (L + kChunkTokens - 1) / kChunkTokens : 0;
 }
 
-// Sequences one thread holds in registers while a CTA plans its own range.
-constexpr int kPlanPerThread = 16;
-
-// The plan of one decode CTA worked out by the CTA itself, for batches of at most
-// blockDim.x * kPlanPerThread sequences (the launcher runs the plan kernel otherwise).
-// Every thread takes a contiguous run of up to kPlanPerThread sequences, loads their lengths
-// (independent loads, all in flight together), and a block-wide scan of the per-thread chunk
-// sums gives every sequence's first chunk and the total T.  The thread whose run holds chunk
-// lo = c*T/P writes the record.  CTA (0, 0) also writes the chunk prefix for the combine
-// kernel and raises the status bits for bad lengths or query ranges; the output rows of
-// empty sequences are zeroed by CTA (i mod gridDim.x, 0).  All threads must call it.
-__device__ __forceinline__ CtaPlan plan_in_cta(const KernelArgs &a, int32_t *cstart_out,
-                                            __nv_bfloat16 *out, int out_row_elems) {
-    __shared__ int32_t warp_sum[32];
-    __shared__ CtaPlan rec;
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
-    const int nw = (nt + 31) >> 5;
-    const int k = (a.num_seqs + nt - 1) / nt;  // sequences per thread (<= kPlanPerThread)
-    const int s0 = tid * k;
-    const bool lead = blockIdx.x == 0 && blockIdx.y == 0;
-    int n[kPlanPerThread], len[kPlanPerThread];
-    int sum = 0;
-#pragma unroll
-    for (int j = 0; j < kPlanPerThread; ++j) {
-        n[j] = 0;
-        len[j] = 0;
-        const int i = s0 + j;
-        if (j < k && i < a.num_seqs) {
-            const int raw = a.seq_lens[i];
-            n[j] = seq_chunks(a, i, len[j]);
-            if (lead) {
-                if (raw < 0 || raw > a.max_len) flag(a.status, KVFP8_DEV_BAD_BLOCK);
-                if (a.qsl) {
-                    const int nq = query_range(a.qsl, i, a.rows_per_seq / a.n_q, a.qrows).count;
-                    if (nq != a.qsl[i + 1] - a.qsl[i] || nq > len[j])
-                        flag(a.status, KVFP8_DEV_BAD_BLOCK);
-                }
-            }
-            if (n[j] == 0 && blockIdx.y == 0 && i % gridDim.x == blockIdx.x) {
-                // an empty sequence: no CTA visits it, so its output rows are zeroed here
-                const QueryRange qr = a.qsl ? query_range(a.qsl, i, a.rows_per_seq / a.n_q, a.qrows)
-                                            : QueryRange{i, 1};
-                uint4 *rows = reinterpret_cast<uint4 *>(out + static_cast<int64_t>(qr.q0) * out_row_elems);
-                for (int64_t e = 0; e < static_cast<int64_t>(qr.count) * out_row_elems / 8; ++e)
-                    rows[e] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            sum += n[j];
-        }
+// Bring the query rows a CTA's consumers will read for sequence s (its head group's rows,
+// or the sequence's query tokens in the multi-query form, at most 32 KiB) into L2 ahead of
+// their first chunk: the producer runs up to a ring of chunks ahead of the consumers, so a
+// consumer starting a sequence finds its q in L2 instead of waiting on HBM.
+template <int HD>
+__device__ __forceinline__ void prefetch_q(const KernelArgs &a, int s, int h0, int lane) {
+    const __nv_bfloat16 *q;
+    int64_t bytes;
+    if (a.qsl != nullptr) {
+        const QueryRange qr = query_range(a.qsl, s, a.rows_per_seq / a.n_q, a.qrows);
+        q = a.query + static_cast<int64_t>(qr.q0) * a.n_q * HD;
+        bytes = static_cast<int64_t>(qr.count) * a.n_q * HD * 2;
+        bytes = bytes < 32768 ? bytes : 32768;
+    } else {
+        q = a.query + (static_cast<int64_t>(s) * a.n_q + h0 * a.group) * HD;
+        bytes = static_cast<int64_t>(a.hpc) * a.group * HD * 2;
     }
-    // exclusive scan of the per-thread sums over the block
-    int x = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) warp_sum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = lane < nw ? warp_sum[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-            if (lane >= o) w += y;
-        }
-        warp_sum[lane] = w;  // inclusive over warps
-    }
-    __syncthreads();
-    const int before = (warp > 0 ? warp_sum[warp - 1] : 0) + x - sum;
-    const int64_t T = warp_sum[nw - 1];
-    const int64_t P = T < a.num_ctas ? T : a.num_ctas;
-    const int c = blockIdx.x;
-    CtaPlan r = {0, 0, 0, 0, 0, 0, static_cast<int32_t>(T), 0};
-    if (tid == 0) rec = r;
-    __syncthreads();
-    const int64_t lo = c < P ? static_cast<int64_t>(c) * T / P : -1;
-    int run = before;
-#pragma unroll
-    for (int j = 0; j < kPlanPerThread; ++j) {
-        const int i = s0 + j;
-        if (j < k && i < a.num_seqs) {
-            if (lead) cstart_out[i] = run;
-            if (n[j] > 0 && run <= lo && lo < run + n[j]) {
-                r.lo = static_cast<int32_t>(lo);
-                r.hi = static_cast<int32_t>(static_cast<int64_t>(c + 1) * T / P);
-                r.s = i;
-                r.cs = run;
-                r.ce = run + n[j];
-                r.L = len[j];
-                rec = r;  // exactly one thread's run holds chunk lo
-            }
-            run += n[j];
-        }
-    }
-    if (lead && tid == 0) cstart_out[a.num_seqs] = static_cast<int32_t>(T);
-    __syncthreads();
-    return rec;
+    const char *p = reinterpret_cast<const char *>(q);
+    for (int64_t off = static_cast<int64_t>(lane) * 128; off < bytes; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p + off));
 }
 
 // The CTA whose chunk range contains chunk x (ranges are [c*T/P, (c+1)*T/P), P <= T).
@@ -495,50 +427,89 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t T, int64_t P) {
 // dims of one head.  A single pass with a running maximum: the loads of all partials are
 // independent of one another (the loop is unrolled), so they are in flight together.
 // Launched as a programmatic dependent of the decode grid.
-template <int HD>
-__global__ void __launch_bounds__(256) combine_kernel(const KernelArgs a) {
+// kCombineSlices slices of a sequence's parts are merged side by side (256 threads each),
+// then the slices' running states are merged: sequences cut into many parts (few, long
+// sequences over a full grid) get several loads in flight per output element.
+template <int HD, int kCombineSlices>
+__global__ void __launch_bounds__(256 * kCombineSlices) combine_kernel(const KernelArgs a) {
     constexpr int TPH = HD / 4;     // threads per head
     constexpr int HPB = 256 / TPH;  // heads per CTA
+    __shared__ float sm_m[kCombineSlices][256], sm_den[kCombineSlices][256];
+    __shared__ float4 sm_acc[kCombineSlices][256];
     const int seq = blockIdx.x;
-    const int row = blockIdx.y * HPB + threadIdx.x / TPH;  // row of the sequence
-    const int d = (threadIdx.x % TPH) * 4;
+    const int slice = threadIdx.x / 256, t = threadIdx.x % 256;
+    const int row = blockIdx.y * HPB + t / TPH;  // row of the sequence
+    const int d = (t % TPH) * 4;
     pdl_wait();  // the decode grid's partials are visible from here on
     const float sk = a.k_bf16 ? 1.f : load_scale(a.k_scale, a.scale_dtype);
     const float sv = a.v_bf16 ? 1.f : load_scale(a.v_scale, a.scale_dtype);
     const int64_t cs = a.cstart[seq], ce = a.cstart[seq + 1], T = a.cstart[a.num_seqs];
-    if (!scale_ok(sk) || !scale_ok(sv) || row >= a.rows_per_seq) return;
-    if (ce == cs) return;  // empty: zeroed by the plan kernel
-    int64_t out_row = static_cast<int64_t>(seq) * a.n_q + row;
-    if (a.qsl != nullptr) {
-        const QueryRange qr = query_range(a.qsl, seq, a.rows_per_seq / a.n_q, a.qrows);
-        if (row / a.n_q >= qr.count) return;  // past this sequence's queries
-        out_row = static_cast<int64_t>(qr.q0) * a.n_q + row;
-    }
+    if (!scale_ok(sk) || !scale_ok(sv)) return;  // uniform over the CTA
+    if (ce == cs) return;                        // empty: zeroed by the plan kernel
     const int64_t P = min(static_cast<int64_t>(a.num_ctas), T);  // the effective grid
     const int cf = cta_of(cs, T, P), cl = cta_of(ce - 1, T, P);
     if (cf == cl) return;  // finished inside one CTA
-    const int k = cl - cf + 1;
-    const int64_t p0 = static_cast<int64_t>(seq) + cf;
-    const float *lse = a.part_lse + p0 * a.rows_per_seq + row;
-    const float *o = a.part_o + (p0 * a.rows_per_seq + row) * HD + d;
-    const int64_t lse_stride = a.rows_per_seq, o_stride = static_cast<int64_t>(a.rows_per_seq) * HD;
-    // eight parts per batch, every load of a batch issued before the first is used
-    PartMerge mg;
-    for (int c0 = 0; c0 < k; c0 += 8) {
-        float l[8];
-        float4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            l[i] = -INFINITY;
-            if (c0 + i < k) {
-                l[i] = lse[(c0 + i) * lse_stride];
-                v[i] = *reinterpret_cast<const float4 *>(o + (c0 + i) * o_stride);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mg.add(l[i], v[i]);
+    bool valid = row < a.rows_per_seq;
+    int64_t out_row = static_cast<int64_t>(seq) * a.n_q + row;
+    if (valid && a.qsl != nullptr) {
+        const QueryRange qr = query_range(a.qsl, seq, a.rows_per_seq / a.n_q, a.qrows);
+        valid = row / a.n_q < qr.count;  // past this sequence's queries otherwise
+        out_row = static_cast<int64_t>(qr.q0) * a.n_q + row;
     }
-    *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = mg.result(sv);
+    // this slice's parts [c_lo, c_hi) of the sequence's k, eight per batch, every load of a
+    // batch issued before the first is used
+    const int k = cl - cf + 1;
+    const int c_lo = slice * k / kCombineSlices, c_hi = (slice + 1) * k / kCombineSlices;
+    PartMerge mg;
+    if (valid) {
+        const int64_t p0 = static_cast<int64_t>(seq) + cf;
+        const float *lse = a.part_lse + p0 * a.rows_per_seq + row;
+        const float *o = a.part_o + (p0 * a.rows_per_seq + row) * HD + d;
+        const int64_t lse_stride = a.rows_per_seq, o_stride = static_cast<int64_t>(a.rows_per_seq) * HD;
+        for (int c0 = c_lo; c0 < c_hi; c0 += 8) {
+            float l[8];
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                l[i] = -INFINITY;
+                if (c0 + i < c_hi) {
+                    l[i] = lse[(c0 + i) * lse_stride];
+                    v[i] = *reinterpret_cast<const float4 *>(o + (c0 + i) * o_stride);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mg.add(l[i], v[i]);
+        }
+    }
+    sm_m[slice][t] = mg.M;
+    sm_den[slice][t] = mg.den;
+    sm_acc[slice][t] = mg.acc;
+    __syncthreads();
+    if (slice != 0 || !valid) return;
+    // merge the slices' running states (a slice that saw no part has M = -inf, den = 0)
+    PartMerge all;
+#pragma unroll
+    for (int sl = 0; sl < kCombineSlices; ++sl) {
+        const float m = sm_m[sl][t];
+        if (m == -INFINITY) continue;
+        if (m > all.M) {
+            const float r = ex2(all.M - m);  // 0 while all.M is still -inf
+            all.den *= r;
+            all.acc.x *= r;
+            all.acc.y *= r;
+            all.acc.z *= r;
+            all.acc.w *= r;
+            all.M = m;
+        }
+        const float w = ex2(m - all.M);
+        const float4 v = sm_acc[sl][t];
+        all.den += w * sm_den[sl][t];
+        all.acc.x += w * v.x;
+        all.acc.y += w * v.y;
+        all.acc.z += w * v.z;
+        all.acc.w += w * v.w;
+    }
+    *reinterpret_cast<uint2 *>(a.out + out_row * HD + d) = all.result(sv);
 }
 
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
@@ -587,7 +558,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
     }
-    pdl_wait();     // the previous grid's writes (plan, cache, last call's combine) are visible
+    if (warp == hpc && blockIdx.y == 0) {
+        // This CTA's slice of the block tables into L2 while the plan grid runs, so the
+        // table read after the plan hits L2.  The tables are inputs written before this call
+        // (the plan kernel was launched behind that work), and a prefetch returns no data,
+        // so it needs no ordering with the plan.
+        const int64_t bytes = static_cast<int64_t>(a.num_seqs) * a.max_blocks_per_seq * 4;
+        const int64_t per = (bytes + gridDim.x - 1) / gridDim.x;
+        const char *tb = reinterpret_cast<const char *>(a.block_tables);
+        for (int64_t off = blockIdx.x * per + lane * 128; off < min(bytes, (blockIdx.x + 1) * per);
+             off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(tb + off));
+    }
+    pdl_wait();     // the plan grid's records and zeroed rows are visible from here on
     pdl_trigger();  // let the combine grid get launched; it waits for this grid to finish
 
     const float sk = KT16 ? 1.f : load_scale(a.k_scale, a.scale_dtype);
@@ -599,11 +582,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     // Effective grid: at most one CTA per chunk, so that every active CTA's range is
     // non-empty and the CTAs between a sequence's first and last one all hold a part of it;
     // the plan leaves CTAs past it an empty range.
-    const CtaPlan pl = a.cta_plan != nullptr
-                           ? a.cta_plan[blockIdx.x]
-                           : plan_in_cta(a, const_cast<int32_t *>(a.cstart), a.out, a.n_q * HD);
-    if (pl.lo >= pl.hi) return;
-    const int64_t chunk_lo = pl.lo, chunk_hi = pl.hi;
+    const CtaPlan *rec = a.cta_plan + blockIdx.x;
+    const int32_t pl_lo = rec->lo, pl_hi = rec->hi;
+    if (pl_lo >= pl_hi) return;
+    const int64_t chunk_lo = pl_lo, chunk_hi = pl_hi;
     __syncthreads();
 
     if (warp == hpc) {
@@ -613,17 +595,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
         uint32_t phase = 0;
         bool aborted = false;
         if (chunk_lo < chunk_hi) {
-            int s = pl.s;  // sequence holding chunk_lo, its chunks and length (from the plan)
-            int64_t cs = pl.cs, ce = pl.ce;
-            int L = pl.L;
+            int s = rec->s;  // sequence holding chunk_lo, its chunks and length (from the plan)
+            int64_t cs = rec->cs, ce = rec->ce;
+            int L = rec->L;
             int wbase = -1 << 30;  // first block-table entry held in the lane window
             int32_t win = 0;
+            prefetch_q<HD>(a, s, h0, lane);
             for (int64_t x = chunk_lo; x < chunk_hi; ++x) {
-                while (x >= ce) {
-                    ++s;
-                    cs = ce;
-                    ce = cs + seq_chunks(a, s, L);
+                if (x >= ce) {
+                    while (x >= ce) {
+                        ++s;
+                        cs = ce;
+                        ce = cs + seq_chunks(a, s, L);
+                    }
                     wbase = -1 << 30;
+                    prefetch_q<HD>(a, s, h0, lane);
                 }
                 const int j = static_cast<int>(x - cs);
                 const int tok0 = j * kChunkTokens;
@@ -662,7 +648,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                         }
                         meta[stage] = ChunkMeta{s, tok0, nvalid, flags};
                         const uint32_t full = bars + 8 * stage;
-                        if (nvalid > 0) {
+                        if (kWithholdFirstChunk && issued == 0) {
+                            // test build: neither a copy nor an arrival for this stage
+                        } else if (nvalid > 0) {
                             const uint32_t rows_bytes = static_cast<uint32_t>(a.box_rows * (RK + RV));
                             mbar_arrive_tx(full, nloads * rows_bytes);
                             const uint32_t kst = base + static_cast<uint32_t>(stage) * stage_bytes;
@@ -1208,24 +1196,14 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     k.k_bf16 = KT16 ? 1 : 0;
     k.v_bf16 = VT16 ? 1 : 0;
 
-    // Batches a CTA can plan from registers are planned inside the decode grid (no plan
-    // launch); larger ones get the one-CTA plan kernel first.
-    const bool plan_inside = d.num_seqs <= threads * kPlanPerThread &&
-                             env_int("KVFP8_DECODE_PLAN_KERNEL", 0) == 0;
-    if (plan_inside) {
-        k.cta_plan = nullptr;
-    } else {
-        plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs,
-                                            k.max_len, num_ctas,
-                                            reinterpret_cast<int32_t *>(w + ws.cstart_off),
-                                            reinterpret_cast<CtaPlan *>(w + ws.cta_off), k.out,
-                                            d.n_q * HD, d.status);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    }
+    plan_kernel<<<1, 1024, 0, stream>>>(d.seq_lens, d.qsl, d.qmax, d.qrows, d.num_seqs, k.max_len,
+                                        num_ctas, reinterpret_cast<int32_t *>(w + ws.cstart_off),
+                                        reinterpret_cast<CtaPlan *>(w + ws.cta_off), k.out,
+                                        d.n_q * HD, d.status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
-    // Programmatic dependent launch: the decode grid starts its prologue while the previous
-    // grid in the stream (the plan kernel, or the caller's last kernel) finishes, and waits
-    // (griddepcontrol.wait) before it reads or writes any memory.
+    // Programmatic dependent launch: the decode grid starts its prologue while the plan
+    // grid runs and waits (griddepcontrol.wait) before touching any data.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_ctas, groups);
     cfg.blockDim = dim3(threads);
@@ -1241,9 +1219,19 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     constexpr int kHeadsPerCta = 256 / (HD / 4);
     cudaLaunchConfig_t ccfg = cfg;
     ccfg.gridDim = dim3(d.num_seqs, (k.rows_per_seq + kHeadsPerCta - 1) / kHeadsPerCta);
-    ccfg.blockDim = dim3(256);
     ccfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&ccfg, combine_kernel<HD>, k);
+    // parts per sequence on average: every CTA's sequences plus one per sequence
+    const int64_t parts = (static_cast<int64_t>(num_ctas) + d.num_seqs) / std::max(1, d.num_seqs);
+    if (parts >= 32) {
+        ccfg.blockDim = dim3(256 * 4);
+        return cudaLaunchKernelEx(&ccfg, combine_kernel<HD, 4>, k);
+    }
+    if (parts >= 16) {
+        ccfg.blockDim = dim3(256 * 2);
+        return cudaLaunchKernelEx(&ccfg, combine_kernel<HD, 2>, k);
+    }
+    ccfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&ccfg, combine_kernel<HD, 1>, k);
 }
 
 }  // namespace

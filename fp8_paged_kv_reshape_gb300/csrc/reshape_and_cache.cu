@@ -23,6 +23,10 @@
 //    element, an infinite element, or a quotient so large that the steps overflow) get
 //    their bytes re-derived from the operands.
 //  * Rows of more than 2048 elements take a plain per-row loop.
+//  * Wide rows.  Rows of 512-2048 elements with 32-byte aligned sources are read 16
+//    elements per lane (one 32-byte load for bf16) and stored as one 16-byte code store.
+//  * L2 placement.  Source loads skip L1; cache stores carry an evict-first L2 policy so
+//    that the written lines reach HBM while this kernel runs rather than after it.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -141,15 +145,40 @@ __device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const F
     return make_uint2(w0, w1);
 }
 
+// Cache placement of the streams.  Source rows are read once: loads skip L1 and keep the
+// normal L2 priority.  Cache rows are written once: stores carry an L2 evict-first policy, so
+// the written lines are the first the L2 writes back, while this kernel runs, instead of
+// staying dirty in L2 after it ends (where the next kernel would pay for their write-back).
+__device__ __forceinline__ uint4 ld_na_v4(const uint8_t *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint64_t evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_ef(uint8_t *p, uint2 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ void st_ef(uint8_t *p, uint4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+
 template <bool kF32>
 struct Group;  // one 8-element group of a source row
 
 template <>
 struct Group<false> {  // bf16: 16 bytes
     uint4 v;
-    __device__ __forceinline__ void load(const uint8_t *p) {
-        v = __ldcs(reinterpret_cast<const uint4 *>(p));
-    }
+    __device__ __forceinline__ void load(const uint8_t *p) { v = ld_na_v4(p); }
     __device__ __forceinline__ void unpack(float (&x)[8]) const {
         x[0] = bf16lo(v.x); x[1] = bf16hi(v.x); x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
         x[4] = bf16lo(v.z); x[5] = bf16hi(v.z); x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
@@ -175,8 +204,11 @@ template <>
 struct Group<true> {  // fp32: 32 bytes
     float4 a, b;
     __device__ __forceinline__ void load(const uint8_t *p) {
-        a = __ldcs(reinterpret_cast<const float4 *>(p));
-        b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+        const uint4 x = ld_na_v4(p), y = ld_na_v4(p + 16);
+        a = make_float4(__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                        __uint_as_float(x.w));
+        b = make_float4(__uint_as_float(y.x), __uint_as_float(y.y), __uint_as_float(y.z),
+                        __uint_as_float(y.w));
     }
     __device__ __forceinline__ void unpack(float (&x)[8]) const {
         x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
@@ -199,9 +231,9 @@ struct Group<true> {  // fp32: 32 bytes
     static constexpr int kBytes = 32;
 };
 
-// 32-byte streaming load (sm_100+): eight words in one instruction; p 32-byte aligned.
-__device__ __forceinline__ void ld_cs_v8(const uint8_t *p, uint32_t *w) {
-    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+// 32-byte load (sm_100+): eight words in one instruction; p 32-byte aligned.
+__device__ __forceinline__ void ld_na_v8(const uint8_t *p, uint32_t *w) {
+    asm volatile("ld.global.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
                    "=r"(w[6]), "=r"(w[7])
                  : "l"(p));
@@ -216,7 +248,7 @@ struct Wide;
 template <>
 struct Wide<false> {  // bf16: 32 bytes
     uint32_t w[8];
-    __device__ __forceinline__ void load(const uint8_t *p) { ld_cs_v8(p, w); }
+    __device__ __forceinline__ void load(const uint8_t *p) { ld_na_v8(p, w); }
     __device__ __forceinline__ void unpack(float (&x)[16]) const {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -236,8 +268,8 @@ template <>
 struct Wide<true> {  // fp32: 64 bytes
     uint32_t w[16];
     __device__ __forceinline__ void load(const uint8_t *p) {
-        ld_cs_v8(p, w);
-        ld_cs_v8(p + 32, w + 8);
+        ld_na_v8(p, w);
+        ld_na_v8(p + 32, w + 8);
     }
     __device__ __forceinline__ void unpack(float (&x)[16]) const {
 #pragma unroll
@@ -257,6 +289,7 @@ struct RowCtx {
     uint8_t *cache;
     int64_t stride_bytes;
     float s;
+    uint64_t pol;  // L2 policy of the cache stores
 };
 
 __device__ __forceinline__ int64_t slot_of(const ReshapeArgs &a, int64_t row, int64_t rows) {
@@ -297,7 +330,8 @@ __device__ __forceinline__ void store_row_bf16(const G (&buf)[U], const RowCtx &
             uint4 *q = reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * G::kElems * 2);
 #pragma unroll
             for (int i = 0; i < G::kElems / 8; ++i)
-                q[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                st_ef(reinterpret_cast<uint8_t *>(q + i),
+                      make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]), c.pol);
         }
     }
 }
@@ -314,14 +348,12 @@ __device__ __forceinline__ void store_row(const G (&buf)[U], const RowCtx &c, co
             float x[G::kElems];
             buf[u].unpack(x);
             if constexpr (G::kElems == 8) {
-                *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
-                    quantize8<kFast>(x, c.s, fd);
+                st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd), c.pol);
             } else {
                 const uint2 lo = quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x), c.s, fd);
                 const uint2 hi =
                     quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x + 8), c.s, fd);
-                *reinterpret_cast<uint4 *>(dst + static_cast<int64_t>(g) * 16) =
-                    make_uint4(lo.x, lo.y, hi.x, hi.y);
+                st_ef(dst + static_cast<int64_t>(g) * 16, make_uint4(lo.x, lo.y, hi.x, hi.y), c.pol);
             }
         }
     }
@@ -388,6 +420,7 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_pipelined_kernel(const Re
     c.cache = is_v ? a.value_cache : a.key_cache;
     c.stride_bytes = (is_v ? a.value_stride : a.key_stride) * (kF32 ? 4 : 2);
     c.s = is_v ? sv : sk;
+    c.pol = evict_first_policy();
     if (is_v ? a.v_bf16 : a.k_bf16)  // uniform per warp
         pipelined_rows<G, U, 2>(a, c, r, stride, rows, lane);
     else if (fast_range(c.s))
@@ -483,9 +516,7 @@ __device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], cons
                 unpack2(add2(mul2(p, sn), mul2(q, c)), x[2 * j + 1], x[2 * j + 3]);
             }
         }
-        if (g < groups)
-            *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
-                quantize8<kFast>(x, c.s, fd);
+        if (g < groups) st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd), c.pol);
     }
 }
 
@@ -551,10 +582,12 @@ __global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const Reshape
     ck.cache = a.key_cache;
     ck.stride_bytes = a.key_stride * (kF32 ? 4 : 2);
     ck.s = sk;
+    ck.pol = evict_first_policy();
     cv.src = static_cast<const uint8_t *>(a.value);
     cv.cache = a.value_cache;
     cv.stride_bytes = a.value_stride * (kF32 ? 4 : 2);
     cv.s = sv;
+    cv.pol = ck.pol;
     if (fast_range(sk) && fast_range(sv))
         rope_token_rows<kF32, U, true>(a, ck, cv, t, W, lane);
     else
@@ -572,6 +605,7 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
     }
     const int lane = threadIdx.x & 31;
     const int64_t rows = 2 * a.num_tokens;
+    const uint64_t pol = evict_first_policy();
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); r < rows;
          r += static_cast<int64_t>(gridDim.x) * kWarps) {
         const int64_t slot = __ldg(a.slot_mapping + (r >> 1));
@@ -596,8 +630,8 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
                 if (g < groups) {
                     float x[8];
                     in[u].unpack(x);
-                    *reinterpret_cast<uint2 *>(dst + static_cast<int64_t>(g) * 8) =
-                        fast ? quantize8<true>(x, s, fd) : quantize8<false>(x, s, fd);
+                    st_ef(dst + static_cast<int64_t>(g) * 8,
+                          fast ? quantize8<true>(x, s, fd) : quantize8<false>(x, s, fd), pol);
                 }
             }
         }

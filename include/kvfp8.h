@@ -317,12 +317,39 @@ KVFP8_API kvfp8_status kvfp8_reshape_and_cache_mixed(
  * A bf16 K enters the tensor cores against bf16 q (exact products); a bf16 V against the
  * probabilities split into two bf16 parts (16 significant bits).
  * This build: exactly one side bf16 (both E4M3 is kvfp8_paged_decode_attention; both
- * bf16 returns KVFP8_ERR_UNSUPPORTED), head_dim 64 or 128, n_q/n_kv <= 16.
+ * bf16 returns KVFP8_ERR_UNSUPPORTED); n_q/n_kv <= 16 at head_dim 64 and 128, <= 8 at 256
+ * (larger groups return KVFP8_ERR_UNSUPPORTED).
  * Workspace: kvfp8_paged_decode_workspace_size(num_seqs, n_q, head_dim).  Everything else
  * as kvfp8_paged_decode_attention.
  */
 KVFP8_API kvfp8_status kvfp8_paged_decode_attention_mixed(
     void *out, const void *query, const void *key_cache, kvfp8_cache_dtype k_cache_dtype,
+    const void *value_cache, kvfp8_cache_dtype v_cache_dtype, const int32_t *block_tables,
+    int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
+    int32_t n_kv, int32_t head_dim, int32_t block_size, int32_t num_blocks, float sm_scale,
+    const void *k_scale, const void *v_scale, kvfp8_dtype scale_dtype, void *workspace,
+    size_t workspace_bytes, uint32_t *status, kvfp8_stream_t stream);
+
+/*
+ * kvfp8_paged_attention_multi with a per-side cache dtype: causal multi-query attention
+ * (each new token attends to the cached tokens up to and including its own position) where
+ * an E4M3 side reads as scale * E4M3dec(byte) and a bf16 side as the stored bf16, unscaled.
+ *
+ * Defined by: [P1] tests/test-fp8.cpp check_fp8_attention, whose batch of new tokens runs
+ * over a cache with K only, V only or both in FP8 (the other side at 16 bits, unscaled),
+ * and tests/test-backend-ops.cpp (the F8/F16 cache mixes with several query rows).
+ *
+ * Both sides E4M3 is kvfp8_paged_attention_multi (and is passed to it).  With one bf16 side
+ * this build runs the split-KV kernel only: max_query_len * (n_q / n_kv) <= 16 score
+ * columns per kv head (<= 8 at head_dim 256); longer query chunks return
+ * KVFP8_ERR_UNSUPPORTED, as do both sides bf16.  Workspace:
+ * kvfp8_paged_attention_multi_workspace_size(num_seqs, n_q, n_kv, head_dim, max_query_len).
+ * Cache layouts as kvfp8_paged_decode_attention_mixed; everything else as
+ * kvfp8_paged_attention_multi.
+ */
+KVFP8_API kvfp8_status kvfp8_paged_attention_multi_mixed(
+    void *out, const void *query, const int32_t *query_start_loc, int32_t num_query_rows,
+    int32_t max_query_len, const void *key_cache, kvfp8_cache_dtype k_cache_dtype,
     const void *value_cache, kvfp8_cache_dtype v_cache_dtype, const int32_t *block_tables,
     int32_t max_blocks_per_seq, const int32_t *seq_lens, int32_t num_seqs, int32_t n_q,
     int32_t n_kv, int32_t head_dim, int32_t block_size, int32_t num_blocks, float sm_scale,

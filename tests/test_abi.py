@@ -163,7 +163,8 @@ def test_mixed_decode_host_validation():
         return kv.LIB.kvfp8_paged_decode_attention_mixed(*args.values())
     assert call(k_kind=5) == binding.ERR_DTYPE
     assert call(k_kind=binding.CACHE_BF16, v_kind=binding.CACHE_BF16) == binding.ERR_UNSUPPORTED
-    assert call(head_dim=256) == binding.ERR_UNSUPPORTED
+    assert call(head_dim=256, n_q=80) == binding.ERR_UNSUPPORTED    # group of 10 at head_dim 256
+    assert call(n_q=17 * 8) == binding.ERR_UNSUPPORTED               # group of 17
     assert call(head_dim=96) == binding.ERR_SHAPE
     assert call(n_q=30) == binding.ERR_SHAPE
     assert call(query=None) == binding.ERR_NULL
@@ -248,3 +249,30 @@ def test_noalloc_binding_checks_tables_like_the_workspace_binding():
                 fn(q, kc, kc, b, s)
         with pytest.raises(ValueError):  # out shaped unlike query
             fn(q, kc, kc, bt, sl, out=torch.zeros(4, 32, 64, dtype=torch.bfloat16))
+
+
+def test_multi_mixed_host_validation():
+    def call(**over):
+        args = dict(out=ctypes.c_void_p(16), query=ctypes.c_void_p(16), qsl=ctypes.c_void_p(16),
+                    rows=16, qmax=4, key_cache=ctypes.c_void_p(16), k_kind=binding.CACHE_BF16,
+                    value_cache=ctypes.c_void_p(16), v_kind=binding.CACHE_E4M3,
+                    block_tables=ctypes.c_void_p(16), max_blocks_per_seq=256,
+                    seq_lens=ctypes.c_void_p(16), num_seqs=4, n_q=32, n_kv=8, head_dim=128,
+                    block_size=16, num_blocks=1024, sm_scale=0.0, k_scale=None, v_scale=None,
+                    scale_dtype=binding.F32, workspace=ctypes.c_void_p(16),
+                    workspace_bytes=1 << 30, status=None, stream=None)
+        args.update(over)
+        return kv.LIB.kvfp8_paged_attention_multi_mixed(*args.values())
+    assert call(k_kind=3) == binding.ERR_DTYPE
+    assert call(k_kind=binding.CACHE_BF16, v_kind=binding.CACHE_BF16) == binding.ERR_UNSUPPORTED
+    assert call(qmax=5) == binding.ERR_UNSUPPORTED                 # 20 score columns
+    assert call(head_dim=256, qmax=3) == binding.ERR_UNSUPPORTED   # 12 columns at head_dim 256
+    assert call(head_dim=96) == binding.ERR_SHAPE
+    assert call(qsl=None) == binding.ERR_NULL
+    assert call(workspace=None) == binding.ERR_NULL
+    assert call(qsl=ctypes.c_void_p(18)) == binding.ERR_ALIGN
+    assert call(workspace_bytes=100) == binding.ERR_WORKSPACE
+    assert call(num_seqs=0, query=None) == binding.OK
+    # both sides E4M3 is the all-FP8 call, with its own validation
+    assert call(k_kind=binding.CACHE_E4M3, head_dim=96) == binding.ERR_SHAPE
+    assert call(k_kind=binding.CACHE_E4M3, query=None) == binding.ERR_NULL

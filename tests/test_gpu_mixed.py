@@ -173,6 +173,9 @@ DECODE_CASES = [
     ("g12_hd64_nt2", 24, 2, 64, 16, [77, 1234]),
     ("bs256_g6", 24, 4, 128, 256, [700, 5]),
     ("mha16_head_groups", 16, 16, 128, 16, [400, 17]),
+    # head_dim 256: groups of up to 8 on the split-KV kernel
+    ("g8_hd256_bs64", 64, 8, 256, 64, [65, 300, 1, 2000]),
+    ("g2_hd256", 4, 2, 256, 16, [17, 129]),
 ]
 
 
@@ -205,3 +208,72 @@ def test_scaling_the_bf16_side_would_be_caught():
     gpu_util.assert_attention_close(out, ref)
     g = out.float().cpu().numpy() * 0.04
     assert np.count_nonzero(np.abs(g - ref) > 2e-3 + 1e-2 * np.abs(ref)) > 0
+
+
+def _multi_case(kinds, n_q, n_kv, hd, bs, lengths, nbs, seed, ks=0.05, vs=0.04):
+    """Causal multi-query attention with one bf16 side: sequence b's last nbs[b] cached tokens
+    are its query tokens.  The cache is written by the GPU; the oracle writes its own."""
+    kk, vk = kinds
+    g = torch.Generator().manual_seed(seed)
+    need = [math.ceil(L / bs) for L in lengths]
+    nb = sum(need) + 2
+    perm = torch.randperm(nb, generator=g).numpy().astype(np.int32)
+    bt = np.full((len(lengths), max(1, max(need))), -1, np.int32)
+    at = 0
+    for i, n in enumerate(need):
+        bt[i, :n] = perm[at:at + n]
+        at += n
+    total = sum(lengths)
+    k = torch.randn(total, n_kv, hd, generator=g).to(torch.bfloat16)
+    v = torch.randn(total, n_kv, hd, generator=g).to(torch.bfloat16)
+    qsl = np.concatenate([[0], np.cumsum(nbs)]).astype(np.int32)
+    q = torch.randn(int(qsl[-1]), n_q, hd, generator=g).to(torch.bfloat16)
+    slots = np.concatenate([bt[i, np.arange(L) // bs].astype(np.int64) * bs + np.arange(L) % bs
+                            for i, L in enumerate(lengths)])
+    kc, vc = _np_cache(kk, (nb, bs, n_kv, hd)), _np_cache(vk, (nb, bs, n_kv, hd))
+    assert oracle.reshape_and_cache_mixed(k, v, kc, kk, vc, vk, slots, bs, ks, vs) == 0
+    ref, st = oracle.paged_attention_multi_mixed(q, qsl, kc, kk, vc, vk, bt,
+                                                 np.array(lengths, np.int32), ks, vs)
+    assert st == 0
+    ksc = torch.tensor([ks], device="cuda")
+    vsc = torch.tensor([vs], device="cuda")
+    gk, gv = _to_gpu(_np_cache(kk, kc.shape)), _to_gpu(_np_cache(vk, vc.shape))
+    kv.reshape_and_cache_mixed(k.cuda(), v.cuda(), gk, gv, torch.from_numpy(slots).cuda(), ksc, vsc)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = kv.paged_attention_multi_mixed(q.cuda(), torch.from_numpy(qsl).cuda(), max(nbs), gk, gv,
+                                         torch.from_numpy(bt).cuda(),
+                                         torch.tensor(lengths, dtype=torch.int32, device="cuda"),
+                                         ksc, vsc, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out, ref
+
+
+MULTI_CASES = [
+    # name, n_q, n_kv, head_dim, block_size, lengths, query tokens per sequence
+    ("g4_q4", 32, 8, 128, 16, [700, 33, 4, 2000], [4, 3, 4, 1]),
+    ("g5_q3_bs32", 40, 8, 128, 32, [100, 1000, 3], [3, 2, 3]),
+    ("g2_q8_hd64", 8, 4, 64, 16, [50, 17, 300], [8, 5, 1]),
+    ("g1_q16", 8, 8, 128, 16, [64, 130], [16, 9]),
+    ("g2_q4_hd256", 8, 4, 256, 64, [90, 500], [4, 2]),
+]
+
+
+@pytest.mark.parametrize("kinds", [K_BF16, V_BF16], ids=["k_bf16", "v_bf16"])
+@pytest.mark.parametrize("case", MULTI_CASES, ids=[c[0] for c in MULTI_CASES])
+def test_mixed_multi_query_against_oracle(case, kinds):
+    name, n_q, n_kv, hd, bs, lengths, nbs = case
+    out, ref = _multi_case(kinds, n_q, n_kv, hd, bs, lengths, nbs, seed=len(name) * 5 + kinds[1])
+    gpu_util.assert_attention_close(out, ref, name)
+
+
+def test_mixed_multi_query_past_the_split_kv_kernel_is_refused():
+    q = torch.zeros(5, 32, 128, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 16, 8, 128, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros(4, 16, 8, 128, dtype=torch.uint8, device="cuda")
+    bt = torch.zeros(1, 4, dtype=torch.int32, device="cuda")
+    sl = torch.tensor([40], dtype=torch.int32, device="cuda")
+    qsl = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    with pytest.raises(kv.KvFp8Error) as e:  # 5 tokens x 4 heads = 20 score columns
+        kv.paged_attention_multi_mixed(q, qsl, 5, kc, vc, bt, sl)
+    assert e.value.status == kv.ERR_UNSUPPORTED
