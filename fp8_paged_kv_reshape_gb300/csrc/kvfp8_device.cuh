@@ -18,6 +18,11 @@
 
 namespace kvfp8 {
 
+// Shared-memory address of a generic pointer into this CTA's shared memory.
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 // ---------------------------------------------------------------- status word
 
 __device__ __forceinline__ void flag(uint32_t *status, uint32_t bit) {

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <cuda_runtime.h>
 
 #include <map>
@@ -13,6 +14,12 @@
 #include "../../include/kvfp8.h"
 
 namespace kvfp8 {
+
+// A tuning knob read from the environment (launch shapes and kernel choices only).
+inline int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    return v ? std::atoi(v) : dflt;
+}
 
 // ---------------------------------------------------------------- launch facts
 // Device attributes and per-kernel occupancy do not change during a process, but querying

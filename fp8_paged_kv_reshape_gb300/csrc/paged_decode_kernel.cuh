@@ -135,9 +135,6 @@ __device__ __forceinline__ QueryRange query_range(const int32_t *qsl, int b, int
 
 // ---------------------------------------------------------------- PTX wrappers
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -1103,10 +1100,6 @@ cudaError_t encode_cache_map_whole(CUtensorMap *map, const uint8_t *cache, int64
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int env_int(const char *name, int dflt) {
-    const char *v = std::getenv(name);
-    return v ? std::atoi(v) : dflt;
-}
 
 template <int HD, int NT, bool kMulti, bool KT16, bool VT16>
 cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t stream) {

@@ -123,6 +123,11 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
            | (1ull << 46)                                 // descriptor version
            | (2ull << 61);                                // 128-byte swizzle
 }
+// The descriptor of an address off bytes (a multiple of 16) past one whose descriptor is d:
+// the start-address field is (address >> 4) in 14 bits, and every shared-memory address of
+// a CTA is below 2^18, so the field never carries into the next one.
+__device__ __forceinline__ uint64_t desc_at(uint64_t d, uint32_t off) { return d + (off >> 4); }
+
 // Instruction descriptor, kind::f16: f16 A and B, fp32 D, both K-major, M x N.
 __host__ __device__ constexpr uint32_t f16_idesc(int m, int n) {
     return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
@@ -439,16 +444,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
         // softmax warps work on the current ones.
         if (lane == 0) {
             const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, L::kVRows);
+            // operand descriptors computed once; each product adds its constant offset
+            const uint64_t qdesc = sw128_desc(base + L::kQ), kdesc = sw128_desc(base + L::kK),
+                           vdesc = sw128_desc(base + L::kV);
             int o_issued = 0;  // O products issued so far
             bool ok = true;
             auto issue_o = [&](int t) {  // O += P(t) . V(t), then release tile t's buffers
                 const int b = t % L::kNB;
                 if (!mbar_wait(bar(L::kPReady, b), (t / L::kNB) & 1, abort_flag)) return false;
                 tc_fence_after();
+                const uint64_t vb = desc_at(vdesc, b * L::kVBuf);
 #pragma unroll
                 for (int k = 0; k < kPfKeys / 16; ++k)
-                    umma_ts(tmem + L::kColO, tmem + 64 * b + 8 * k,
-                            sw128_desc(base + L::kV + b * L::kVBuf + k * 32), idesc_o,
+                    umma_ts(tmem + L::kColO, tmem + 64 * b + 8 * k, desc_at(vb, k * 32), idesc_o,
                             (t > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(L::kKvFree, b));
                 ++o_issued;
@@ -462,11 +470,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     ok = mbar_wait(bar(L::kKvFree, b), ((i / L::kNB) & 1) ^ 1u, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
+                const uint64_t kb = desc_at(kdesc, b * L::kKBuf);
 #pragma unroll
                 for (int k = 0; k < HD / 16; ++k) {
-                    const uint64_t ad = sw128_desc(base + L::kQ + (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
-                    const uint64_t bd = sw128_desc(base + L::kK + b * L::kKBuf + (k >> 2) * (kPfKeys * 128) +
-                                                   (k & 3) * 32);
+                    const uint64_t ad = desc_at(qdesc, (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
+                    const uint64_t bd = desc_at(kb, (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
                     umma_ss(tmem + 64 * b, ad, bd, idesc_s, k > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(L::kSReady, b));
@@ -966,10 +974,14 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         // has completed: o_done[r][j].
         if (lane == 0) {
             const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, HD);
+            // operand descriptors computed once; each product adds its constant offset
+            const uint64_t qdesc = sw128_desc(base + L::kQ), kdesc = sw128_desc(base + L::kK),
+                           vdesc = sw128_desc(base + L::kV);
             int o_issued = 0;
             bool ok = true;
             auto issue_o = [&](int t) {
                 const int b = t % L::kNB, j = t & 1;
+                const uint64_t vb = desc_at(vdesc, b * L::kVBuf);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     if (!mbar_wait(bar(L::kPReady, 2 * r + j), (t >> 1) & 1, abort_flag)) return false;
@@ -977,8 +989,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 #pragma unroll
                     for (int k = 0; k < kPfKeys / 16; ++k)
                         umma_ts(tmem + L::col_o(r), tmem + L::col_s(r, j) + 8 * k,
-                                sw128_desc(base + L::kV + b * L::kVBuf + k * 32), idesc_o,
-                                (t > 0 || k > 0) ? 1u : 0u);
+                                desc_at(vb, k * 32), idesc_o, (t > 0 || k > 0) ? 1u : 0u);
                     umma_commit(bar(L::kODone, 2 * r + j));
                 }
                 umma_commit(bar(L::kKvFree, b));
@@ -994,12 +1005,12 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                         ok = mbar_wait(bar(L::kODone, 2 * r + j), ((i >> 1) & 1) ^ 1u, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
+                    const uint64_t qr_d = desc_at(qdesc, r * L::kQTile);
+                    const uint64_t kb = desc_at(kdesc, b * L::kKBuf);
 #pragma unroll
                     for (int k = 0; k < HD / 16; ++k) {
-                        const uint64_t ad = sw128_desc(base + L::kQ + r * L::kQTile +
-                                                       (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
-                        const uint64_t bd = sw128_desc(base + L::kK + b * L::kKBuf +
-                                                       (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
+                        const uint64_t ad = desc_at(qr_d, (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
+                        const uint64_t bd = desc_at(kb, (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
                         umma_ss(tmem + L::col_s(r, j), ad, bd, idesc_s, k > 0 ? 1u : 0u);
                     }
                     umma_commit(bar(L::kSReady, 2 * r + j));

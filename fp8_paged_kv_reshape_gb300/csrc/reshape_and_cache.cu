@@ -642,16 +642,17 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
 // for the rope kernel).
 template <typename K>
 cudaError_t launch_persistent(K kernel, const ReshapeArgs &a, cudaStream_t stream,
-                              int64_t units) {
+                              int64_t units, size_t smem = 0) {
     DeviceFacts f;
     int occ = 0;
     cudaError_t err = device_facts(&f);
     if (err != cudaSuccess) return err;
-    if ((err = kernel_occupancy(kernel, kWarps * 32, 0, &occ)) != cudaSuccess) return err;
+    if (smem > static_cast<size_t>(f.smem_optin)) return cudaErrorNotSupported;
+    if ((err = kernel_occupancy(kernel, kWarps * 32, smem, &occ)) != cudaSuccess) return err;
     const int64_t want = (units + kWarps - 1) / kWarps;
     const int64_t full = static_cast<int64_t>(f.sms) * std::max(occ, 1);
     const unsigned blocks = static_cast<unsigned>(std::min(want, full));
-    kernel<<<blocks, kWarps * 32, 0, stream>>>(a);
+    kernel<<<blocks, kWarps * 32, smem, stream>>>(a);
     return cudaGetLastError();
 }
 

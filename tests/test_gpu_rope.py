@@ -87,3 +87,31 @@ def test_rope_changes_k_but_not_v_and_bad_positions_are_flagged():
     ok = [i for i in range(64) if i not in (5, 9)]
     assert torch.equal(flat_v[ok], vp.view(64, -1)[ok])                      # V untouched by rope
     assert not torch.equal(flat_k[ok], kp.view(64, -1)[ok])                  # K rotated
+
+
+@pytest.mark.parametrize("scales", [(0.05, 0.04), (1e-25, 3.7e22)], ids=["fast_divide", "slow_divide"])
+def test_rope_divide_paths(scales):
+    # scales inside the reciprocal-and-corrections range and outside it (IEEE divide)
+    n_kv, hd, rot, n = 8, 128, 128, 2000
+    g = torch.Generator().manual_seed(99)
+    k = (torch.randn(n, n_kv, hd, generator=g) * 3).to(torch.bfloat16)
+    v = (torch.randn(n, n_kv, hd, generator=g) * 3).to(torch.bfloat16)
+    pos = torch.randint(0, 4096, (n,), generator=g, dtype=torch.int64)
+    nb, bs = (n + 15) // 16 + 3, 16
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(torch.int64)
+    slots[::13] = -1
+    table = _table(4096, rot)
+    ks = np.float32(scales[0]).item()
+    vs = np.float32(scales[1]).item()
+    kc = torch.full((nb, bs, n_kv, hd), 0x5A, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    kv.rope_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, slots.cuda(), pos.cuda(),
+                              torch.from_numpy(table).cuda(), True,
+                              torch.tensor([ks], device="cuda"), torch.tensor([vs], device="cuda"))
+    torch.cuda.synchronize()
+    ko = np.full((nb, bs, n_kv, hd), 0x5A, np.uint8)
+    vo = ko.copy()
+    assert oracle.rope_reshape_and_cache(k, v, ko, vo, slots.numpy(), pos.numpy(), table, rot,
+                                         True, bs, ks, vs) == 0
+    np.testing.assert_array_equal(kc.cpu().numpy(), ko)
+    np.testing.assert_array_equal(vc.cpu().numpy(), vo)
