@@ -767,15 +767,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 //
 // For head_dim 64 and 128 when a (sequence, kv head) has more than 128 score rows: one CTA
 // takes 256 rows as two row tiles that share every converted K/V tile, so the copies and
-// the conversion are paid once per two tiles of tensor work.  Each row tile has its own
-// softmax warpgroup and two score buffers in tensor memory, so S(i+1) of a row tile is
-// computed while its softmax works on S(i), and the two row tiles' products interleave on
-// the tensor core.  Tensor memory (512 columns at head_dim 128): S[r][j] at 64*(2r+j),
-// O[r] at 256 + head_dim*r.  The rows sum P themselves (fp32, in pairs).
+// the conversion are paid once per two tiles of tensor work.  Keys go in tiles of 128: the
+// score product S = Q.K^T then has N = 128, where a kind::f16 product runs at the tensor
+// core's full rate (at N = 64 the shared-memory reads of its two operands bound it to about
+// two thirds of that), and each tile costs half as many products, commits and waits.
+//
+// Tensor memory (512 columns at head_dim 128): S[r] at 128*r (P written over its first 64
+// columns as f16), O[r] at 256 + head_dim*r.  Each row tile has one score buffer: the tensor
+// core runs the products one thread issues in order, and S(r, i+1) is issued after O(r, i),
+// so the next scores land only after the product that reads P.  The two row tiles take
+// turns: while one row tile's softmax works, the tensor core runs the other's O and next S.
+// The commit that signals S(r, i) also covers O(r, i-1), so the softmax may rescale O as
+// soon as its scores are ready.  The rows sum P themselves (fp32, in pairs).
+//
+// FP8 K/V arrive by TMA in halves of 64 keys (a staging ring of NS halves) and are converted
+// into two f16 K buffers and two V^T buffers of 128 keys.  A K buffer is free once both row
+// tiles' S products are done with it; a V^T buffer (and the valid-key masks stored with it)
+// once both O products are.
 //
 // Warps (14): 0-3 softmax of row tile 0, 4-7 softmax of row tile 1 (warp w reads TMEM
 // lanes 32*(w%4)..+31), 8-11 conversion, 12 tensor-core issue (and TMEM allocation), 13 TMA.
 constexpr int kP2Rows = 2 * kPfRows;
+constexpr int kP2Keys = 2 * kPfKeys;   // keys per tile; FP8 staging and conversion go by halves
 constexpr int kP2ConvWarps = 4;
 constexpr int kP2MmaWarp = 8 + kP2ConvWarps, kP2TmaWarp = kP2MmaWarp + 1;
 constexpr int kP2Warps = kP2TmaWarp + 1;
@@ -784,29 +797,54 @@ template <int HD>
 struct Pf2Smem {
     static constexpr int kSeg = HD >= 128 ? 128 : 64;
     static constexpr int kSegs = HD / kSeg;
-    static constexpr int kNB = 3;                                  // f16 K / V^T buffers
-    static constexpr int kNS = HD >= 128 ? 3 : 4;                  // FP8 staging stages
+    static constexpr int kNS = HD >= 128 ? 2 : 4;                  // FP8 staging halves
     static constexpr int kQTile = HD * 256;                        // one row tile of Q (f16)
     static constexpr int kQ = 0;
-    static constexpr int kKBuf = HD * 128, kVBuf = HD * 128;
+    // K f16: HD/64 blocks x 128 keys x 128 B; V^T f16: 2 key blocks x HD rows x 128 B
+    static constexpr int kKBuf = HD * 256, kVBuf = HD * 256;
     static constexpr int kK = kQ + 2 * kQTile;
-    static constexpr int kV = kK + kNB * kKBuf;
-    static constexpr int kStage = kV + kNB * kVBuf;
-    static constexpr int kStageBytes = 2 * kPfKeys * HD;
+    static constexpr int kV = kK + 2 * kKBuf;
+    static constexpr int kStage = kV + 2 * kVBuf;
+    static constexpr int kStageBytes = 2 * kPfKeys * HD;           // FP8 K then V of 64 keys
     static constexpr int kBars = kStage + kNS * kStageBytes;
-    // mbarriers: full[NS], empty[NS], kv_ready[NB], kv_free[NB], then per (row tile r,
-    // score buffer j) at index 2r+j: s_ready, p_ready, o_done
-    static constexpr int kFull = kBars, kEmpty = kFull + 8 * kNS, kKvReady = kEmpty + 8 * kNS;
-    static constexpr int kKvFree = kKvReady + 8 * kNB, kSReady = kKvFree + 8 * kNB;
-    static constexpr int kPReady = kSReady + 8 * 4, kODone = kPReady + 8 * 4;
-    static constexpr int kMeta = kODone + 8 * 4;
-    static constexpr int kBufMask = kMeta + 8 * kNS;
-    static constexpr int kMisc = kBufMask + 8 * kNB;
+    // mbarriers: full[NS], empty[NS], then per buffer k_ready, v_ready, k_free, v_free, then
+    // per row tile s_ready, p_ready, o_done, and one to drain the tensor core on a timeout
+    static constexpr int kFull = kBars, kEmpty = kFull + 8 * kNS, kKReady = kEmpty + 8 * kNS;
+    static constexpr int kVReady = kKReady + 16, kKFree = kVReady + 16, kVFree = kKFree + 16;
+    static constexpr int kSReady = kVFree + 16, kPReady = kSReady + 16, kODone = kPReady + 16;
+    static constexpr int kDrain = kODone + 16;
+    static constexpr int kMeta = kDrain + 8;                       // valid-key mask per stage
+    static constexpr int kBufMask = kMeta + 8 * kNS;               // per V^T buffer, two halves
+    static constexpr int kMisc = kBufMask + 32;                    // tmem base, abort flag
     static constexpr int kTotal = kMisc + 16;
     static constexpr uint32_t kTmemCols = 512;
-    __host__ __device__ static constexpr uint32_t col_s(int r, int j) { return static_cast<uint32_t>(64 * (2 * r + j)); }
+    __host__ __device__ static constexpr uint32_t col_s(int r) { return static_cast<uint32_t>(128 * r); }
     __host__ __device__ static constexpr uint32_t col_o(int r) { return static_cast<uint32_t>(256 + HD * r); }
 };
+
+// the largest (kMax) or smallest of 32 scores, four chains of 3-input ops
+template <bool kMax>
+__device__ __forceinline__ float extreme32(const uint32_t (&s)[32]) {
+    auto v = [&](int c) { return __uint_as_float(s[c]); };
+    auto op = [](float a, float b, float c) { return kMax ? max3f(a, b, c) : min3f(a, b, c); };
+    float a0 = v(0), a1 = v(1), a2 = v(2), a3 = v(3);
+#pragma unroll
+    for (int c = 4; c < 28; c += 8) {
+        a0 = op(a0, v(c), v(c + 1));
+        a1 = op(a1, v(c + 2), v(c + 3));
+        a2 = op(a2, v(c + 4), v(c + 5));
+        a3 = op(a3, v(c + 6), v(c + 7));
+    }
+    a0 = op(a0, v(28), v(29));
+    a1 = op(a1, v(30), v(31));
+    return op(a0, a1, kMax ? fmaxf(a2, a3) : fminf(a2, a3));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kP2Warps * 32, 1)
@@ -848,7 +886,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
     if (row0 >= nb * G) return;
     const int j_last = min(nb, (row0 + kP2Rows + G - 1) / G) - 1;
     const int kend = Ls - nb + j_last + 1;            // keys the CTA's last row may see
-    const int ntiles = kend > 0 ? (kend + kPfKeys - 1) / kPfKeys : 0;
+    const int ntiles = kend > 0 ? (kend + kP2Keys - 1) / kP2Keys : 0;
     const int rot = ntiles > 0 ? static_cast<int>((static_cast<int64_t>(ctile) * ntiles) / a.row_tiles) % ntiles : 0;
     auto key_tile = [&](int i) { const int k = i + rot; return k >= ntiles ? k - ntiles : k; };
 
@@ -870,15 +908,16 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             mbar_init(bar(L::kFull, s), 1);
             mbar_init(bar(L::kEmpty, s), kP2ConvWarps);
         }
-        for (int b = 0; b < L::kNB; ++b) {
-            mbar_init(bar(L::kKvReady, b), kP2ConvWarps);
-            mbar_init(bar(L::kKvFree, b), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::kKReady, b), kP2ConvWarps);
+            mbar_init(bar(L::kVReady, b), kP2ConvWarps);
+            mbar_init(bar(L::kKFree, b), 1);
+            mbar_init(bar(L::kVFree, b), 1);
+            mbar_init(bar(L::kSReady, b), 1);
+            mbar_init(bar(L::kPReady, b), 4);
+            mbar_init(bar(L::kODone, b), 1);
         }
-        for (int q = 0; q < 4; ++q) {
-            mbar_init(bar(L::kSReady, q), 1);
-            mbar_init(bar(L::kPReady, q), 4);
-            mbar_init(bar(L::kODone, q), 1);
-        }
+        mbar_init(bar(L::kDrain, 0), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -898,7 +937,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
 
     if (warp == kP2TmaWarp) {
         // ------------------------------------------------------------ TMA producer
-        // lane p < nbox: K box p of the tile; lane nbox + p: V box p (as in prefill_kernel)
+        // half h of the key pass (64 keys of tile h/2): lane p < nbox fetches K box p, lane
+        // nbox + p V box p
         const int32_t *bt = a.block_tables + static_cast<int64_t>(seq) * a.max_blocks_per_seq;
         const int bs = a.block_size, br = a.box_rows;
         const int lbs = __ffs(bs) - 1;
@@ -912,17 +952,20 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         int32_t win = -1;
         int issued = 0;
         bool aborted = false;
-        for (int i = 0; i < ntiles; ++i) {
-            const int st = i % L::kNS;
-            const int t0 = key_tile(i) * kPfKeys;
-            const int e0 = t0 >> lbs, e1 = (min(kend, t0 + kPfKeys) - 1) >> lbs;
-            if (e0 < wbase || e1 >= wbase + 32) {
-                wbase = e0;
-                win = wbase + lane < a.max_blocks_per_seq ? bt[wbase + lane] : -1;
-            }
+        for (int h = 0; h < 2 * ntiles; ++h) {
+            const int st = h % L::kNS;
+            const int t0 = key_tile(h >> 1) * kP2Keys + (h & 1) * kPfKeys;
             const int t = t0 + p * br;
+            const bool any = t0 < kend;
+            if (any) {
+                const int e0 = t0 >> lbs, e1 = (min(kend, t0 + kPfKeys) - 1) >> lbs;
+                if (e0 < wbase || e1 >= wbase + 32) {
+                    wbase = e0;
+                    win = wbase + lane < a.max_blocks_per_seq ? bt[wbase + lane] : -1;
+                }
+            }
             const int blk = __shfl_sync(0xFFFFFFFFu, win, ((t >> lbs) - wbase) & 31);
-            const bool live = box_lane && t < kend;
+            const bool live = any && box_lane && t < kend;
             const bool good = live && blk >= 0 && blk < a.num_blocks;
             if (live && !good && k_lane) flag(a.status, KVFP8_DEV_BAD_BLOCK);
             const int row = blk * bs + (t & (bs - 1));
@@ -936,7 +979,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 static_cast<uint64_t>(__reduce_or_sync(0xFFFFFFFFu, static_cast<uint32_t>(part >> 32))) << 32;
             const int boxes = __popc(__ballot_sync(0xFFFFFFFFu, good && k_lane));
             if (lane == 0) {
-                if (!mbar_wait(bar(L::kEmpty, st), ((i / L::kNS) & 1) ^ 1u, abort_flag)) {
+                if (!mbar_wait(bar(L::kEmpty, st), ((h / L::kNS) & 1) ^ 1u, abort_flag)) {
                     aborted = true;
                 } else {
                     meta[st] = mask;
@@ -969,63 +1012,63 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
     }
     else if (warp == kP2MmaWarp) {
         // ------------------------------------------------------------ tensor-core issue
-        // Tile i: S[r][i%2] = Q[r].K(i)^T for both row tiles, then O[r] += P[r](i-1).V(i-1).
-        // S[r][j] may be overwritten once O[r] of the tile two back (which read P from it)
-        // has completed: o_done[r][j].
+        // S(r, 0) for both row tiles, then per tile i and row tile r: O(r, i) once P(r, i) is
+        // ready, then S(r, i+1) into the same columns.
         if (lane == 0) {
-            const uint32_t idesc_s = f16_idesc(kPfRows, kPfKeys), idesc_o = f16_idesc(kPfRows, HD);
+            const uint32_t idesc_s = f16_idesc(kPfRows, kP2Keys), idesc_o = f16_idesc(kPfRows, HD);
             // operand descriptors computed once; each product adds its constant offset
             const uint64_t qdesc = sw128_desc(base + L::kQ), kdesc = sw128_desc(base + L::kK),
                            vdesc = sw128_desc(base + L::kV);
-            int o_issued = 0;
-            bool ok = true;
-            auto issue_o = [&](int t) {
-                const int b = t % L::kNB, j = t & 1;
-                const uint64_t vb = desc_at(vdesc, b * L::kVBuf);
+            auto issue_s = [&](int i, int r) {
+                const uint64_t qd = desc_at(qdesc, r * L::kQTile);
+                const uint64_t kb = desc_at(kdesc, (i & 1) * L::kKBuf);
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (!mbar_wait(bar(L::kPReady, 2 * r + j), (t >> 1) & 1, abort_flag)) return false;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < kPfKeys / 16; ++k)
-                        umma_ts(tmem + L::col_o(r), tmem + L::col_s(r, j) + 8 * k,
-                                desc_at(vb, k * 32), idesc_o, (t > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(bar(L::kODone, 2 * r + j));
-                }
-                umma_commit(bar(L::kKvFree, b));
-                ++o_issued;
-                return true;
+                for (int k = 0; k < HD / 16; ++k)
+                    umma_ss(tmem + L::col_s(r), desc_at(qd, (k >> 2) * (kPfRows * 128) + (k & 3) * 32),
+                            desc_at(kb, (k >> 2) * (kP2Keys * 128) + (k & 3) * 32), idesc_s,
+                            k > 0 ? 1u : 0u);
+                umma_commit(bar(L::kSReady, r));
             };
+            auto issue_o = [&](int i, int r) {
+                const uint64_t vb = desc_at(vdesc, (i & 1) * L::kVBuf);
+#pragma unroll
+                for (int k = 0; k < kP2Keys / 16; ++k)
+                    umma_ts(tmem + L::col_o(r), tmem + L::col_s(r) + 8 * k,
+                            desc_at(vb, (k >> 2) * (HD * 128) + (k & 3) * 32), idesc_o,
+                            (i > 0 || k > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(bar(L::kKReady, 0), 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                issue_s(0, 1);
+                umma_commit(bar(L::kKFree, 0));
+            }
             for (int i = 0; i < ntiles && ok; ++i) {
-                const int b = i % L::kNB, j = i & 1;
-                ok = mbar_wait(bar(L::kKvReady, b), (i / L::kNB) & 1, abort_flag);
+                const int b = i & 1;
+                ok = mbar_wait(bar(L::kVReady, b), (i >> 1) & 1, abort_flag);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    if (ok && i >= 2)
-                        ok = mbar_wait(bar(L::kODone, 2 * r + j), ((i >> 1) & 1) ^ 1u, abort_flag);
+                    if (ok) ok = mbar_wait(bar(L::kPReady, r), i & 1, abort_flag);
+                    if (ok && r == 0 && i + 1 < ntiles)
+                        ok = mbar_wait(bar(L::kKReady, (i + 1) & 1), ((i + 1) >> 1) & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t qr_d = desc_at(qdesc, r * L::kQTile);
-                    const uint64_t kb = desc_at(kdesc, b * L::kKBuf);
-#pragma unroll
-                    for (int k = 0; k < HD / 16; ++k) {
-                        const uint64_t ad = desc_at(qr_d, (k >> 2) * (kPfRows * 128) + (k & 3) * 32);
-                        const uint64_t bd = desc_at(kb, (k >> 2) * (kPfKeys * 128) + (k & 3) * 32);
-                        umma_ss(tmem + L::col_s(r, j), ad, bd, idesc_s, k > 0 ? 1u : 0u);
+                    issue_o(i, r);
+                    if (i + 1 == ntiles) umma_commit(bar(L::kODone, r));
+                    if (r == 1) umma_commit(bar(L::kVFree, b));
+                    if (i + 1 < ntiles) {
+                        issue_s(i + 1, r);
+                        if (r == 1) umma_commit(bar(L::kKFree, (i + 1) & 1));
                     }
-                    umma_commit(bar(L::kSReady, 2 * r + j));
                 }
-                if (ok && i >= 1) ok = issue_o(i - 1);
             }
-            if (ok) ok = issue_o(ntiles - 1);
             if (!ok) {
                 flag(a.status, KVFP8_DEV_TIMEOUT);
                 *abort_flag = 1;
-                // let products already issued finish before tensor memory is released
-                if (o_issued > 0) {
-                    const int t = o_issued - 1;
-                    mbar_wait(bar(L::kKvFree, t % L::kNB), (t / L::kNB) & 1, &never);
-                }
+                // let the products already issued finish before tensor memory is released
+                umma_commit(bar(L::kDrain, 0));
+                mbar_wait(bar(L::kDrain, 0), 0, &never);
             }
         }
     }
@@ -1061,20 +1104,21 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         const int w8 = warp - 8;
         const uint32_t vsel = static_cast<uint32_t>(2 * (lane & 3)) | static_cast<uint32_t>(2 * (lane & 3) + 1) << 4;
         bool ok = true;
-        for (int i = 0; i < ntiles && ok; ++i) {
-            const int st = i % L::kNS, b = i % L::kNB;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kFull, st), (i / L::kNS) & 1, abort_flag));
-            // the buffer's previous tile (i-NB) has been through every product
-            if (ok)
+        for (int h = 0; h < 2 * ntiles && ok; ++h) {
+            const int st = h % L::kNS, i = h >> 1, hf = h & 1, b = i & 1;
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kFull, st), (h / L::kNS) & 1, abort_flag));
+            // the K buffer's previous tile (i-2) is through both S products
+            if (ok && hf == 0)
                 ok = __all_sync(0xFFFFFFFFu,
-                                mbar_wait(bar(L::kKvFree, b), ((i / L::kNB) & 1) ^ 1u, abort_flag));
+                                mbar_wait(bar(L::kKFree, b), ((i >> 1) & 1) ^ 1u, abort_flag));
             if (!ok) break;
             const uint64_t mask = meta[st];
             const uint8_t *kst = bp + L::kStage + st * L::kStageBytes;
             const uint8_t *vst = kst + kPfKeys * HD;
-            uint8_t *kdst0 = bp + L::kK + b * L::kKBuf;
-            const uint32_t vbase = base + L::kV + b * L::kVBuf;
-            // every load of a round before its conversions (as in prefill_kernel)
+            // this half's 64 keys: rows 64*hf.. of every 64-dim block of the K buffer
+            uint8_t *kdst0 = bp + L::kK + b * L::kKBuf + hf * (kPfKeys * 128);
+            // and key block hf of the V^T buffer
+            const uint32_t vbase = base + L::kV + b * L::kVBuf + hf * (HD * 128);
             uint4 kw[kKT];
             uint4 vw[kVG][2];
             auto v_load = [&](int g0) {
@@ -1105,6 +1149,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                     stsm_x4_t(vbase + sw128(n, ko), rv[0], rv[1], rv[2], rv[3]);
                 }
             };
+            // K: every load of the half before its conversions
 #pragma unroll
             for (int q = 0; q < kKT; ++q) {
                 const int task = ct + q * kCT;
@@ -1114,7 +1159,6 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                                                          swz<L::kSeg>(key, within >> 4));
                 if (!((mask >> key) & 1ull)) kw[q] = make_uint4(0u, 0u, 0u, 0u);
             }
-            v_load(0);
 #pragma unroll
             for (int q = 0; q < kKT; ++q) {
                 const int task = ct + q * kCT;
@@ -1130,22 +1174,33 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 h1.z = f16x2_from_e4m3x2(w.w);
                 h1.w = f16x2_from_e4m3x2_hi(w.w);
                 const int kb = (16 * c) / 64, c8 = ((16 * c) % 64) / 8;
-                uint8_t *kdst = kdst0 + kb * (kPfKeys * 128);
+                uint8_t *kdst = kdst0 + kb * (kP2Keys * 128);
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
                 *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
             }
+            if (hf == 1) {  // both halves of the tile's K are in place
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::kKReady, b));
+            }
+            // the V^T buffer's previous tile (i-2) is through both O products
+            if (hf == 0)
+                ok = __all_sync(0xFFFFFFFFu,
+                                mbar_wait(bar(L::kVFree, b), ((i >> 1) & 1) ^ 1u, abort_flag));
+            if (!ok) break;
+            v_load(0);
             v_store(0);
 #pragma unroll
             for (int g0 = kVG; g0 < kVB; g0 += kVG) {
                 v_load(g0);
                 v_store(g0);
             }
-            if (ct == 0) buf_mask[b] = mask;  // for the softmax warps, released with kv_ready
+            if (ct == 0) buf_mask[2 * b + hf] = mask;  // for the softmax warps, released with v_ready
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar(L::kEmpty, st));
-                mbar_arrive(bar(L::kKvReady, b));
+                if (hf == 1) mbar_arrive(bar(L::kVReady, b));
             }
         }
         if (!ok && lane == 0) {
@@ -1162,42 +1217,43 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         const int pos = Ls - nb + jq;               // last key position the row may see
         const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t scol = lane_addr + L::col_s(rt);
         float m_used = -INFINITY, la = 0.f, lb = 0.f;  // running maximum, row sum in two halves
         bool ok = true;
         for (int i = 0; i < ntiles && ok; ++i) {
-            const int b = i % L::kNB, j = i & 1;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kSReady, 2 * rt + j), (i >> 1) & 1, abort_flag));
-            // the tile's valid-key mask (already complete: S(i) needed the same phase)
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kKvReady, b), (i / L::kNB) & 1, abort_flag));
+            const int b = i & 1;
+            // S(rt, i) is done, and with it O(rt, i-1)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kSReady, rt), i & 1, abort_flag));
+            // the tile's valid-key masks (stored with its V^T)
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kVReady, b), (i >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const uint64_t mask = buf_mask[b];
-            const uint32_t scol = lane_addr + L::col_s(rt, j);
-            uint32_t s[2][32];
-            tmem_ld32(scol, s[0]);
-            tmem_ld32(scol + 32, s[1]);
-            tmem_wait_ld();
-            const int k0 = key_tile(i) * kPfKeys;
-            const int vis_n = row_ok ? min(kPfKeys, max(0, pos - k0 + 1)) : 0;
-            const uint64_t vis = mask & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
-            float mx, mult;
-            if (__all_sync(0xFFFFFFFFu, vis == ~0ull)) {
-                mx = (score_scale >= 0.f ? extreme64<true>(s) : extreme64<false>(s)) * score_scale;
-                mult = score_scale;
-            } else {
-                mx = -INFINITY;
-                mult = 1.f;
+            const int k0 = key_tile(i) * kP2Keys;
+            const int vis_n = row_ok ? min(kP2Keys, max(0, pos - k0 + 1)) : 0;
+            const uint64_t vis0 = buf_mask[2 * b] & (vis_n >= 64 ? ~0ull : ((1ull << vis_n) - 1));
+            const uint64_t vis1 = buf_mask[2 * b + 1] &
+                                  (vis_n >= 128 ? ~0ull : vis_n <= 64 ? 0ull : ((1ull << (vis_n - 64)) - 1));
+            const bool whole = __all_sync(0xFFFFFFFFu, (vis0 & vis1) == ~0ull);
+            auto vis_bits = [&](int c) {  // the visible keys among columns 32c..32c+31
+                return static_cast<uint32_t>((c < 2 ? vis0 : vis1) >> (32 * (c & 1)));
+            };
+            // pass 1: the row's maximum over the tile (raw extreme, scaled once, on a whole tile)
+            float mx = -INFINITY, ext = score_scale >= 0.f ? -INFINITY : INFINITY;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+            for (int c = 0; c < kP2Keys / 32; ++c) {
+                uint32_t s[32];
+                tmem_ld32(scol + 32 * c, s);
+                tmem_wait_ld();
+                if (whole) {
+                    ext = score_scale >= 0.f ? fmaxf(ext, extreme32<true>(s)) : fminf(ext, extreme32<false>(s));
+                } else {
+                    const uint32_t bits = vis_bits(c);
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float v = ((vis >> (32 * h + c)) & 1ull)
-                                            ? __uint_as_float(s[h][c]) * score_scale
-                                            : -INFINITY;
-                        s[h][c] = __float_as_uint(v);
-                        mx = fmaxf(mx, v);
-                    }
+                    for (int e = 0; e < 32; ++e)
+                        if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(s[e]) * score_scale);
+                }
             }
+            if (whole) mx = ext * score_scale;
             float factor = 1.f;
             if (mx > -INFINITY) {
                 if (m_used == -INFINITY) {
@@ -1208,11 +1264,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 }
             }
             if (__any_sync(0xFFFFFFFFu, factor != 1.f)) {
-                // O[rt] of the previous tile must be complete before it is rescaled
-                const int t = i - 1;
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, 2 * rt + (t & 1)), (t >> 1) & 1, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
+                // O(rt, i-1) is complete (covered by the commit of S(rt, i))
                 la *= factor;
                 lb *= factor;
 #pragma unroll 1
@@ -1225,33 +1277,45 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                     tmem_st32(lane_addr + L::col_o(rt) + c0, o);
                 }
             }
-            uint32_t p[32];
+            // pass 2: P = 2^(score - m) as f16 pairs, written over the scores already read
             const float msub = m_used == -INFINITY ? 0.f : m_used;
-            const uint64_t mul2 = pk2(mult, mult), sub2 = pk2(-msub, -msub);
+            const uint64_t sub2 = pk2(-msub, -msub);
+            const float mult = whole ? score_scale : 1.f;
+            const uint64_t mul2 = pk2(mult, mult);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int h = c >> 4, e = (2 * c) & 31;
-                const float2 x = upk2(fma_f32x2(pk2u(s[h][e], s[h][e + 1]), mul2, sub2));
-                p[c] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
-            }
-            tmem_st32(scol, p);
-            // the row sum: pairs of P added in f16 (one rounding on values <= 2^9), then fp32
+            for (int c = 0; c < kP2Keys / 32; ++c) {
+                uint32_t s[32];
+                tmem_ld32(scol + 32 * c, s);
+                tmem_wait_ld();
+                if (!whole) {
+                    const uint32_t bits = vis_bits(c);
 #pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-                uint32_t h2;
-                asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h2) : "r"(p[c]), "r"(p[c + 1]));
-                la += f16lo_f32(h2);
-                lb += f16hi_f32(h2);
+                    for (int e = 0; e < 32; ++e)
+                        s[e] = __float_as_uint(((bits >> e) & 1u) ? __uint_as_float(s[e]) * score_scale
+                                                                   : -INFINITY);
+                }
+                uint32_t p[16];
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    const float2 x = upk2(fma_f32x2(pk2u(s[2 * w], s[2 * w + 1]), mul2, sub2));
+                    p[w] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
+                }
+                tmem_st16(scol + 16 * c, p);
+                // the row sum: pairs of P added in f16 (one rounding on values <= 2^9), then fp32
+#pragma unroll
+                for (int w = 0; w < 16; w += 2) {
+                    uint32_t h2;
+                    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h2) : "r"(p[w]), "r"(p[w + 1]));
+                    la += f16lo_f32(h2);
+                    lb += f16hi_f32(h2);
+                }
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::kPReady, 2 * rt + j));
+            if (lane == 0) mbar_arrive(bar(L::kPReady, rt));
         }
-        if (ok) {
-            const int t = ntiles - 1;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, 2 * rt + (t & 1)), (t >> 1) & 1, abort_flag));
-        }
+        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, rt), 0, abort_flag));
         if (ok) {
             tc_fence_after();
             const float lsum = la + lb;

@@ -78,6 +78,8 @@ CASES = [
     ("prefill_from_empty", 32, 8, 128, 16, [50, 200], [50, 200]),
     ("zero_query_sequences", 32, 8, 128, 16, [80, 0, 300, 5], [0, 0, 40, 5]),
     ("g128_one_token_per_tile", 128, 1, 64, 16, [90], [6]),
+    ("bs8_two_row_tiles", 16, 4, 128, 8, [700, 90], [90, 40]),
+    ("hd64_long_rotated_passes", 16, 8, 64, 16, [3000, 129], [300, 129]),
 ]
 
 
@@ -90,7 +92,7 @@ def test_prefill_against_oracle(case):
 
 def test_growing_scores_take_the_rescale_path():
     # scores rise by about 0.3 per key, so the running maximum grows by far more than 2^8
-    # from one 64-key tile to the next and O is rescaled in tensor memory
+    # from one key tile to the next and O is rescaled in tensor memory
     lengths, qlens = [700, 300], [40, 20]
     q_fn = lambda q: torch.ones_like(q)                                    # noqa: E731
     k_fn = lambda k, pos: (pos.float() * 0.03)[:, None, None].expand_as(k) + 0.1 * k  # noqa: E731
