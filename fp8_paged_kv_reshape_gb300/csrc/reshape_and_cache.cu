@@ -84,19 +84,17 @@ struct FastDiv {
         y2 = pack2(y, y);
         nsa2 = pack2(-sa, -sa);
     }
-    // RN(x / |s|) with the sign of x, for a pair: q0 = x*y, then two residual steps
-    // q += fma(q, -|s|, x) * y, each operation on both lanes (fma(q, -|s|, x) equals
-    // fma(-q, |s|, x): negation is exact); the sign is restored from x (a zero may lose it)
+    // RN(x / |s|) for a pair: q0 = x*y, then two residual steps q += fma(q, -|s|, x) * y,
+    // each operation on both lanes (fma(q, -|s|, x) equals fma(-q, |s|, x): negation is
+    // exact).  The sign is that of x except for x = -0, where the residual sums give +0;
+    // the caller ORs the sign bits of x into the codes.
     __device__ __forceinline__ void quot2(float x0, float x1, float &r0, float &r1) const {
         const uint64_t x = pack2(x0, x1);
         const uint64_t q0 = mul2(x, y2);
         const uint64_t e0 = fma2(q0, nsa2, x);
         const uint64_t q1 = fma2(e0, y2, q0);
         const uint64_t e1 = fma2(q1, nsa2, x);
-        float a, b;
-        unpack2(fma2(e1, y2, q1), a, b);
-        r0 = __uint_as_float((__float_as_uint(a) & 0x7FFFFFFFu) | (__float_as_uint(x0) & 0x80000000u));
-        r1 = __uint_as_float((__float_as_uint(b) & 0x7FFFFFFFu) | (__float_as_uint(x1) & 0x80000000u));
+        unpack2(fma2(e1, y2, q1), r0, r1);
     }
 };
 
@@ -118,9 +116,23 @@ __device__ __noinline__ uint32_t patch_word(uint32_t w, uint32_t nanmask, float 
     return fix_byte(w, nanmask, 3, x3, s_neg);
 }
 
-// Eight floats -> eight E4M3 bytes (x[0] in the lowest byte): E4M3(x / s).
+// The sign bits of eight floats at bit 7 of the bytes of two words (element i in byte i % 4
+// of word i / 4); the other bits are left over and masked by the caller.
+__device__ __forceinline__ uint2 sign_bytes(const float (&x)[8]) {
+    auto w = [&](int i) { return __float_as_uint(x[i]); };
+    const uint32_t a = __byte_perm(w(0), w(1), 0x0073), b = __byte_perm(w(2), w(3), 0x0073);
+    const uint32_t c = __byte_perm(w(4), w(5), 0x0073), d = __byte_perm(w(6), w(7), 0x0073);
+    return make_uint2(__byte_perm(a, b, 0x5410), __byte_perm(c, d, 0x5410));
+}
+// the same for eight bf16 values in four words (the high byte of each)
+__device__ __forceinline__ uint2 sign_bytes_bf16(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3) {
+    return make_uint2(__byte_perm(w0, w1, 0x7531), __byte_perm(w2, w3, 0x7531));
+}
+
+// Eight floats -> eight E4M3 bytes (x[0] in the lowest byte): E4M3(x / s).  sgn: the sign
+// bits of x as sign_bytes gives them (used by the fast divide only).
 template <bool kFast>
-__device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const FastDiv &fd) {
+__device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const FastDiv &fd, uint2 sgn) {
     float q[8];
     if (kFast) {
 #pragma unroll
@@ -131,13 +143,16 @@ __device__ __forceinline__ uint2 quantize8(const float (&x)[8], float s, const F
     }
     uint32_t w0 = e4m3x2_from_f32(q[0], q[1]) | (e4m3x2_from_f32(q[2], q[3]) << 16);
     uint32_t w1 = e4m3x2_from_f32(q[4], q[5]) | (e4m3x2_from_f32(q[6], q[7]) << 16);
-    if (kFast) {  // the fast quotient carries sign(x); apply sign(s)
-        w0 ^= fd.neg;
-        w1 ^= fd.neg;
+    if (kFast) {  // sign(x) (which a zero quotient may have lost), then sign(s)
+        w0 = (w0 | (sgn.x & 0x80808080u)) ^ fd.neg;
+        w1 = (w1 | (sgn.y & 0x80808080u)) ^ fd.neg;
     }
-    const uint32_t m0 = nan_byte_mask(w0);
-    const uint32_t m1 = nan_byte_mask(w1);
-    if (__builtin_expect((m0 | m1) != 0u, 0)) {
+    // any NaN code (a byte whose low seven bits are all set)?  Adding 1 to each byte of the
+    // low-seven-bit part carries into bit 7 exactly there, and never into the next byte.
+    const uint32_t t0 = (w0 & 0x7F7F7F7Fu) + 0x01010101u, t1 = (w1 & 0x7F7F7F7Fu) + 0x01010101u;
+    if (__builtin_expect(((t0 | t1) & 0x80808080u) != 0u, 0)) {
+        const uint32_t m0 = nan_byte_mask(w0);
+        const uint32_t m1 = nan_byte_mask(w1);
         const bool s_neg = signbit(s);
         if (m0) w0 = patch_word(w0, m0, x[0], x[1], x[2], x[3], s_neg);
         if (m1) w1 = patch_word(w1, m1, x[4], x[5], x[6], x[7], s_neg);
@@ -196,6 +211,7 @@ struct Group<false> {  // bf16: 16 bytes
     __device__ __forceinline__ void bf16_words(uint32_t (&o)[4]) const {
         o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
     }
+    __device__ __forceinline__ uint2 signs8(int) const { return sign_bytes_bf16(v.x, v.y, v.z, v.w); }
     static constexpr int kElems = 8;
     static constexpr int kBytes = 16;
 };
@@ -226,6 +242,10 @@ struct Group<true> {  // fp32: 32 bytes
     __device__ __forceinline__ void bf16_words(uint32_t (&o)[4]) const {
         o[0] = bf16x2_from_f32(a.x, a.y); o[1] = bf16x2_from_f32(a.z, a.w);
         o[2] = bf16x2_from_f32(b.x, b.y); o[3] = bf16x2_from_f32(b.z, b.w);
+    }
+    __device__ __forceinline__ uint2 signs8(int) const {
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        return sign_bytes(x);
     }
     static constexpr int kElems = 8;
     static constexpr int kBytes = 32;
@@ -260,6 +280,10 @@ struct Wide<false> {  // bf16: 32 bytes
 #pragma unroll
         for (int i = 0; i < 8; ++i) o[i] = w[i];
     }
+    // sign bytes of elements 8h .. 8h+7
+    __device__ __forceinline__ uint2 signs8(int h) const {
+        return sign_bytes_bf16(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
+    }
     static constexpr int kElems = 16;
     static constexpr int kBytes = 32;
 };
@@ -279,6 +303,12 @@ struct Wide<true> {  // fp32: 64 bytes
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             o[i] = bf16x2_from_f32(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
+    }
+    __device__ __forceinline__ uint2 signs8(int h) const {
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = __uint_as_float(w[8 * h + i]);
+        return sign_bytes(x);
     }
     static constexpr int kElems = 16;
     static constexpr int kBytes = 64;
@@ -348,11 +378,13 @@ __device__ __forceinline__ void store_row(const G (&buf)[U], const RowCtx &c, co
             float x[G::kElems];
             buf[u].unpack(x);
             if constexpr (G::kElems == 8) {
-                st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd), c.pol);
+                st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd, buf[u].signs8(0)),
+                      c.pol);
             } else {
-                const uint2 lo = quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x), c.s, fd);
-                const uint2 hi =
-                    quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x + 8), c.s, fd);
+                const uint2 lo = quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x), c.s, fd,
+                                                  buf[u].signs8(0));
+                const uint2 hi = quantize8<kFast>(*reinterpret_cast<const float(*)[8]>(x + 8), c.s,
+                                                  fd, buf[u].signs8(1));
                 st_ef(dst + static_cast<int64_t>(g) * 16, make_uint4(lo.x, lo.y, hi.x, hi.y), c.pol);
             }
         }
@@ -516,7 +548,8 @@ __device__ __forceinline__ void store_row_rope(const Group<kF32> (&buf)[U], cons
                 unpack2(add2(mul2(p, sn), mul2(q, c)), x[2 * j + 1], x[2 * j + 3]);
             }
         }
-        if (g < groups) st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd), c.pol);
+        if (g < groups)
+            st_ef(dst + static_cast<int64_t>(g) * 8, quantize8<kFast>(x, c.s, fd, sign_bytes(x)), c.pol);
     }
 }
 
@@ -631,7 +664,9 @@ __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const Resh
                     float x[8];
                     in[u].unpack(x);
                     st_ef(dst + static_cast<int64_t>(g) * 8,
-                          fast ? quantize8<true>(x, s, fd) : quantize8<false>(x, s, fd), pol);
+                          fast ? quantize8<true>(x, s, fd, in[u].signs8(0))
+                               : quantize8<false>(x, s, fd, in[u].signs8(0)),
+                          pol);
                 }
             }
         }
