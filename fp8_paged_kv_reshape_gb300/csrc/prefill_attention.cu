@@ -820,6 +820,10 @@ struct Pf2Smem {
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int r) { return static_cast<uint32_t>(128 * r); }
     __host__ __device__ static constexpr uint32_t col_o(int r) { return static_cast<uint32_t>(256 + HD * r); }
+    // P of keys 16k..16k+15 (f16 pairs, 8 columns): the first half of the 32 columns that
+    // held the scores of keys 32(k/2)..+31, so each 32-key chunk's P overwrites only its own
+    // scores
+    __host__ __device__ static constexpr uint32_t col_p(int k) { return static_cast<uint32_t>(32 * (k >> 1) + 8 * (k & 1)); }
 };
 
 // the largest (kMax) or smallest of 32 scores, four chains of 3-input ops
@@ -1033,7 +1037,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 const uint64_t vb = desc_at(vdesc, (i & 1) * L::kVBuf);
 #pragma unroll
                 for (int k = 0; k < kP2Keys / 16; ++k)
-                    umma_ts(tmem + L::col_o(r), tmem + L::col_s(r) + 8 * k,
+                    umma_ts(tmem + L::col_o(r), tmem + L::col_s(r) + L::col_p(k),
                             desc_at(vb, (k >> 2) * (HD * 128) + (k & 3) * 32), idesc_o,
                             (i > 0 || k > 0) ? 1u : 0u);
             };
@@ -1237,22 +1241,31 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             auto vis_bits = [&](int c) {  // the visible keys among columns 32c..32c+31
                 return static_cast<uint32_t>((c < 2 ? vis0 : vis1) >> (32 * (c & 1)));
             };
-            // pass 1: the row's maximum over the tile (raw extreme, scaled once, on a whole tile)
+            // pass 1: the row's maximum over the tile (raw extreme, scaled once, on a whole
+            // tile).  Chunks 0 and 1, then 2 and 3, each pair loaded together; 2 and 3 stay in
+            // registers for pass 2.
+            uint32_t sa[32], sb[32];
             float mx = -INFINITY, ext = score_scale >= 0.f ? -INFINITY : INFINITY;
-#pragma unroll
-            for (int c = 0; c < kP2Keys / 32; ++c) {
-                uint32_t s[32];
-                tmem_ld32(scol + 32 * c, s);
-                tmem_wait_ld();
+            auto chunk_max = [&](const uint32_t (&sc)[32], int c) {
                 if (whole) {
-                    ext = score_scale >= 0.f ? fmaxf(ext, extreme32<true>(s)) : fminf(ext, extreme32<false>(s));
+                    ext = score_scale >= 0.f ? fmaxf(ext, extreme32<true>(sc)) : fminf(ext, extreme32<false>(sc));
                 } else {
                     const uint32_t bits = vis_bits(c);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(s[e]) * score_scale);
+                        if ((bits >> e) & 1u) mx = fmaxf(mx, __uint_as_float(sc[e]) * score_scale);
                 }
-            }
+            };
+            tmem_ld32(scol, sa);
+            tmem_ld32(scol + 32, sb);
+            tmem_wait_ld();
+            chunk_max(sa, 0);
+            chunk_max(sb, 1);
+            tmem_ld32(scol + 64, sa);
+            tmem_ld32(scol + 96, sb);
+            tmem_wait_ld();
+            chunk_max(sa, 2);
+            chunk_max(sb, 3);
             if (whole) mx = ext * score_scale;
             float factor = 1.f;
             if (mx > -INFINITY) {
@@ -1277,30 +1290,28 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                     tmem_st32(lane_addr + L::col_o(rt) + c0, o);
                 }
             }
-            // pass 2: P = 2^(score - m) as f16 pairs, written over the scores already read
+            // pass 2: P = 2^(score - m) as f16 pairs, written over the first half of each
+            // chunk's own scores; chunks 2 and 3 from registers, each followed by the reload
+            // of chunk 0 or 1 into its registers
             const float msub = m_used == -INFINITY ? 0.f : m_used;
             const uint64_t sub2 = pk2(-msub, -msub);
             const float mult = whole ? score_scale : 1.f;
             const uint64_t mul2 = pk2(mult, mult);
-#pragma unroll
-            for (int c = 0; c < kP2Keys / 32; ++c) {
-                uint32_t s[32];
-                tmem_ld32(scol + 32 * c, s);
-                tmem_wait_ld();
+            auto chunk_p = [&](uint32_t (&sc)[32], int c) {
                 if (!whole) {
                     const uint32_t bits = vis_bits(c);
 #pragma unroll
                     for (int e = 0; e < 32; ++e)
-                        s[e] = __float_as_uint(((bits >> e) & 1u) ? __uint_as_float(s[e]) * score_scale
-                                                                   : -INFINITY);
+                        sc[e] = __float_as_uint(((bits >> e) & 1u) ? __uint_as_float(sc[e]) * score_scale
+                                                                    : -INFINITY);
                 }
                 uint32_t p[16];
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
-                    const float2 x = upk2(fma_f32x2(pk2u(s[2 * w], s[2 * w + 1]), mul2, sub2));
+                    const float2 x = upk2(fma_f32x2(pk2u(sc[2 * w], sc[2 * w + 1]), mul2, sub2));
                     p[w] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
                 }
-                tmem_st16(scol + 16 * c, p);
+                tmem_st16(scol + 32 * c, p);
                 // the row sum: pairs of P added in f16 (one rounding on values <= 2^9), then fp32
 #pragma unroll
                 for (int w = 0; w < 16; w += 2) {
@@ -1309,7 +1320,14 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                     la += f16lo_f32(h2);
                     lb += f16hi_f32(h2);
                 }
-            }
+            };
+            chunk_p(sa, 2);
+            tmem_ld32(scol, sa);       // chunk 0's scores: its columns are not written yet
+            chunk_p(sb, 3);
+            tmem_ld32(scol + 32, sb);  // chunk 1's
+            tmem_wait_ld();
+            chunk_p(sa, 0);
+            chunk_p(sb, 1);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
