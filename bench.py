@@ -65,6 +65,10 @@ KERNEL_SOURCES = {
                           "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
     "paged_decode_attention": ["fp8_paged_kv_reshape_gb300/csrc/paged_decode_kernel.cuh",
                                "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
+    # the multi-query calls whose long chunks run on the tensor-core kernels
+    "prefill_attention": ["fp8_paged_kv_reshape_gb300/csrc/prefill_attention.cu",
+                          "fp8_paged_kv_reshape_gb300/csrc/paged_decode_kernel.cuh",
+                          "fp8_paged_kv_reshape_gb300/csrc/kvfp8_device.cuh"],
 }
 VARIANTS = ("fp8", "rope", "k_bf16", "v_bf16", "multi", "prefill")
 # a CPU sample of the multi-query forms attends with at most this many oracle FLOPs: the
@@ -495,7 +499,9 @@ def kernel_report(p: "Problem", t: dict, workload: str, variant: str):
         k["frac"] = k["gbs"] / peak
         k["frac_of_nominal_8tbs"] = k["gbs"] / NOMINAL_HBM_GBS
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
-    traffic = recorded_traffic(dom, workload if variant == "fp8" else "%s:%s" % (workload, variant))
+    # the attention group of the tensor-core route is recorded under its own kernel source
+    rec_kernel = "prefill_attention" if dom == "paged_decode_attention" and p.decode and p.tensor_route else dom
+    traffic = recorded_traffic(rec_kernel, workload if variant == "fp8" else "%s:%s" % (workload, variant))
     if p.decode and p.tensor_route:
         att = kernels["paged_decode_attention"]
         att["tflops"] = p.attn_flops / (att["ms"] * 1e-3) / 1e12
