@@ -158,6 +158,16 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -1222,7 +1232,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         const float score_scale = a.sm_scale * sk * 1.4426950408889634f;  // log2(e)
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t scol = lane_addr + L::col_s(rt);
-        float m_used = -INFINITY, la = 0.f, lb = 0.f;  // running maximum, row sum in two halves
+        float m_used = -INFINITY;
+        uint64_t lsum2 = pk2(0.f, 0.f);  // the row sum, in two fp32 halves
         bool ok = true;
         for (int i = 0; i < ntiles && ok; ++i) {
             const int b = i & 1;
@@ -1278,8 +1289,7 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             }
             if (__any_sync(0xFFFFFFFFu, factor != 1.f)) {
                 // O(rt, i-1) is complete (covered by the commit of S(rt, i))
-                la *= factor;
-                lb *= factor;
+                lsum2 = mul_f32x2(lsum2, pk2(factor, factor));
 #pragma unroll 1
                 for (int c0 = 0; c0 < HD; c0 += 32) {
                     uint32_t o[32];
@@ -1305,21 +1315,17 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                         sc[e] = __float_as_uint(((bits >> e) & 1u) ? __uint_as_float(sc[e]) * score_scale
                                                                     : -INFINITY);
                 }
+                // P = 2^x in fp32, rounded to f16 pairs for the product; the row sum adds the
+                // fp32 values in packed pairs
                 uint32_t p[16];
 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
                     const float2 x = upk2(fma_f32x2(pk2u(sc[2 * w], sc[2 * w + 1]), mul2, sub2));
-                    p[w] = ex2_f16x2(f16x2_from_f32(x.x, x.y));
+                    const float e0 = ex2(x.x), e1 = ex2(x.y);
+                    p[w] = f16x2_from_f32(e0, e1);
+                    lsum2 = add_f32x2(lsum2, pk2(e0, e1));
                 }
                 tmem_st16(scol + 32 * c, p);
-                // the row sum: pairs of P added in f16 (one rounding on values <= 2^9), then fp32
-#pragma unroll
-                for (int w = 0; w < 16; w += 2) {
-                    uint32_t h2;
-                    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h2) : "r"(p[w]), "r"(p[w + 1]));
-                    la += f16lo_f32(h2);
-                    lb += f16hi_f32(h2);
-                }
             };
             chunk_p(sa, 2);
             tmem_ld32(scol, sa);       // chunk 0's scores: its columns are not written yet
@@ -1336,7 +1342,8 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar(L::kODone, rt), 0, abort_flag));
         if (ok) {
             tc_fence_after();
-            const float lsum = la + lb;
+            const float2 ls = upk2(lsum2);
+            const float lsum = ls.x + ls.y;
             const float inv = lsum > 0.f ? sv / lsum : 0.f;
             uint4 *orow = reinterpret_cast<uint4 *>(
                 a.out + ((static_cast<int64_t>(qr.q0) + jq) * a.n_q + kvh * G + gq) * HD);
