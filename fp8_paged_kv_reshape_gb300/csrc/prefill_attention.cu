@@ -1112,7 +1112,10 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 *reinterpret_cast<uint4 *>(qt + (c >> 3) * (kPfRows * 128) + sw128(lr, c & 7)) = h;
             }
         }
-        constexpr int kKT = kPfKeys * (HD / 16) / kCT;                   // K tasks per thread
+        // K: a task is 8 dims of one key (8 FP8 bytes in, one 16-byte f16 chunk out); eight
+        // consecutive threads take the eight chunks of one 64-dim block row, so each
+        // quarter-warp's stores cover all 32 banks
+        constexpr int kKT = kPfKeys * (HD / 8) / kCT;                    // K tasks per thread
         constexpr int kVB = (kPfKeys / 8) * (HD / 32) / kP2ConvWarps;    // V^T blocks per warp
         constexpr int kVG = kVB < 4 ? kVB : 4;                           // V^T blocks per round
         const int w8 = warp - 8;
@@ -1133,7 +1136,6 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
             uint8_t *kdst0 = bp + L::kK + b * L::kKBuf + hf * (kPfKeys * 128);
             // and key block hf of the V^T buffer
             const uint32_t vbase = base + L::kV + b * L::kVBuf + hf * (HD * 128);
-            uint4 kw[kKT];
             uint4 vw[kVG][2];
             auto v_load = [&](int g0) {
 #pragma unroll
@@ -1164,33 +1166,27 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
                 }
             };
             // K: every load of the half before its conversions
+            uint2 kw[kKT];
 #pragma unroll
             for (int q = 0; q < kKT; ++q) {
                 const int task = ct + q * kCT;
-                const int key = task / (HD / 16), c = task % (HD / 16);
-                const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
-                kw[q] = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
-                                                         swz<L::kSeg>(key, within >> 4));
-                if (!((mask >> key) & 1ull)) kw[q] = make_uint4(0u, 0u, 0u, 0u);
+                const int key = task / (HD / 8), c = task % (HD / 8);
+                const int sgi = (8 * c) / L::kSeg, within = (8 * c) % L::kSeg;
+                kw[q] = *reinterpret_cast<const uint2 *>(kst + sgi * kPfKeys * L::kSeg +
+                                                         swz<L::kSeg>(key, within >> 4) + (within & 8));
+                if (!((mask >> key) & 1ull)) kw[q] = make_uint2(0u, 0u);
             }
 #pragma unroll
             for (int q = 0; q < kKT; ++q) {
                 const int task = ct + q * kCT;
-                const int key = task / (HD / 16), c = task % (HD / 16);
-                const uint4 w = kw[q];
-                uint4 h0, h1;
-                h0.x = f16x2_from_e4m3x2(w.x);
-                h0.y = f16x2_from_e4m3x2_hi(w.x);
-                h0.z = f16x2_from_e4m3x2(w.y);
-                h0.w = f16x2_from_e4m3x2_hi(w.y);
-                h1.x = f16x2_from_e4m3x2(w.z);
-                h1.y = f16x2_from_e4m3x2_hi(w.z);
-                h1.z = f16x2_from_e4m3x2(w.w);
-                h1.w = f16x2_from_e4m3x2_hi(w.w);
-                const int kb = (16 * c) / 64, c8 = ((16 * c) % 64) / 8;
-                uint8_t *kdst = kdst0 + kb * (kP2Keys * 128);
-                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
-                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
+                const int key = task / (HD / 8), c = task % (HD / 8);
+                const uint2 w = kw[q];
+                uint4 h;
+                h.x = f16x2_from_e4m3x2(w.x);
+                h.y = f16x2_from_e4m3x2_hi(w.x);
+                h.z = f16x2_from_e4m3x2(w.y);
+                h.w = f16x2_from_e4m3x2_hi(w.y);
+                *reinterpret_cast<uint4 *>(kdst0 + (c >> 3) * (kP2Keys * 128) + sw128(key, c & 7)) = h;
             }
             if (hf == 1) {  // both halves of the tile's K are in place
                 fence_proxy_async();
