@@ -545,19 +545,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             const uint8_t *vst = kst + kPfKeys * HD;
             uint8_t *kdst0 = bp + L::kK + b * L::kKBuf;
             uint8_t *vdst = bp + L::kV + b * L::kVBuf;
-            // K: 64 keys x HD/16 chunks of 16 fp8 -> f16 (invalid keys: zeros).
+            // K: 64 keys x HD/8 chunks of 8 fp8 -> one 16-byte f16 chunk (invalid keys: zeros);
+            // eight consecutive threads take the eight chunks of one 64-dim block row, so each
+            // quarter-warp's stores cover all 32 banks.
             // V^T by 8-key x 32-dim blocks: lane t converts dims (8j + 2(t%4), +1) of key t/4
             // (one e4m3 pair -> f16x2 per matrix j) and stmatrix.trans writes each dim's 8 keys
             // as one 16-byte row of V^T (head dims as rows, keys along K).
             // Every load of a round is issued before the first conversion, so their latencies
             // overlap (a store to shared memory would otherwise hold back the next load).
-            constexpr int kKT = kPfKeys * (HD / 16) / kCT;                   // K tasks per thread
+            constexpr int kKT = kPfKeys * (HD / 8) / kCT;                    // K tasks per thread
             constexpr int kVB = (kPfKeys / 8) * (HD / 32) / kPfConvWarps;    // V^T blocks per warp
             constexpr int kVG = kVB < 4 ? kVB : 4;                           // V^T blocks per round
             const int w4 = warp - 4;
             const uint32_t vbase = base + L::kV + b * L::kVBuf;
             const uint32_t vsel = static_cast<uint32_t>(2 * (lane & 3)) | static_cast<uint32_t>(2 * (lane & 3) + 1) << 4;
-            uint4 kw[kKT];
+            uint2 kw[kKT];
             uint4 vw[kVG][2];
             auto v_load = [&](int g0) {
 #pragma unroll
@@ -590,31 +592,24 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < kKT; ++j) {
                 const int task = ct + j * kCT;
-                const int key = task / (HD / 16), c = task % (HD / 16);  // dims 16c .. 16c+15
-                const int sgi = (16 * c) / L::kSeg, within = (16 * c) % L::kSeg;
-                kw[j] = *reinterpret_cast<const uint4 *>(kst + sgi * kPfKeys * L::kSeg +
-                                                         swz<L::kSeg>(key, within >> 4));
-                if (!((mask >> key) & 1ull)) kw[j] = make_uint4(0u, 0u, 0u, 0u);
+                const int key = task / (HD / 8), c = task % (HD / 8);  // dims 8c .. 8c+7
+                const int sgi = (8 * c) / L::kSeg, within = (8 * c) % L::kSeg;
+                kw[j] = *reinterpret_cast<const uint2 *>(kst + sgi * kPfKeys * L::kSeg +
+                                                         swz<L::kSeg>(key, within >> 4) + (within & 8));
+                if (!((mask >> key) & 1ull)) kw[j] = make_uint2(0u, 0u);
             }
             v_load(0);
 #pragma unroll
             for (int j = 0; j < kKT; ++j) {
                 const int task = ct + j * kCT;
-                const int key = task / (HD / 16), c = task % (HD / 16);
-                const uint4 w = kw[j];
-                uint4 h0, h1;
-                h0.x = f16x2_from_e4m3x2(w.x);
-                h0.y = f16x2_from_e4m3x2_hi(w.x);
-                h0.z = f16x2_from_e4m3x2(w.y);
-                h0.w = f16x2_from_e4m3x2_hi(w.y);
-                h1.x = f16x2_from_e4m3x2(w.z);
-                h1.y = f16x2_from_e4m3x2_hi(w.z);
-                h1.z = f16x2_from_e4m3x2(w.w);
-                h1.w = f16x2_from_e4m3x2_hi(w.w);
-                const int kb = (16 * c) / 64, c8 = ((16 * c) % 64) / 8;
-                uint8_t *kdst = kdst0 + kb * (kPfKeys * 128);
-                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8)) = h0;
-                *reinterpret_cast<uint4 *>(kdst + sw128(key, c8 + 1)) = h1;
+                const int key = task / (HD / 8), c = task % (HD / 8);
+                const uint2 w = kw[j];
+                uint4 h;
+                h.x = f16x2_from_e4m3x2(w.x);
+                h.y = f16x2_from_e4m3x2_hi(w.x);
+                h.z = f16x2_from_e4m3x2(w.y);
+                h.w = f16x2_from_e4m3x2_hi(w.y);
+                *reinterpret_cast<uint4 *>(kdst0 + (c >> 3) * (kPfKeys * 128) + sw128(key, c & 7)) = h;
             }
             v_store(0);
 #pragma unroll
