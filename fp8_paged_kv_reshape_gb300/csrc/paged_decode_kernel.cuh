@@ -512,13 +512,31 @@ __global__ void __launch_bounds__(256 * kCombineSlices) combine_kernel(const Ker
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
 // (head_dim * query tiles <= 128, and not the bf16-V form with two query tiles, whose extra
 // probability fragments do not fit); one otherwise.
-template <int HD, int NT, bool VT16>
-constexpr int min_ctas_per_sm() { return HD * NT <= 128 && !(VT16 && NT == 2) ? 2 : 1; }
+// 16 FP8 score columns at head_dim 128 keep q in shared memory instead of 32 registers a
+// lane, take at most 4 kv heads per CTA (5 warps) and run 3 CTAs per SM: 12 consumer warps per
+// SM instead of 8, for a consumer that is bound by its own dependency chains.
+template <int HD, int NT, bool KT16, bool VT16>
+__host__ __device__ constexpr bool q_in_smem() { return HD == 128 && NT == 2 && !KT16 && !VT16; }
+
+// kv heads (consumer warps) per CTA at most
+template <int HD, int NT, bool KT16, bool VT16>
+__host__ __device__ constexpr int max_heads() { return q_in_smem<HD, NT, KT16, VT16>() ? 4 : kMaxKvHeads; }
+
+template <int HD, int NT, bool KT16, bool VT16>
+__host__ __device__ constexpr int min_ctas_per_sm() {
+    return q_in_smem<HD, NT, KT16, VT16>() ? 3 : HD * NT <= 128 && !(VT16 && NT == 2) ? 2 : 1;
+}
+
+// bytes of one consumer warp's q fragments in shared memory: per 16-dim k-step, each lane's
+// words of both n-tiles (16 bytes)
+template <int HD>
+__host__ __device__ constexpr int q_smem_bytes_per_warp() { return (HD / 16) * 32 * 16; }
 
 // KT16 / VT16: that side's cache holds bf16 (mixed cache dtypes) instead of E4M3 bytes; its
 // fragments go to bf16 mma.sync without a convert and its scale is not applied.
 template <int HD, int NT, bool kMulti, bool KT16, bool VT16>
-__global__ void __launch_bounds__(kThreadsMax, min_ctas_per_sm<HD, NT, VT16>())
+__global__ void __launch_bounds__(32 * (max_heads<HD, NT, KT16, VT16>() + 1),
+                                  min_ctas_per_sm<HD, NT, KT16, VT16>())
 decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
               const KernelArgs a) {
     constexpr int KB = KT16 ? 2 : 1, VB = VT16 ? 2 : 1;  // bytes per element of each side
@@ -541,6 +559,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
     const uint32_t bars = base + static_cast<uint32_t>(S) * stage_bytes;  // full[S], empty[S]
     ChunkMeta *meta = reinterpret_cast<ChunkMeta *>(base_ptr + S * stage_bytes + 16 * S);
     volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(meta + S);
+    constexpr bool kQS = q_in_smem<HD, NT, KT16, VT16>();
+    // q fragments (kQS): after the ring's barriers, records and abort flag, 16-byte aligned
+    const uint32_t q_smem = (smem_u32(const_cast<int32_t *>(abort_flag)) + 16u + 15u) & ~15u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -713,7 +734,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
 
         float o[KP][2][NT][4];
         float m[NT][2], l[NT][2];
-        uint32_t qb[2 * KP][NT][2];
+        uint32_t qb[kQS ? 1 : 2 * KP][NT][2];
+        // kQS: this lane's words of k-step c at q_lane + 512 c
+        const uint32_t q_lane = q_smem + static_cast<uint32_t>(warp * q_smem_bytes_per_warp<HD>() + lane * 16);
         // multi-query form: per score column (query token j, head g) the last cache
         // position it may see, and its row within the sequence (-1: a padding column)
         int plim[NT][2], crow[NT][2];
@@ -766,30 +789,58 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                             crow[nt][c] = j < nq ? j * a.n_q + kvh * a.group + g : -1;
                         }
                 }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    // column gid of n-tile nt: query token jq, head gq of the group
+                // column gid of n-tile nt: query token jq, head gq of the group
+                auto q_row = [&](int nt, bool &qv) {
                     const int n = nt * 8 + gid;
                     const int jq = kMulti ? n / a.group : 0;
                     const int gq = kMulti ? n % a.group : n;
-                    const bool qv = kMulti ? jq < nq : n < a.group;
-                    const __nv_bfloat16 *qrow =
-                        a.query +
-                        ((static_cast<int64_t>(kMulti ? q0 + jq : mt.seq)) * a.n_q + kvh * a.group + gq) *
-                            HD;
+                    qv = kMulti ? jq < nq : n < a.group;
+                    return a.query +
+                           ((static_cast<int64_t>(kMulti ? q0 + jq : mt.seq)) * a.n_q + kvh * a.group + gq) * HD;
+                };
+                if constexpr (kQS) {
+                    // each lane's B fragment words, converted once per sequence, into its own
+                    // 16-byte slots (read back only by the same lane: no warp sync needed)
+                    bool qv[NT];
+                    const __nv_bfloat16 *qrow[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) qrow[nt] = q_row(nt, qv[nt]);
 #pragma unroll
                     for (int c = 0; c < 2 * KP; ++c) {
-                        if constexpr (KT16) {  // bf16 as it is, in the natural k order
-                            const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow + 16 * c);
-                            qb[c][nt][0] = qv ? qw[tig] : 0u;
-                            qb[c][nt][1] = qv ? qw[4 + tig] : 0u;
-                        } else {
+                        uint32_t wd[2 * NT];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
                             uint2 w = make_uint2(0u, 0u);
-                            if (qv) w = *reinterpret_cast<const uint2 *>(qrow + 16 * c + 4 * tig);
-                            qb[c][nt][0] = f16x2_from_f32(bf16lo(w.x), bf16hi(w.x));
-                            qb[c][nt][1] = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
+                            if (qv[nt]) w = *reinterpret_cast<const uint2 *>(qrow[nt] + 16 * c + 4 * tig);
+                            wd[2 * nt] = f16x2_from_f32(bf16lo(w.x), bf16hi(w.x));
+                            wd[2 * nt + 1] = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
+                        }
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(q_lane + 512u * c),
+                                     "r"(wd[0]), "r"(wd[1]), "r"(wd[2]), "r"(wd[3])
+                                     : "memory");
+                    }
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        bool qv;
+                        const __nv_bfloat16 *qrow = q_row(nt, qv);
+#pragma unroll
+                        for (int c = 0; c < 2 * KP; ++c) {
+                            if constexpr (KT16) {  // bf16 as it is, in the natural k order
+                                const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow + 16 * c);
+                                qb[c][nt][0] = qv ? qw[tig] : 0u;
+                                qb[c][nt][1] = qv ? qw[4 + tig] : 0u;
+                            } else {
+                                uint2 w = make_uint2(0u, 0u);
+                                if (qv) w = *reinterpret_cast<const uint2 *>(qrow + 16 * c + 4 * tig);
+                                qb[c][nt][0] = f16x2_from_f32(bf16lo(w.x), bf16hi(w.x));
+                                qb[c][nt][1] = f16x2_from_f32(bf16lo(w.y), bf16hi(w.y));
+                            }
                         }
                     }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
                     m[nt][0] = m[nt][1] = -INFINITY;
                     l[nt][0] = l[nt][1] = 0.f;
                 }
@@ -840,11 +891,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ C
                     const uint32_t a2 = f16x2_from_e4m3x2_hi(r0), a3 = f16x2_from_e4m3x2_hi(r1);
                     const uint32_t b0 = f16x2_from_e4m3x2(r2), b1 = f16x2_from_e4m3x2(r3);
                     const uint32_t b2 = f16x2_from_e4m3x2_hi(r2), b3 = f16x2_from_e4m3x2_hi(r3);
+                    if constexpr (kQS) {
+                        uint32_t qa[4], qc[4];  // k-steps 2kk, 2kk+1: (n-tile 0 b0, b1, n-tile 1 b0, b1)
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qa[0]), "=r"(qa[1]), "=r"(qa[2]), "=r"(qa[3])
+                                     : "r"(q_lane + 1024u * kk));
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(qc[0]), "=r"(qc[1]), "=r"(qc[2]), "=r"(qc[3])
+                                     : "r"(q_lane + 1024u * kk + 512u));
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma16816(sacc[nt], a0, a1, a2, a3, qb[2 * kk][nt][0], qb[2 * kk][nt][1]);
-                        mma16816(sacc[nt], b0, b1, b2, b3, qb[2 * kk + 1][nt][0],
-                                 qb[2 * kk + 1][nt][1]);
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816(sacc[nt], a0, a1, a2, a3, qa[2 * nt], qa[2 * nt + 1]);
+                            mma16816(sacc[nt], b0, b1, b2, b3, qc[2 * nt], qc[2 * nt + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816(sacc[nt], a0, a1, a2, a3, qb[2 * kk][nt][0], qb[2 * kk][nt][1]);
+                            mma16816(sacc[nt], b0, b1, b2, b3, qb[2 * kk + 1][nt][0],
+                                     qb[2 * kk + 1][nt][1]);
+                        }
                     }
                 }
 
@@ -1112,17 +1178,20 @@ cudaError_t run(const DecodeArgs &d, const DecodeWorkspace &ws, cudaStream_t str
     constexpr int SEGK = HD * KB >= 128 ? 128 : 64, SEGV = HD * VB >= 128 ? 128 : 64;
     const int kbytes = d.n_kv * HD * KB, vbytes = d.n_kv * HD * VB;  // cache row bytes
     // kv heads per CTA: the largest divisor of n_kv up to 8; the groups are a grid dimension
-    int hpc = std::min(d.n_kv, kMaxKvHeads);
+    int hpc = std::min(d.n_kv, max_heads<HD, NT, KT16, VT16>());
     while (d.n_kv % hpc != 0) --hpc;
     const int groups = d.n_kv / hpc;
     const int stage_bytes = kChunkTokens * hpc * HD * (KB + VB);
     const int ctas_per_sm = std::max(
-        1, std::min(min_ctas_per_sm<HD, NT, VT16>(), env_int("KVFP8_DECODE_CTAS_PER_SM", 2)));
+        1, std::min(min_ctas_per_sm<HD, NT, KT16, VT16>(), env_int("KVFP8_DECODE_CTAS_PER_SM", 3)));
     const int max_stages = std::max(2, std::min(8, env_int("KVFP8_DECODE_MAX_STAGES", 8)));
     // per stage: the K and V chunk, two mbarriers and one ChunkMeta; then the abort flag
     // and up to 1 KiB to align the ring to the 128-byte swizzle span; 1 KiB of the SM's
     // shared memory goes to each CTA's system use
-    auto smem_for = [&](int st) { return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 1024; };
+    // (and the consumers' q fragments where they live in shared memory)
+    constexpr size_t q_bytes =
+        q_in_smem<HD, NT, KT16, VT16>() ? 4 * q_smem_bytes_per_warp<HD>() + 16 : 0;
+    auto smem_for = [&](int st) { return static_cast<size_t>(st) * (stage_bytes + 32) + 16 + 1024 + q_bytes; };
     const size_t sm_budget = static_cast<size_t>(smem_optin) + 1024;
     int stages = max_stages;
     while (stages > 2 && (smem_for(stages) + 1024) * ctas_per_sm > sm_budget) --stages;
