@@ -405,10 +405,13 @@ __device__ __forceinline__ void pipelined_rows(const ReshapeArgs &a, const RowCt
     const FastDiv fd(c.s);
     const int units = a.row_elems / G::kElems;
     G A[U], B[U];
+    // the first row's source is read before its slot is known (the source row exists for
+    // every token; a padding row's bytes are simply not stored), so the warp's first loads do
+    // not wait behind the slot load
+    if (r < rows) load_row(A, c, r, units, lane);
     int64_t s1 = slot_of(a, r, rows);
     int64_t s2 = slot_of(a, r + stride, rows);
     bool ok1 = r < rows && row_ok(a, r, s1, lane);
-    if (ok1) load_row(A, c, r, units, lane);
     while (r < rows) {
         int64_t rn = r + stride;
         bool ok2 = rn < rows && row_ok(a, rn, s2, lane);
