@@ -8,7 +8,7 @@
 //
 // Design (HBM-bound: 1 byte of K and 1 of V per element, G = n_q/n_kv flops per byte):
 //  * Work split: the cache is cut into 16-token chunks; the chunks of all sequences are
-//    laid end to end and each CTA of a fixed grid (one or two per SM; fewer when there
+//    laid end to end and each CTA of a fixed grid (one to three per SM; fewer when there
 //    are fewer chunks than CTAs) takes an equal contiguous, non-empty range, whatever
 //    the length mix.  A sequence that lies inside one CTA is finished there; otherwise
 //    each CTA writes a partial (normalized o, log2-sum-exp) and a combine kernel merges
@@ -20,8 +20,8 @@
 //    predecessor; while a decode CTA waits for the plan it prefetches its slice of the
 //    block tables into L2, and its producer prefetches each next sequence's query rows.
 //  * One CTA = one producer warp + one consumer warp per kv head of its head group (the
-//    kv heads split into equal groups of at most 8, a second grid dimension; one group
-//    when n_kv <= 8).  A 16-token chunk of a block holds all kv heads of those tokens (16
+//    kv heads split into equal groups of at most 8, or 4 for 16 FP8 score columns at head_dim
+//    128, a second grid dimension; one group when n_kv is at most that).  A 16-token chunk of a block holds all kv heads of those tokens (16
 //    contiguous rows of n_kv*head_dim bytes), and a CTA fetches its group's part of them,
 //    so the producer issues TMA tensor loads of [16 rows x 128 B] boxes (one per head and
 //    128-byte segment of head_dim) with 128-byte swizzle into a multi-stage ring, on an
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(256 * kCombineSlices) combine_kernel(const Ker
 
 // Two CTAs per SM where the accumulators fit in the resulting 96 registers per thread
 // (head_dim * query tiles <= 128, and not the bf16-V form with two query tiles, whose extra
-// probability fragments do not fit); one otherwise.
+// probability fragments do not fit); three for the form below; one otherwise.
 // 16 FP8 score columns at head_dim 128 keep q in shared memory instead of 32 registers a
 // lane, take at most 4 kv heads per CTA (5 warps) and run 3 CTAs per SM: 12 consumer warps per
 // SM instead of 8, for a consumer that is bound by its own dependency chains.
