@@ -581,12 +581,14 @@ __device__ __forceinline__ void rope_token_rows(const ReshapeArgs &a, const RowC
     RopeCS tc;
     int64_t s1 = slot_at(t), p1 = pos_at(t);
     int64_t s2 = slot_at(t + W), p2 = pos_at(t + W);
-    bool ok1 = ok_of(t, s1, p1);
-    if (ok1) {
+    // the first token's rows are read before its slot and position are known (the source
+    // rows exist for every token), so the warp's first loads do not wait behind those loads
+    if (t < T) {
         load_row(A, ck, 2 * t, groups, lane);
-        load_cs(tc, a, p1, lane);
         load_row(B, cv, 2 * t + 1, groups, lane);
     }
+    bool ok1 = ok_of(t, s1, p1);
+    if (ok1) load_cs(tc, a, p1, lane);
     while (t < T) {
         const int64_t tn = t + W;
         const bool ok2 = ok_of(tn, s2, p2);
