@@ -183,8 +183,8 @@ KVFP8_API size_t kvfp8_paged_decode_workspace_size(int32_t num_seqs, int32_t n_q
  * seq_lens          device int32 [num_seqs]
  * num_seqs >= 0; n_q % n_kv == 0; head_dim in {64, 128, 256}; block_size in
  * {8, 16, 32, 64, 128, 256}; num_blocks*block_size < 2^31.  Any n_kv: a CTA serves a
- * group of at most 8 kv heads (the largest divisor of n_kv up to 8), the groups side by
- * side.  Groups of up to 16 query heads per kv head (8 at head_dim 256) run on the
+ * group of at most 8 kv heads (4 when a kv head has 9-16 score columns at head_dim 128 on
+ * an FP8 cache; the largest divisor of n_kv up to that), the groups side by side.  Groups of up to 16 query heads per kv head (8 at head_dim 256) run on the
  * split-KV kernel; larger ones, up to 128, on the tensor-core kernel of
  * kvfp8_paged_attention_multi; more return KVFP8_ERR_UNSUPPORTED.
  * sm_scale          <= 0 selects 1/sqrt(head_dim)
