@@ -620,7 +620,46 @@ def run_ours(args, rank, world, device):
     return line
 
 
+def gpu_local_cpus(device):
+    """The host CPUs on the GPU's own NUMA node (from sysfs), or None where that is not
+    available: pinned buffers allocated from one of them land in the memory next to the GPU's
+    host link instead of behind the link between host sockets."""
+    try:
+        pr = torch.cuda.get_device_properties(device)
+        bus = "%04x:%02x:%02x.0" % (getattr(pr, "pci_domain_id", 0), pr.pci_bus_id, pr.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/local_cpulist" % bus) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        avail = os.sched_getaffinity(0)
+        cpus &= avail
+        return cpus if cpus and cpus != avail else None
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
 def run_e2e(args, p: Problem, device):
+    """The end-to-end leg, run with the process on the GPU's own host CPUs (where sysfs names
+    them) so that its pinned buffers are allocated in the memory next to the GPU."""
+    local = gpu_local_cpus(device)
+    old = os.sched_getaffinity(0) if local else None
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        r = run_e2e_pinned(args, p, device)
+    finally:
+        if old:
+            os.sched_setaffinity(0, old)
+    r["host_cpus"] = "GPU-local NUMA node (%d CPUs)" % len(local) if local else "unrestricted"
+    return r
+
+
+def run_e2e_pinned(args, p: Problem, device):
     """Same metric through the public API with host inputs: every step copies its inputs
     from pinned host memory and reads the output back, inside the timed region.  As a serving
     loop would, the copies go on a copy stream into two alternating device input sets, so

@@ -57,6 +57,9 @@ CASES = [
     ("zero_queries", 32, 8, 128, 16, [50, 80, 0], [0, 3, 0]),
     ("mha16_head_groups_q1", 16, 16, 128, 16, [300, 33], [1, 1]),
     ("g2_12_kv_heads_q8", 24, 12, 64, 16, [200, 100], [8, 5]),
+    # 16 columns at head_dim 128: head groups of 3 (6 kv heads) and of 1 kv head
+    ("g4_q4_six_kv_heads", 24, 6, 128, 16, [700, 64], [4, 3]),
+    ("g16_q1_one_kv_head", 16, 1, 128, 16, [500, 90], [1, 1]),
 ]
 
 
