@@ -231,6 +231,110 @@ struct PrefillArgs {
     int32_t row_tiles;  // tiles of 128 score rows per (sequence, kv head)
 };
 
+// ---------------------------------------------------------------- work order
+//
+// The CTAs of the sequences with the most keys go first.  The hardware starts CTAs in index
+// order as SMs free up, so giving the low indices to the longest sequences keeps one of them
+// from starting last and running alone at the end (longest-processing-time-first list
+// scheduling; with lengths log-uniform over 16..32768 tokens, as in a serving mix, index
+// order leaves the last SMs busy ~20 % past the mean).  Sequences are ranked by a bucket of
+// their length, four buckets per octave (lengths in one bucket differ by less than 19 %),
+// longest bucket first, and by index within a bucket.
+
+__device__ __forceinline__ int length_bucket(int len, int max_len) {
+    const int l = min(max(len, 0), max_len);
+    if (l == 0) return 0;
+    const int b = 31 - __clz(l);                                     // floor(log2 l), 0..30
+    const int frac = b >= 2 ? (l >> (b - 2)) & 3 : (l << (2 - b)) & 3;  // next two bits
+    return 1 + 4 * b + frac;                                         // 1..124
+}
+
+// The sequence of rank u (0 = longest).  Every thread of the CTA calls it (it synchronizes
+// the CTA); scratch is 168 words of this CTA's shared memory, free until it returns.
+__device__ __forceinline__ int seq_of_rank(const int32_t *seq_lens, int num_seqs, int max_len, int u,
+                           uint32_t *scratch) {
+    if (num_seqs <= 1) return u;
+    uint32_t *cnt = scratch;                      // [128] sequences per bucket
+    // bucket of rank u, rank within it, the result, and whether the result is final
+    volatile uint32_t *pick = scratch + 128;
+    volatile uint32_t *wsum = scratch + 136;      // [32] per-warp counts of one round
+    const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    const int nwarps = nthr >> 5;
+    // bucket of sequence tid, kept for the histogram and the first round of the scan
+    const int my_bucket = tid < num_seqs ? length_bucket(seq_lens[tid], max_len) : -1;
+    if (num_seqs <= nthr) {  // lengths all in one bucket (a batch of equal lengths): index order
+        const int b0 = length_bucket(seq_lens[0], max_len);
+        if (__syncthreads_and(tid >= num_seqs || my_bucket == b0)) return u;
+    }
+    for (int b = tid; b < 128; b += nthr) cnt[b] = 0u;
+    if (tid == 0) {  // (u < num_seqs always finds its bucket; index order otherwise)
+        pick[0] = 0u;
+        pick[1] = 0u;
+        pick[2] = static_cast<uint32_t>(u);
+        pick[3] = 0u;
+    }
+    __syncthreads();
+    for (int s = tid; s < num_seqs; s += nthr)
+        atomicAdd(&cnt[s == tid ? my_bucket : length_bucket(seq_lens[s], max_len)], 1u);
+    __syncthreads();
+    if (warp == 0) {
+        // lane l holds buckets 127-4l .. 124-4l, so lanes run longest first
+        uint32_t c[4], tot = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            c[q] = cnt[127 - 4 * lane - q];
+            tot += c[q];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        uint32_t before = incl - tot;
+        const uint32_t uu = static_cast<uint32_t>(u);
+        if (uu >= before && uu < incl) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (uu < before + c[q]) {
+                    pick[0] = static_cast<uint32_t>(127 - 4 * lane - q);
+                    pick[1] = uu - before;
+                    // every sequence in one bucket (a batch of equal lengths): index order
+                    if (c[q] == static_cast<uint32_t>(num_seqs)) pick[3] = 1u;
+                    break;
+                }
+                before += c[q];
+            }
+        }
+    }
+    __syncthreads();
+    if (pick[3] != 0u) return u;
+    const int B = static_cast<int>(pick[0]);
+    const uint32_t k = pick[1];
+    // the k-th sequence of bucket B in index order, nthr sequences a round
+    uint32_t seen = 0;
+    for (int s0 = 0; s0 < num_seqs; s0 += nthr) {
+        const int s = s0 + tid;
+        const int b = s0 == 0 ? my_bucket : (s < num_seqs ? length_bucket(seq_lens[s], max_len) : -1);
+        const bool in = s < num_seqs && b == B;
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, in);
+        if (lane == 0) wsum[warp] = static_cast<uint32_t>(__popc(bal));
+        __syncthreads();
+        uint32_t pre = seen, tot = 0;
+        for (int w = 0; w < nwarps; ++w) {
+            const uint32_t v = wsum[w];
+            if (w < warp) pre += v;
+            tot += v;
+        }
+        pre += static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
+        if (in && pre == k) pick[2] = static_cast<uint32_t>(s);
+        seen += tot;
+        __syncthreads();  // pick[2] is written; wsum may be reused
+        if (seen > k) break;
+    }
+    return static_cast<int>(pick[2]);
+}
+
 // Shared-memory plan (byte offsets from a 1024-aligned base).  Q is converted once; K and
 // V^T (f16) have NB buffers, and so do the scores in tensor memory; the FP8 staging ring has
 // NS stages.  At head_dim 256 the f16 buffers fill the shared memory: NB = 2, NS = 1.
@@ -254,13 +358,15 @@ struct PfSmem {
     static constexpr int kStage = kV + kNB * kVBuf;                // fp8 K then V, per stage
     static constexpr int kStageBytes = 2 * kPfKeys * HD;
     static constexpr int kBars = kStage + kNS * kStageBytes;
-    // mbarriers: full[NS], empty[NS], then per buffer kv_ready, kv_free, s_ready, p_ready.
-    // kv_free[b] completes when the products of the buffer's tile are done (one commit after
-    // its O product covers its S product too); it also tells that O is up to date.
+    // mbarriers: full[NS], empty[NS], then per buffer kv_ready, kv_free, s_ready, p_ready,
+    // and one to drain the tensor core on a timeout.  kv_free[b] completes when the products
+    // of the buffer's tile are done (one commit after its O product covers its S product
+    // too); it also tells that O is up to date.
     static constexpr int kFull = kBars, kEmpty = kFull + 8 * kNS, kKvReady = kEmpty + 8 * kNS;
     static constexpr int kKvFree = kKvReady + 8 * kNB, kSReady = kKvFree + 8 * kNB;
     static constexpr int kPReady = kSReady + 8 * kNB;
-    static constexpr int kMeta = kPReady + 8 * kNB;                // valid-key mask per stage
+    static constexpr int kDrain = kPReady + 8 * kNB;
+    static constexpr int kMeta = kDrain + 8;                       // valid-key mask per stage
     static constexpr int kBufMask = kMeta + 8 * kNS;               // valid-key mask per K/V buffer
     static constexpr int kMisc = kBufMask + 8 * kNB;               // tmem base, abort flag
     static constexpr int kTotal = kMisc + 16;
@@ -292,17 +398,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
     auto bar = [&](int off, int i) { return base + static_cast<uint32_t>(off + 8 * i); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // kv head fastest, then row tile, then sequence: the CTAs resident at one time read every
-    // kv head's slice of the same cache rows, and a (sequence, kv head)'s row tiles run
-    // together, so its K/V tiles are fetched from HBM once and re-read from L2
+    // kv head fastest, then row tile, then sequence (longest first): the CTAs resident at one
+    // time read every kv head's slice of the same cache rows, and a (sequence, kv head)'s row
+    // tiles run together, so its K/V tiles are fetched from HBM once and re-read from L2
     const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.n_kv));
     const int tile = static_cast<int>((blockIdx.x / static_cast<unsigned>(a.n_kv)) % static_cast<unsigned>(a.row_tiles));
-    const int seq = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
+    const int rank = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
 
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
+    // the K buffers are free scratch until the pipeline starts
+    const int seq = seq_of_rank(a.seq_lens, a.num_seqs, a.max_len, rank,
+                                reinterpret_cast<uint32_t *>(bp + L::kK));
     if (!scale_ok(sk) || !scale_ok(sv)) {
-        if (seq == 0 && tile == 0 && kvh == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        if (blockIdx.x == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
         return;
     }
     // this sequence's query rows (qsl == nullptr: one query per sequence, row seq) and cached
@@ -352,6 +461,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             mbar_init(bar(L::kSReady, b), 1);
             mbar_init(bar(L::kPReady, b), 4);
         }
+        mbar_init(bar(L::kDrain, 0), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -457,7 +567,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             // operand descriptors computed once; each product adds its constant offset
             const uint64_t qdesc = sw128_desc(base + L::kQ), kdesc = sw128_desc(base + L::kK),
                            vdesc = sw128_desc(base + L::kV);
-            int o_issued = 0;  // O products issued so far
             bool ok = true;
             auto issue_o = [&](int t) {  // O += P(t) . V(t), then release tile t's buffers
                 const int b = t % L::kNB;
@@ -469,7 +578,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
                     umma_ts(tmem + L::kColO, tmem + 64 * b + 8 * k, desc_at(vb, k * 32), idesc_o,
                             (t > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bar(L::kKvFree, b));
-                ++o_issued;
                 return true;
             };
             for (int i = 0; i < ntiles && ok; ++i) {
@@ -494,11 +602,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ 
             if (!ok) {
                 flag(a.status, KVFP8_DEV_TIMEOUT);
                 *abort_flag = 1;
-                // let products already issued finish before tensor memory is released
-                if (o_issued > 0) {
-                    const int t = o_issued - 1;
-                    mbar_wait(bar(L::kKvFree, t % L::kNB), (t / L::kNB) & 1, &never);
-                }
+                // let the products already issued finish before tensor memory is released
+                umma_commit(bar(L::kDrain, 0));
+                mbar_wait(bar(L::kDrain, 0), 0, &never);
             }
         }
     } else if (warp >= 4) {
@@ -875,12 +981,15 @@ prefill2_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.n_kv));
     const int ctile = static_cast<int>((blockIdx.x / static_cast<unsigned>(a.n_kv)) % static_cast<unsigned>(a.row_tiles));
-    const int seq = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
+    const int rank = static_cast<int>(blockIdx.x / static_cast<unsigned>(a.n_kv * a.row_tiles));
 
     const float sk = load_scale(a.k_scale, a.scale_dtype);
     const float sv = load_scale(a.v_scale, a.scale_dtype);
+    // longest sequences first; the K buffers are free scratch until the pipeline starts
+    const int seq = seq_of_rank(a.seq_lens, a.num_seqs, a.max_len, rank,
+                                reinterpret_cast<uint32_t *>(bp + L::kK));
     if (!scale_ok(sk) || !scale_ok(sv)) {
-        if (seq == 0 && ctile == 0 && kvh == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        if (blockIdx.x == 0 && tid == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
         return;
     }
     const int raw_nq = a.qsl[seq + 1] - a.qsl[seq];

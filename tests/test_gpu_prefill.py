@@ -90,6 +90,22 @@ def test_prefill_against_oracle(case):
     gpu_util.assert_attention_close(out, ref, name)
 
 
+@pytest.mark.parametrize("n_q,n_kv,hd,qlen", [(32, 8, 128, 5), (8, 2, 64, 40)],
+                         ids=["one_row_tile", "two_row_tiles"])
+def test_many_sequences_of_mixed_lengths_run_longest_first(n_q, n_kv, hd, qlen):
+    # The CTAs take the sequences longest first, each CTA ranking every sequence's length
+    # itself.  470 sequences are more than a CTA's 448 threads, so its lookup of the
+    # sequence of a given rank takes two rounds; lengths repeat within a length bucket, and
+    # a few sequences are empty.  Every row must land where it belongs (the output starts
+    # as NaN, so a row that no CTA writes fails the comparison).
+    rng = np.random.default_rng(qlen)
+    lengths = rng.integers(qlen, 120, 470)
+    lengths[rng.choice(470, 6, replace=False)] = 0
+    qlens = np.where(lengths > 0, qlen, 0)
+    out, ref = _run(n_q, n_kv, hd, 16, lengths.tolist(), qlens.tolist(), seed=qlen)
+    gpu_util.assert_attention_close(out, ref, "470 sequences, %d query tokens" % qlen)
+
+
 def test_growing_scores_take_the_rescale_path():
     # scores rise by about 0.3 per key, so the running maximum grows by far more than 2^8
     # from one key tile to the next and O is rescaled in tensor memory
