@@ -632,6 +632,279 @@ __global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const Reshape
         rope_token_rows<kF32, U, false>(a, ck, cv, t, W, lane);
 }
 
+// ---------------------------------------------------------------- rope + cache write, staged
+//
+// The rope write with its source rows staged in shared memory (bf16 sources, 16-element
+// units).  The kernel above keeps each warp's next rows in registers, and the rotation's
+// table values and temporaries take so many registers (117) that 16 warps fit an SM, with
+// about one row per warp in flight: too few bytes in flight to cover HBM latency.  Here
+// each warp owns a ring of kRing slots; a slot holds one token's K row and V row (the source
+// bytes as they are) and its table row, brought by three bulk copies (cp.async.bulk, issued
+// by one lane) that complete on the slot's mbarrier.  The copies run kRing tokens ahead of
+// the token the warp converts, so the bytes in flight are set by the ring, not by
+// registers.  A lane converts 16 consecutive elements and stores their codes with one
+// 16-byte store; the NeoX partner unit is read from shared memory, not shuffled.  The
+// arithmetic, and so every byte, is that of store_row_rope and store_row.
+constexpr int kRing = 3;
+// per warp: kRing mbarriers (8 bytes), then kRing (slot, position) pairs (16 bytes), padded
+// to 16 bytes so that the slots (bulk-copy destinations) start 16-byte aligned
+constexpr int kRingHeader = (kRing * (8 + 16) + 15) / 16 * 16;
+static_assert(kRingHeader >= 8 * kRing + 16 * kRing && kRingHeader % 16 == 0, "ring header");
+
+__host__ __device__ constexpr int ring_slot_bytes(int row_elems, int rot) {
+    return 2 * row_elems * 2 + rot * 4;  // K row, V row (bf16), table row (fp32)
+}
+__host__ __device__ constexpr int ring_region_bytes(int row_elems, int rot) {
+    return kRingHeader + kRing * ring_slot_bytes(row_elems, rot);
+}
+
+__device__ __forceinline__ void ring_bar_init(uint32_t bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void ring_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void ring_arrive_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool ring_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// bounded wait (~2 s at 2 GHz); false when it runs out
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity) {
+    if (ring_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 0; it < (1u << 30); ++it) {
+        if (ring_try(bar, parity)) return true;
+        if ((it & 15u) == 15u && clock64() - t0 > 4000000000LL) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ float4 lds16f(uint32_t addr) {
+    const uint4 v = lds16(addr);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
+}
+// 16 bf16 values (32 bytes of shared memory) -> floats, and the words themselves
+__device__ __forceinline__ void lds_bf16x16(uint32_t addr, float (&x)[16], uint32_t (&w)[8]) {
+    const uint4 a = lds16(addr), b = lds16(addr + 16);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16lo(w[i]);
+        x[2 * i + 1] = bf16hi(w[i]);
+    }
+}
+
+// The staged path takes bf16 sources with rows of 16-element units, and NeoX rotations of
+// at least 32 dims (a unit and its partner then lie in different halves).
+bool rope_ring_ok(const ReshapeArgs &a) {
+    return a.src_dtype != KVFP8_F32 && a.row_elems % 16 == 0 && a.row_elems <= 2048 &&
+           (!a.neox || a.rot >= 32);
+}
+
+template <int U, bool kFast>
+__device__ __forceinline__ void ring_tokens(const ReshapeArgs &a, uint32_t region, uint8_t *region_p,
+                                            int64_t t, int64_t W, int lane, float sk, float sv) {
+    const FastDiv fk(sk), fv(sv);
+    const uint64_t pol = evict_first_policy();
+    const int64_t T = a.num_tokens;
+    const int rb = a.row_elems * 2;                       // source row bytes
+    const uint32_t slot_bytes = static_cast<uint32_t>(ring_slot_bytes(a.row_elems, a.rot));
+    const uint32_t tx = slot_bytes;
+    volatile int64_t *meta = reinterpret_cast<volatile int64_t *>(region_p + 8 * kRing);
+    const uint32_t slots = region + kRingHeader;
+    const int units = a.row_elems >> 4;
+    const int half = a.rot >> 1;
+    const int64_t kstride = a.key_stride * 2, vstride = a.value_stride * 2;
+    const uint8_t *kbase = static_cast<const uint8_t *>(a.key);
+    const uint8_t *vbase = static_cast<const uint8_t *>(a.value);
+    // the first lane fetches token tok into slot r: its slot and position (read one token
+    // ahead, so the warp does not wait for them) are checked here; a token with nothing to
+    // store completes the slot's phase without copies
+    auto issue = [&](int64_t tok, int r, int64_t slot, int64_t pos) {
+        const bool ok = slot >= 0 && slot < a.num_slots && pos_ok(a, pos);
+        if (!ok && slot != -1) flag(a.status, KVFP8_DEV_BAD_SLOT);
+        meta[2 * r] = ok ? slot : -1;
+        meta[2 * r + 1] = pos;
+        const uint32_t bar = region + 8 * r;
+        if (ok) {
+            const uint32_t dst = slots + r * slot_bytes;
+            ring_arrive_tx(bar, tx);
+            bulk_g2s(dst, kbase + tok * kstride, rb, bar);
+            bulk_g2s(dst + rb, vbase + tok * vstride, rb, bar);
+            bulk_g2s(dst + 2 * rb, a.cos_sin + pos * a.rot, static_cast<uint32_t>(a.rot * 4), bar);
+        } else {
+            ring_arrive(bar);
+        }
+    };
+    int issued = 0;  // tokens fetched so far (this warp's j-th token is t + j*W)
+    auto slot_at = [&](int64_t tok) -> int64_t { return tok < T ? __ldg(a.slot_mapping + tok) : -1; };
+    auto pos_at = [&](int64_t tok) -> int64_t { return tok < T ? __ldg(a.positions + tok) : 0; };
+    int64_t nslot = -1, npos = 0;  // the next token to fetch (lane 0)
+    if (lane == 0) {
+        for (int r = 0; r < kRing; ++r) ring_bar_init(region + 8 * r);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int r = 0; r < kRing && t + r * W < T; ++r) {
+            issue(t + r * W, r, slot_at(t + r * W), pos_at(t + r * W));
+            ++issued;
+        }
+        nslot = slot_at(t + kRing * W);
+        npos = pos_at(t + kRing * W);
+    }
+    __syncwarp();
+    bool ok = true;
+    int j = 0;
+    for (; t + j * W < T; ++j) {
+        const int r = j % kRing;
+        ok = __all_sync(0xFFFFFFFFu, ring_wait(region + 8 * r, static_cast<uint32_t>((j / kRing) & 1)));
+        if (!ok) break;
+        const int64_t slot = meta[2 * r];
+        if (slot >= 0) {
+            const uint32_t ks = slots + r * slot_bytes, vs = ks + rb, cs = vs + rb;
+            uint8_t *kdst = a.key_cache + slot * a.row_elems;
+            uint8_t *vdst = a.value_cache + slot * a.row_elems;
+            // the lane's units all start at the same dim of their head (head_dim divides 512)
+            const int d0 = (lane * 16) % a.head_dim;
+            const bool rotated = d0 < a.rot;
+            float c[16], sn[16];
+            if (rotated) {
+                const int ci = a.neox ? (d0 < half ? d0 : d0 - half) : d0 / 2;
+                const int nc = a.neox ? 16 : 8;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (4 * q < nc) {
+                        const float4 cv = lds16f(cs + 4 * (ci + 4 * q));
+                        const float4 sv4 = lds16f(cs + 4 * (half + ci + 4 * q));
+                        c[4 * q] = cv.x; c[4 * q + 1] = cv.y; c[4 * q + 2] = cv.z; c[4 * q + 3] = cv.w;
+                        sn[4 * q] = sv4.x; sn[4 * q + 1] = sv4.y; sn[4 * q + 2] = sv4.z; sn[4 * q + 3] = sv4.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int u = lane + 32 * q;
+                if (u < units) {
+                    float x[16];
+                    uint32_t w[8];
+                    lds_bf16x16(ks + 32 * u, x, w);
+                    if (rotated) {
+                        if (a.neox) {
+                            // first half: x*c - y*s; second half: y*s + x*c (= x*c + y*s exactly)
+                            const bool first = d0 < half;
+                            const int up = first ? u + (half >> 4) : u - (half >> 4);
+                            float y[16];
+                            uint32_t wy[8];
+                            lds_bf16x16(ks + 32 * up, y, wy);
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) {
+                                const uint64_t xc = mul2(pack2(x[i], x[i + 1]), pack2(c[i], c[i + 1]));
+                                const uint64_t ys = mul2(pack2(y[i], y[i + 1]), pack2(sn[i], sn[i + 1]));
+                                unpack2(first ? sub2(xc, ys) : add2(xc, ys), x[i], x[i + 1]);
+                            }
+                        } else {
+                            // pairs (p, q) = (x[2j], x[2j+1]): p' = p*c - q*s, q' = p*s + q*c
+#pragma unroll
+                            for (int jj = 0; jj < 8; jj += 2) {
+                                const uint64_t p = pack2(x[2 * jj], x[2 * jj + 2]);
+                                const uint64_t qq = pack2(x[2 * jj + 1], x[2 * jj + 3]);
+                                const uint64_t cc = pack2(c[jj], c[jj + 1]);
+                                const uint64_t ss = pack2(sn[jj], sn[jj + 1]);
+                                unpack2(sub2(mul2(p, cc), mul2(qq, ss)), x[2 * jj], x[2 * jj + 2]);
+                                unpack2(add2(mul2(p, ss), mul2(qq, cc)), x[2 * jj + 1], x[2 * jj + 3]);
+                            }
+                        }
+                    }
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        lo[i] = x[i];
+                        hi[i] = x[8 + i];
+                    }
+                    const uint2 c0 = quantize8<kFast>(lo, sk, fk, rotated ? sign_bytes(lo) : sign_bytes_bf16(w[0], w[1], w[2], w[3]));
+                    const uint2 c1 = quantize8<kFast>(hi, sk, fk, rotated ? sign_bytes(hi) : sign_bytes_bf16(w[4], w[5], w[6], w[7]));
+                    st_ef(kdst + 16 * u, make_uint4(c0.x, c0.y, c1.x, c1.y), pol);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < U; ++q) {
+                const int u = lane + 32 * q;
+                if (u < units) {
+                    float x[16];
+                    uint32_t w[8];
+                    lds_bf16x16(vs + 32 * u, x, w);
+                    float lo[8], hi[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        lo[i] = x[i];
+                        hi[i] = x[8 + i];
+                    }
+                    const uint2 c0 = quantize8<kFast>(lo, sv, fv, sign_bytes_bf16(w[0], w[1], w[2], w[3]));
+                    const uint2 c1 = quantize8<kFast>(hi, sv, fv, sign_bytes_bf16(w[4], w[5], w[6], w[7]));
+                    st_ef(vdst + 16 * u, make_uint4(c0.x, c0.y, c1.x, c1.y), pol);
+                }
+            }
+        }
+        __syncwarp();  // every lane is done reading slot r
+        if (lane == 0) {
+            const int64_t tn = t + (j + kRing) * W;
+            if (tn < T) {
+                // the slot's shared-memory reads (generic proxy) before the copies that
+                // overwrite it (async proxy)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(tn, r, nslot, npos);
+                ++issued;
+                nslot = slot_at(tn + W);
+                npos = pos_at(tn + W);
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        flag(a.status, KVFP8_DEV_TIMEOUT);
+        // let the copies still in flight land before the CTA's shared memory goes away
+        for (int k = j; k < issued; ++k) ring_wait(region + 8 * (k % kRing), static_cast<uint32_t>((k / kRing) & 1));
+    }
+}
+
+template <int U>
+__global__ void __launch_bounds__(kWarps * 32) rope_ring_kernel(const ReshapeArgs a) {
+    extern __shared__ __align__(128) uint8_t ring_smem[];
+    const float sk = load_scale(a.k_scale, a.scale_dtype);
+    const float sv = load_scale(a.v_scale, a.scale_dtype);
+    if (!scale_ok(sk) || !scale_ok(sv)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) flag(a.status, KVFP8_DEV_BAD_SCALE);
+        return;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    const int region_bytes = ring_region_bytes(a.row_elems, a.rot);
+    uint8_t *region_p = ring_smem + warp * region_bytes;
+    const uint32_t region = smem_u32(region_p);
+    if (fast_range(sk) && fast_range(sv))
+        ring_tokens<U, true>(a, region, region_p, t, W, lane, sk, sv);
+    else
+        ring_tokens<U, false>(a, region, region_p, t, W, lane, sk, sv);
+}
+
 // Any row length: one warp per row, groups streamed in rounds of 4 per lane.
 template <bool kF32>
 __global__ void __launch_bounds__(kWarps * 32) reshape_rowloop_kernel(const ReshapeArgs a) {
@@ -724,6 +997,13 @@ cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
 
 template <bool kF32>
 cudaError_t dispatch_rope(const ReshapeArgs &a, cudaStream_t stream) {
+    if (!kF32 && rope_ring_ok(a)) {
+        const size_t smem = static_cast<size_t>(kWarps) * ring_region_bytes(a.row_elems, a.rot);
+        const int units = (a.row_elems / 16 + 31) / 32;  // 16-element units per lane
+        if (units <= 1) return launch_persistent(rope_ring_kernel<1>, a, stream, a.num_tokens, smem);
+        if (units <= 2) return launch_persistent(rope_ring_kernel<2>, a, stream, a.num_tokens, smem);
+        return launch_persistent(rope_ring_kernel<4>, a, stream, a.num_tokens, smem);
+    }
     const int per_lane = (a.row_elems / 8 + 31) / 32;
     if (per_lane <= 1) return launch_persistent(rope_reshape_kernel<kF32, 1>, a, stream, a.num_tokens);
     if (per_lane <= 2) return launch_persistent(rope_reshape_kernel<kF32, 2>, a, stream, a.num_tokens);

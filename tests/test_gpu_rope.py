@@ -29,6 +29,8 @@ CASES = [  # n_kv, head_dim, rot, neox, src dtype, tokens
     (8, 256, 128, False, torch.bfloat16, 300),
     (1, 128, 16, True, torch.bfloat16, 64),
     (8, 128, 128, True, torch.float32, 600),
+    (16, 128, 128, True, torch.bfloat16, 500),   # 2048-element rows: four units a lane
+    (4, 128, 128, True, torch.bfloat16, 500),    # 512-element rows: one unit a lane
 ]
 
 
@@ -113,5 +115,36 @@ def test_rope_divide_paths(scales):
     vo = ko.copy()
     assert oracle.rope_reshape_and_cache(k, v, ko, vo, slots.numpy(), pos.numpy(), table, rot,
                                          True, bs, ks, vs) == 0
+    np.testing.assert_array_equal(kc.cpu().numpy(), ko)
+    np.testing.assert_array_equal(vc.cpu().numpy(), vo)
+
+
+def test_rope_special_values_bit_exact():
+    # NaN, infinities, values that overflow E4M3 after the divide, zeros of both signs and
+    # subnormal quotients, in K (rotated) and V; every byte against the oracle
+    n_kv, hd, rot, n = 8, 128, 128, 700
+    g = torch.Generator().manual_seed(5)
+    k = torch.randn(n, n_kv, hd, generator=g) * 3
+    v = torch.randn(n, n_kv, hd, generator=g) * 3
+    specials = torch.tensor([float("nan"), float("inf"), -float("inf"), 1e30, -1e30, 0.0, -0.0,
+                             1e-38, -3e-39, 448.0 * 0.05, 500.0])
+    for t in (k, v):
+        idx = torch.randint(0, t.numel(), (4000,), generator=g)
+        t.view(-1)[idx] = specials[torch.randint(0, specials.numel(), (4000,), generator=g)]
+    k, v = k.to(torch.bfloat16), v.to(torch.bfloat16)
+    pos = torch.randint(0, 4096, (n,), generator=g, dtype=torch.int64)
+    nb, bs = (n + 15) // 16 + 3, 16
+    slots = torch.randperm(nb * bs, generator=g)[:n].to(torch.int64)
+    table = _table(4096, rot)
+    kc = torch.full((nb, bs, n_kv, hd), 0x5A, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    kv.rope_reshape_and_cache(k.cuda(), v.cuda(), kc, vc, slots.cuda(), pos.cuda(),
+                              torch.from_numpy(table).cuda(), True,
+                              torch.tensor([0.05], device="cuda"), torch.tensor([0.04], device="cuda"))
+    torch.cuda.synchronize()
+    ko = np.full((nb, bs, n_kv, hd), 0x5A, np.uint8)
+    vo = ko.copy()
+    assert oracle.rope_reshape_and_cache(k, v, ko, vo, slots.numpy(), pos.numpy(), table, rot,
+                                         True, bs, 0.05, 0.04) == 0
     np.testing.assert_array_equal(kc.cpu().numpy(), ko)
     np.testing.assert_array_equal(vc.cpu().numpy(), vo)
