@@ -91,7 +91,7 @@ def test_prefill_against_oracle(case):
 
 
 @pytest.mark.parametrize("n_q,n_kv,hd,qlen", [(32, 8, 128, 5), (8, 2, 64, 40)],
-                         ids=["one_row_tile", "two_row_tiles"])
+                         ids=["20_rows", "160_rows"])
 def test_many_sequences_of_mixed_lengths_run_longest_first(n_q, n_kv, hd, qlen):
     # The CTAs take the sequences longest first, each CTA ranking every sequence's length
     # itself.  470 sequences are more than a CTA's 448 threads, so its lookup of the
@@ -114,6 +114,16 @@ def test_growing_scores_take_the_rescale_path():
     k_fn = lambda k, pos: (pos.float() * 0.03)[:, None, None].expand_as(k) + 0.1 * k  # noqa: E731
     out, ref = _run(32, 8, 128, 16, lengths, qlens, seed=7, k_fn=k_fn, q_fn=q_fn)
     gpu_util.assert_attention_close(out, ref, "rescale")
+
+
+def test_growing_scores_rescale_with_one_row_tile():
+    # 80 rows per kv head (prefill_kernel, one row tile of 64-key tiles): the rescale waits
+    # for the previous tile's O product through that tile's buffer release
+    lengths, qlens = [900, 300], [20, 11]
+    q_fn = lambda q: torch.ones_like(q)                                    # noqa: E731
+    k_fn = lambda k, pos: (pos.float() * 0.03)[:, None, None].expand_as(k) + 0.1 * k  # noqa: E731
+    out, ref = _run(32, 8, 128, 16, lengths, qlens, seed=8, k_fn=k_fn, q_fn=q_fn)
+    gpu_util.assert_attention_close(out, ref, "rescale, one row tile")
 
 
 def test_more_new_tokens_than_cached_are_flagged_and_give_zero_rows():
