@@ -637,29 +637,19 @@ __global__ void __launch_bounds__(kWarps * 32) rope_reshape_kernel(const Reshape
 // The rope write with its source rows staged in shared memory (bf16 sources, 16-element
 // units).  The kernel above keeps each warp's next rows in registers, and the rotation's
 // table values and temporaries take so many registers (117) that 16 warps fit an SM, with
-// about one row per warp in flight: too few bytes in flight to cover HBM latency.  Here
-// each warp owns a ring of kRing slots; a slot holds one token's K row and V row (the source
-// bytes as they are) and its table row, brought by three bulk copies (cp.async.bulk, issued
-// by one lane) that complete on the slot's mbarrier.  The copies run kRing tokens ahead of
-// the token the warp converts, so the bytes in flight are set by the ring, not by
-// registers.  A lane converts 16 consecutive elements, in two halves of 8 (64 registers),
-// and stores their codes with one 16-byte store; the NeoX partner unit and the table values
-// are read from shared memory, not shuffled or kept in registers.  Two slots a warp (74 KB a
-// CTA at 1024-element rows) let three CTAs, 24 warps, share an SM: measured against three
-// slots and two CTAs, 0.833 against 0.790 of the copy peak on llama3_8b.  The arithmetic,
-// and so every byte, is that of store_row_rope and store_row.
-constexpr int kRing = 2;
-// per warp: kRing mbarriers (8 bytes), then kRing (slot, position) pairs (16 bytes), padded
-// to 16 bytes so that the slots (bulk-copy destinations) start 16-byte aligned
-constexpr int kRingHeader = (kRing * (8 + 16) + 15) / 16 * 16;
-static_assert(kRingHeader >= 8 * kRing + 16 * kRing && kRingHeader % 16 == 0, "ring header");
-
-__host__ __device__ constexpr int ring_slot_bytes(int row_elems, int rot) {
-    return 2 * row_elems * 2 + rot * 4;  // K row, V row (bf16), table row (fp32)
-}
-__host__ __device__ constexpr int ring_region_bytes(int row_elems, int rot) {
-    return kRingHeader + kRing * ring_slot_bytes(row_elems, rot);
-}
+// about one row per warp in flight: too few bytes in flight to cover HBM latency, and too
+// few warps to cover the conversion's own latencies.  Here each warp owns two slots, one
+// for a token's K row (with its table row) and one for its V row, each filled by bulk copies
+// (cp.async.bulk, issued by one lane) that complete on the slot's own mbarrier: the next
+// token's K row is fetched while this token's V row is converted, and its V row while its K
+// row is.  A lane converts 16 consecutive elements, in two halves of 8 (64 registers), and
+// stores their codes with one 16-byte store; the NeoX partner unit and the table values are
+// read from shared memory, not shuffled or kept in registers.  A warp needs ~4.6 KB at
+// 1024-element rows, so four CTAs of 8 warps share an SM.  Measured on llama3_8b's rope
+// step (fraction of the copy peak): whole units, a ring of two or three tokens, 16 warps
+// per SM 0.790; half units, two tokens, 24 warps 0.818-0.833; these two row slots, 32 warps
+// 0.827 (0.818 for the 24-warp form on the same box), and on the shorter prefill write
+// 0.659 (0.635).  The arithmetic, and so every byte, is that of store_row_rope and store_row.
 
 __device__ __forceinline__ void ring_bar_init(uint32_t bar) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
@@ -706,17 +696,6 @@ __device__ __forceinline__ float4 lds16f(uint32_t addr) {
     const uint4 v = lds16(addr);
     return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
 }
-// 16 bf16 values (32 bytes of shared memory) -> floats, and the words themselves
-__device__ __forceinline__ void lds_bf16x16(uint32_t addr, float (&x)[16], uint32_t (&w)[8]) {
-    const uint4 a = lds16(addr), b = lds16(addr + 16);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        x[2 * i] = bf16lo(w[i]);
-        x[2 * i + 1] = bf16hi(w[i]);
-    }
-}
-
 // The staged path takes bf16 sources with rows of 16-element units, and NeoX rotations of
 // at least 32 dims (a unit and its partner then lie in different halves).
 bool rope_ring_ok(const ReshapeArgs &a) {
@@ -724,166 +703,200 @@ bool rope_ring_ok(const ReshapeArgs &a) {
            (!a.neox || a.rot >= 32);
 }
 
+// One K row of a staged token: rotate and encode the lane's units (the row's source at
+// shared-memory address ks, its table row at cs).
 template <int U, bool kFast>
-__device__ __forceinline__ void ring_tokens(const ReshapeArgs &a, uint32_t region, uint8_t *region_p,
-                                            int64_t t, int64_t W, int lane, float sk, float sv) {
+__device__ __forceinline__ void ring_k_row(const ReshapeArgs &a, uint32_t ks, uint32_t cs, uint8_t *kdst,
+                                           int lane, float sk, const FastDiv &fk, uint64_t pol) {
+    const int units = a.row_elems >> 4;
+    const int half = a.rot >> 1;
+    // the lane's units all start at the same dim of their head (head_dim divides 512)
+    const int d0 = (lane * 16) % a.head_dim;
+    const bool rotated = d0 < a.rot;
+    const bool first = d0 < half;
+    // NeoX: cos/sin of pairs ci.. (dims d0.. and their partners); GPT-J: of pairs d0/2..
+    const int ci = a.neox ? (first ? d0 : d0 - half) : d0 / 2;
+    const int step = half >> 4;  // units between a NeoX unit and its partner
+    // K: each unit in two halves of 8 elements (fewer values live at once), one
+    // 16-byte store of codes
+#pragma unroll 1
+    for (int q = 0; q < U; ++q) {
+        const int u = lane + 32 * q;
+        if (u >= units) break;
+        uint32_t code[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 wx = lds16(ks + 32 * u + 16 * h);
+            float x[8];
+            x[0] = bf16lo(wx.x); x[1] = bf16hi(wx.x); x[2] = bf16lo(wx.y); x[3] = bf16hi(wx.y);
+            x[4] = bf16lo(wx.z); x[5] = bf16hi(wx.z); x[6] = bf16lo(wx.w); x[7] = bf16hi(wx.w);
+            uint2 sg;
+            if (rotated) {
+                if (a.neox) {
+                    // first half: x*c - y*s; second half: y*s + x*c (= x*c + y*s exactly)
+                    const uint4 wy = lds16(ks + 32 * (first ? u + step : u - step) + 16 * h);
+                    const float y[8] = {bf16lo(wy.x), bf16hi(wy.x), bf16lo(wy.y), bf16hi(wy.y),
+                                        bf16lo(wy.z), bf16hi(wy.z), bf16lo(wy.w), bf16hi(wy.w)};
+                    const float4 c0 = lds16f(cs + 4 * (ci + 8 * h)), c1 = lds16f(cs + 4 * (ci + 8 * h + 4));
+                    const float4 s0 = lds16f(cs + 4 * (half + ci + 8 * h)), s1 = lds16f(cs + 4 * (half + ci + 8 * h + 4));
+                    const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+                    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const uint64_t xc = mul2(pack2(x[i], x[i + 1]), pack2(c[i], c[i + 1]));
+                        const uint64_t ys = mul2(pack2(y[i], y[i + 1]), pack2(sn[i], sn[i + 1]));
+                        unpack2(first ? sub2(xc, ys) : add2(xc, ys), x[i], x[i + 1]);
+                    }
+                } else {
+                    // pairs (p, q) = (x[2j], x[2j+1]): p' = p*c - q*s, q' = p*s + q*c
+                    const float4 cv = lds16f(cs + 4 * (ci + 4 * h));
+                    const float4 sv4 = lds16f(cs + 4 * (half + ci + 4 * h));
+                    const float c[4] = {cv.x, cv.y, cv.z, cv.w};
+                    const float sn[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+#pragma unroll
+                    for (int j = 0; j < 4; j += 2) {
+                        const uint64_t p = pack2(x[2 * j], x[2 * j + 2]);
+                        const uint64_t qq = pack2(x[2 * j + 1], x[2 * j + 3]);
+                        const uint64_t cc = pack2(c[j], c[j + 1]);
+                        const uint64_t ss = pack2(sn[j], sn[j + 1]);
+                        unpack2(sub2(mul2(p, cc), mul2(qq, ss)), x[2 * j], x[2 * j + 2]);
+                        unpack2(add2(mul2(p, ss), mul2(qq, cc)), x[2 * j + 1], x[2 * j + 3]);
+                    }
+                }
+                sg = sign_bytes(x);
+            } else {
+                sg = sign_bytes_bf16(wx.x, wx.y, wx.z, wx.w);
+            }
+            const uint2 cd = quantize8<kFast>(x, sk, fk, sg);
+            code[2 * h] = cd.x;
+            code[2 * h + 1] = cd.y;
+        }
+        st_ef(kdst + 16 * u, make_uint4(code[0], code[1], code[2], code[3]), pol);
+    }
+}
+
+// One V row of a staged token: encode the lane's units (source at shared-memory address vs).
+template <int U, bool kFast>
+__device__ __forceinline__ void ring_v_row(const ReshapeArgs &a, uint32_t vs, uint8_t *vdst, int lane,
+                                           float sv, const FastDiv &fv, uint64_t pol) {
+    const int units = a.row_elems >> 4;
+#pragma unroll 1
+    for (int q = 0; q < U; ++q) {
+        const int u = lane + 32 * q;
+        if (u >= units) break;
+        uint32_t code[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 wx = lds16(vs + 32 * u + 16 * h);
+            const float x[8] = {bf16lo(wx.x), bf16hi(wx.x), bf16lo(wx.y), bf16hi(wx.y),
+                                bf16lo(wx.z), bf16hi(wx.z), bf16lo(wx.w), bf16hi(wx.w)};
+            const uint2 cd = quantize8<kFast>(x, sv, fv, sign_bytes_bf16(wx.x, wx.y, wx.z, wx.w));
+            code[2 * h] = cd.x;
+            code[2 * h + 1] = cd.y;
+        }
+        st_ef(vdst + 16 * u, make_uint4(code[0], code[1], code[2], code[3]), pol);
+    }
+}
+
+constexpr int kRowHeader = 32;  // two mbarriers, then the K and V slots' cache slot indices
+__host__ __device__ constexpr int rowring_region_bytes(int row_elems, int rot) {
+    return kRowHeader + 2 * row_elems * 2 + rot * 4;
+}
+
+template <int U, bool kFast>
+__device__ __forceinline__ void ring_rows(const ReshapeArgs &a, uint32_t region, uint8_t *region_p,
+                                          int64_t t, int64_t W, int lane, float sk, float sv) {
     const FastDiv fk(sk), fv(sv);
     const uint64_t pol = evict_first_policy();
     const int64_t T = a.num_tokens;
     const int rb = a.row_elems * 2;                       // source row bytes
-    const uint32_t slot_bytes = static_cast<uint32_t>(ring_slot_bytes(a.row_elems, a.rot));
-    const uint32_t tx = slot_bytes;
-    volatile int64_t *meta = reinterpret_cast<volatile int64_t *>(region_p + 8 * kRing);
-    const uint32_t slots = region + kRingHeader;
-    const int units = a.row_elems >> 4;
-    const int half = a.rot >> 1;
+    const uint32_t bk = region, bv = region + 8;
+    volatile int64_t *meta = reinterpret_cast<volatile int64_t *>(region_p + 16);  // K slot, V slot
+    const uint32_t ks = region + kRowHeader, cs = ks + rb, vs = cs + a.rot * 4;
     const int64_t kstride = a.key_stride * 2, vstride = a.value_stride * 2;
     const uint8_t *kbase = static_cast<const uint8_t *>(a.key);
     const uint8_t *vbase = static_cast<const uint8_t *>(a.value);
-    // the first lane fetches token tok into slot r: its slot and position (read one token
-    // ahead, so the warp does not wait for them) are checked here; a token with nothing to
-    // store completes the slot's phase without copies
-    auto issue = [&](int64_t tok, int r, int64_t slot, int64_t pos) {
-        const bool ok = slot >= 0 && slot < a.num_slots && pos_ok(a, pos);
-        if (!ok && slot != -1) flag(a.status, KVFP8_DEV_BAD_SLOT);
-        meta[2 * r] = ok ? slot : -1;
-        meta[2 * r + 1] = pos;
-        const uint32_t bar = region + 8 * r;
-        if (ok) {
-            const uint32_t dst = slots + r * slot_bytes;
-            ring_arrive_tx(bar, tx);
-            bulk_g2s(dst, kbase + tok * kstride, rb, bar);
-            bulk_g2s(dst + rb, vbase + tok * vstride, rb, bar);
-            bulk_g2s(dst + 2 * rb, a.cos_sin + pos * a.rot, static_cast<uint32_t>(a.rot * 4), bar);
-        } else {
-            ring_arrive(bar);
-        }
-    };
-    int issued = 0;  // tokens fetched so far (this warp's j-th token is t + j*W)
     auto slot_at = [&](int64_t tok) -> int64_t { return tok < T ? __ldg(a.slot_mapping + tok) : -1; };
     auto pos_at = [&](int64_t tok) -> int64_t { return tok < T ? __ldg(a.positions + tok) : 0; };
-    int64_t nslot = -1, npos = 0;  // the next token to fetch (lane 0)
-    if (lane == 0) {
-        for (int r = 0; r < kRing; ++r) ring_bar_init(region + 8 * r);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int r = 0; r < kRing && t + r * W < T; ++r) {
-            issue(t + r * W, r, slot_at(t + r * W), pos_at(t + r * W));
-            ++issued;
+    // first lane: fetch token tok's K row and table row (its slot and position, read one
+    // token ahead, are checked here); returns the cache slot its rows go to, -1 for none, in
+    // which case the K slot's phase completes without copies
+    auto issue_k = [&](int64_t tok, int64_t slot, int64_t pos) -> int64_t {
+        const bool ok = slot >= 0 && slot < a.num_slots && pos_ok(a, pos);
+        if (!ok && slot != -1) flag(a.status, KVFP8_DEV_BAD_SLOT);
+        const int64_t st = ok ? slot : -1;
+        meta[0] = st;
+        if (ok) {
+            ring_arrive_tx(bk, static_cast<uint32_t>(rb + a.rot * 4));
+            bulk_g2s(ks, kbase + tok * kstride, rb, bk);
+            bulk_g2s(cs, a.cos_sin + pos * a.rot, static_cast<uint32_t>(a.rot * 4), bk);
+        } else {
+            ring_arrive(bk);
         }
-        nslot = slot_at(t + kRing * W);
-        npos = pos_at(t + kRing * W);
+        return st;
+    };
+    // first lane: fetch token tok's V row (st: its cache slot, -1 for none)
+    auto issue_v = [&](int64_t tok, int64_t st) {
+        meta[1] = st;
+        if (st >= 0) {
+            ring_arrive_tx(bv, static_cast<uint32_t>(rb));
+            bulk_g2s(vs, vbase + tok * vstride, rb, bv);
+        } else {
+            ring_arrive(bv);
+        }
+    };
+    int issued_k = 0, issued_v = 0, done_k = 0, done_v = 0;  // rows fetched / converted
+    int64_t nslot = -1, npos = 0;  // the next token's slot and position (first lane)
+    if (lane == 0) {
+        ring_bar_init(bk);
+        ring_bar_init(bv);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (t < T) {
+            const int64_t st = issue_k(t, slot_at(t), pos_at(t));
+            issue_v(t, st);
+            issued_k = issued_v = 1;
+        }
+        nslot = slot_at(t + W);
+        npos = pos_at(t + W);
     }
     __syncwarp();
     bool ok = true;
-    int j = 0;
-    for (; t + j * W < T; ++j) {
-        const int r = j % kRing;
-        ok = __all_sync(0xFFFFFFFFu, ring_wait(region + 8 * r, static_cast<uint32_t>((j / kRing) & 1)));
+    for (int j = 0; t + j * W < T; ++j) {
+        const int64_t tok = t + j * W;
+        const bool more = tok + W < T;
+        ok = __all_sync(0xFFFFFFFFu, ring_wait(bk, static_cast<uint32_t>(j & 1)));
         if (!ok) break;
-        const int64_t slot = meta[2 * r];
-        if (slot >= 0) {
-            const uint32_t ks = slots + r * slot_bytes, vs = ks + rb, cs = vs + rb;
-            uint8_t *kdst = a.key_cache + slot * a.row_elems;
-            uint8_t *vdst = a.value_cache + slot * a.row_elems;
-            // the lane's units all start at the same dim of their head (head_dim divides 512)
-            const int d0 = (lane * 16) % a.head_dim;
-            const bool rotated = d0 < a.rot;
-            const bool first = d0 < half;
-            // NeoX: cos/sin of pairs ci.. (dims d0.. and their partners); GPT-J: of pairs d0/2..
-            const int ci = a.neox ? (first ? d0 : d0 - half) : d0 / 2;
-            const int step = half >> 4;  // units between a NeoX unit and its partner
-            // K: each unit in two halves of 8 elements (fewer values live at once), one
-            // 16-byte store of codes
-#pragma unroll 1
-            for (int q = 0; q < U; ++q) {
-                const int u = lane + 32 * q;
-                if (u >= units) break;
-                uint32_t code[4];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 wx = lds16(ks + 32 * u + 16 * h);
-                    float x[8];
-                    x[0] = bf16lo(wx.x); x[1] = bf16hi(wx.x); x[2] = bf16lo(wx.y); x[3] = bf16hi(wx.y);
-                    x[4] = bf16lo(wx.z); x[5] = bf16hi(wx.z); x[6] = bf16lo(wx.w); x[7] = bf16hi(wx.w);
-                    uint2 sg;
-                    if (rotated) {
-                        if (a.neox) {
-                            // first half: x*c - y*s; second half: y*s + x*c (= x*c + y*s exactly)
-                            const uint4 wy = lds16(ks + 32 * (first ? u + step : u - step) + 16 * h);
-                            const float y[8] = {bf16lo(wy.x), bf16hi(wy.x), bf16lo(wy.y), bf16hi(wy.y),
-                                                bf16lo(wy.z), bf16hi(wy.z), bf16lo(wy.w), bf16hi(wy.w)};
-                            const float4 c0 = lds16f(cs + 4 * (ci + 8 * h)), c1 = lds16f(cs + 4 * (ci + 8 * h + 4));
-                            const float4 s0 = lds16f(cs + 4 * (half + ci + 8 * h)), s1 = lds16f(cs + 4 * (half + ci + 8 * h + 4));
-                            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                            const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-                            for (int i = 0; i < 8; i += 2) {
-                                const uint64_t xc = mul2(pack2(x[i], x[i + 1]), pack2(c[i], c[i + 1]));
-                                const uint64_t ys = mul2(pack2(y[i], y[i + 1]), pack2(sn[i], sn[i + 1]));
-                                unpack2(first ? sub2(xc, ys) : add2(xc, ys), x[i], x[i + 1]);
-                            }
-                        } else {
-                            // pairs (p, q) = (x[2j], x[2j+1]): p' = p*c - q*s, q' = p*s + q*c
-                            const float4 cv = lds16f(cs + 4 * (ci + 4 * h));
-                            const float4 sv4 = lds16f(cs + 4 * (half + ci + 4 * h));
-                            const float c[4] = {cv.x, cv.y, cv.z, cv.w};
-                            const float sn[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
-#pragma unroll
-                            for (int j = 0; j < 4; j += 2) {
-                                const uint64_t p = pack2(x[2 * j], x[2 * j + 2]);
-                                const uint64_t qq = pack2(x[2 * j + 1], x[2 * j + 3]);
-                                const uint64_t cc = pack2(c[j], c[j + 1]);
-                                const uint64_t ss = pack2(sn[j], sn[j + 1]);
-                                unpack2(sub2(mul2(p, cc), mul2(qq, ss)), x[2 * j], x[2 * j + 2]);
-                                unpack2(add2(mul2(p, ss), mul2(qq, cc)), x[2 * j + 1], x[2 * j + 3]);
-                            }
-                        }
-                        sg = sign_bytes(x);
-                    } else {
-                        sg = sign_bytes_bf16(wx.x, wx.y, wx.z, wx.w);
-                    }
-                    const uint2 cd = quantize8<kFast>(x, sk, fk, sg);
-                    code[2 * h] = cd.x;
-                    code[2 * h + 1] = cd.y;
-                }
-                st_ef(kdst + 16 * u, make_uint4(code[0], code[1], code[2], code[3]), pol);
-            }
-            // V: the same without the rotation
-#pragma unroll 1
-            for (int q = 0; q < U; ++q) {
-                const int u = lane + 32 * q;
-                if (u >= units) break;
-                uint32_t code[4];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 wx = lds16(vs + 32 * u + 16 * h);
-                    const float x[8] = {bf16lo(wx.x), bf16hi(wx.x), bf16lo(wx.y), bf16hi(wx.y),
-                                        bf16lo(wx.z), bf16hi(wx.z), bf16lo(wx.w), bf16hi(wx.w)};
-                    const uint2 cd = quantize8<kFast>(x, sv, fv, sign_bytes_bf16(wx.x, wx.y, wx.z, wx.w));
-                    code[2 * h] = cd.x;
-                    code[2 * h + 1] = cd.y;
-                }
-                st_ef(vdst + 16 * u, make_uint4(code[0], code[1], code[2], code[3]), pol);
-            }
+        ++done_k;
+        int64_t slot = meta[0];
+        if (slot >= 0) ring_k_row<U, kFast>(a, ks, cs, a.key_cache + slot * a.row_elems, lane, sk, fk, pol);
+        __syncwarp();  // every lane is done reading the K slot
+        int64_t next_v = -1;
+        if (lane == 0 && more) {
+            // the slot's shared-memory reads (generic proxy) before the copies that overwrite
+            // it (async proxy)
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            next_v = issue_k(tok + W, nslot, npos);
+            ++issued_k;
+            nslot = slot_at(tok + 2 * W);
+            npos = pos_at(tok + 2 * W);
         }
-        __syncwarp();  // every lane is done reading slot r
-        if (lane == 0) {
-            const int64_t tn = t + (j + kRing) * W;
-            if (tn < T) {
-                // the slot's shared-memory reads (generic proxy) before the copies that
-                // overwrite it (async proxy)
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(tn, r, nslot, npos);
-                ++issued;
-                nslot = slot_at(tn + W);
-                npos = pos_at(tn + W);
-            }
+        ok = __all_sync(0xFFFFFFFFu, ring_wait(bv, static_cast<uint32_t>(j & 1)));
+        if (!ok) break;
+        ++done_v;
+        slot = meta[1];
+        if (slot >= 0) ring_v_row<U, kFast>(a, vs, a.value_cache + slot * a.row_elems, lane, sv, fv, pol);
+        __syncwarp();  // every lane is done reading the V slot
+        if (lane == 0 && more) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_v(tok + W, next_v);
+            ++issued_v;
         }
     }
     if (!ok && lane == 0) {
         flag(a.status, KVFP8_DEV_TIMEOUT);
         // let the copies still in flight land before the CTA's shared memory goes away
-        for (int k = j; k < issued; ++k) ring_wait(region + 8 * (k % kRing), static_cast<uint32_t>((k / kRing) & 1));
+        for (int k = done_k; k < issued_k; ++k) ring_wait(bk, static_cast<uint32_t>(k & 1));
+        for (int k = done_v; k < issued_v; ++k) ring_wait(bv, static_cast<uint32_t>(k & 1));
     }
 }
 
@@ -899,13 +912,12 @@ __global__ void __launch_bounds__(kWarps * 32) rope_ring_kernel(const ReshapeArg
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t W = static_cast<int64_t>(gridDim.x) * kWarps;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-    const int region_bytes = ring_region_bytes(a.row_elems, a.rot);
-    uint8_t *region_p = ring_smem + warp * region_bytes;
+    uint8_t *region_p = ring_smem + warp * rowring_region_bytes(a.row_elems, a.rot);
     const uint32_t region = smem_u32(region_p);
     if (fast_range(sk) && fast_range(sv))
-        ring_tokens<U, true>(a, region, region_p, t, W, lane, sk, sv);
+        ring_rows<U, true>(a, region, region_p, t, W, lane, sk, sv);
     else
-        ring_tokens<U, false>(a, region, region_p, t, W, lane, sk, sv);
+        ring_rows<U, false>(a, region, region_p, t, W, lane, sk, sv);
 }
 
 // Any row length: one warp per row, groups streamed in rounds of 4 per lane.
@@ -1001,7 +1013,7 @@ cudaError_t dispatch(const ReshapeArgs &a, cudaStream_t stream) {
 template <bool kF32>
 cudaError_t dispatch_rope(const ReshapeArgs &a, cudaStream_t stream) {
     if (!kF32 && rope_ring_ok(a)) {
-        const size_t smem = static_cast<size_t>(kWarps) * ring_region_bytes(a.row_elems, a.rot);
+        const size_t smem = static_cast<size_t>(kWarps) * rowring_region_bytes(a.row_elems, a.rot);
         const int units = (a.row_elems / 16 + 31) / 32;  // 16-element units per lane
         if (units <= 1) return launch_persistent(rope_ring_kernel<1>, a, stream, a.num_tokens, smem);
         if (units <= 2) return launch_persistent(rope_ring_kernel<2>, a, stream, a.num_tokens, smem);
