@@ -31,6 +31,8 @@ CASES = [  # n_kv, head_dim, rot, neox, src dtype, tokens
     (8, 128, 128, True, torch.float32, 600),
     (16, 128, 128, True, torch.bfloat16, 500),   # 2048-element rows: four units a lane
     (4, 128, 128, True, torch.bfloat16, 500),    # 512-element rows: one unit a lane
+    (2, 64, 16, False, torch.bfloat16, 100),     # GPT-J over 16 dims: one rotated unit a head
+    (4, 64, 32, True, torch.bfloat16, 200),      # NeoX over 32 dims: partner one unit away
 ]
 
 
